@@ -1,0 +1,80 @@
+// Shared device helpers of the moestep library: types, reductions, error word.
+#pragma once
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "moestep.h"
+
+namespace moestep {
+
+using bf16 = __nv_bfloat16;
+
+// Bits of the device error word (kept in the workspace header).
+enum : int {
+    kErrTimeoutProducer = 1 << 0,
+    kErrTimeoutMma = 1 << 1,
+    kErrTimeoutEpilogue = 1 << 2,
+    kErrBadInput = 1 << 8,
+};
+
+template <typename T>
+__device__ __forceinline__ float to_f32(T v);
+template <>
+__device__ __forceinline__ float to_f32<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ float to_f32<bf16>(bf16 v) { return __bfloat162float(v); }
+
+template <typename T>
+__device__ __forceinline__ T from_f32(float v);
+template <>
+__device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ bf16 from_f32<bf16>(float v) { return __float2bfloat16_rn(v); }
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+// (value, index) maximum; equal values keep the lower index.
+__device__ __forceinline__ void warp_argmax(float& v, int& i) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+        float v2 = __shfl_xor_sync(0xffffffffu, v, o);
+        int i2 = __shfl_xor_sync(0xffffffffu, i, o);
+        if (v2 > v || (v2 == v && i2 < i)) { v = v2; i = i2; }
+    }
+}
+
+__device__ __forceinline__ void record_error(int* err, int bits) {
+    if (err) atomicOr(err, bits);
+}
+
+// Merge of softmax partials (m = max logit, a = its lowest index, s = sum exp(l - m)).
+struct SoftmaxPartial {
+    float m;
+    int a;
+    float s;
+};
+__device__ __forceinline__ SoftmaxPartial merge_partial(SoftmaxPartial x, SoftmaxPartial y) {
+    if (y.m == -INFINITY) return x;
+    if (x.m == -INFINITY) return y;
+    SoftmaxPartial r;
+    if (y.m > x.m || (y.m == x.m && y.a < x.a)) {
+        r.m = y.m;
+        r.a = y.a;
+    } else {
+        r.m = x.m;
+        r.a = x.a;
+    }
+    r.s = x.s * __expf(x.m - r.m) + y.s * __expf(y.m - r.m);
+    return r;
+}
+
+}  // namespace moestep

@@ -1,0 +1,108 @@
+// Host-side launch functions of the moestep kernels (one translation unit per
+// kernel family; api.cu validates arguments and calls these).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moestep {
+
+// ------------------------------------------------------------------ grouped tcgen05 GEMM
+enum GemmMode { kGateUp = 0, kDown = 1, kLmHead = 2 };
+
+struct GemmParams {
+    // expert modes: work plan written by the coreset kernel
+    const int* plan;       // [0] routed chunks, [1] shared chunks, [2] slots
+    const int4* chunks;    // {expert, first slot, slots, 0}; routed chunks first, then shared
+    int routed_tiles;      // M tiles per routed chunk
+    int shared_tiles;      // M tiles per shared chunk
+    int routed_kb;         // 64-wide K blocks per routed unit (LM head: per unit)
+    int shared_kb;         // 64-wide K blocks per shared unit
+    int rows_per_expert;   // rows of one routed expert in the A tensor
+    int tile_rows;         // row step between M tiles (128)
+    // LM head
+    int lm_chunks;         // position chunks
+    int lm_tiles;          // vocabulary tiles of 128 rows
+    int n_pos;             // positions (rows of B)
+    int V;
+    float scale;
+    float* pmax;           // [lm_tiles * 4][n_pos]: one partial per 32-row slice
+    int* parg;
+    float* psum;
+    float* logits;         // optional [n_pos][V]
+    // outputs of expert modes: act (bf16, gate/up) or y (fp32, down)
+    void* out;
+    int out_ld;
+    int* err;
+    unsigned long long timeout_ns;
+};
+
+// mapA0: routed weights (or LM head), mapA1: shared-expert weights, mapB: activations.
+cudaError_t launch_tc_gemm(int mode, int nch, const CUtensorMap& a0, const CUtensorMap& a1,
+                           const CUtensorMap& b, const GemmParams& p, int grid, cudaStream_t s);
+int tc_gemm_smem_bytes(int nch);
+
+// ------------------------------------------------------------------ routing / coreset / plan
+struct CoresetArgs {
+    int R, P, k, E, T;
+    const float* top_p;
+    const int32_t* idx;
+    const float* mass;
+    int32_t* n_sel;
+    int32_t* sel;
+    uint8_t* survive;
+    float* gate_rr;
+    int32_t* slot_of;   // [T][k]
+    int32_t* slot_sh;   // [T]
+    int32_t* slot_tok;  // [max slots]
+    int32_t* slot_exp;  // [max slots]
+    int4* chunks;
+    int* plan;
+    int* counter;
+    int nch;
+    int has_shared;
+    int* err;
+};
+
+cudaError_t launch_route(int dtype, const void* x, const void* Wr, int T, int H, int E, int k, float* logits,
+                         int32_t* idx, float* mass, float* gate, int* counters, int* err, cudaStream_t s);
+cudaError_t launch_topk_from_logits(const float* logits, int T, int E, int k, int32_t* idx, float* mass,
+                                    float* gate, cudaStream_t s);
+cudaError_t launch_coreset(const CoresetArgs& a, cudaStream_t s);
+int coreset_smem_bytes(int E, int T);
+cudaError_t launch_gather(int dtype, const void* x, int H, const int32_t* slot_tok, const int* plan,
+                          int max_slots, void* xp, cudaStream_t s);
+
+// ------------------------------------------------------------------ combine / norm / embed
+// mode 0: out = routed + shared; mode 1: h += routed + shared, x = RMSNorm(h); mode 2: h = h_in, x = RMSNorm(h)
+cudaError_t launch_combine(int mode, int dtype, int T, int H, int k, const float* y, const int32_t* slot_of,
+                           const int32_t* slot_sh, const float* gate_rr, int has_shared, const float* h_in,
+                           float* h, void* x, float* x_f32, float* out, cudaStream_t s);
+cudaError_t launch_embed(int dtype, int T, int H, int P, int V, const int32_t* tokens, const uint8_t* masked,
+                         const void* emb, const void* pos, int mask_id, float* h, cudaStream_t s);
+
+// ------------------------------------------------------------------ fp32 FFMA path
+// act[slot][i] = silu(gate_i . xp[slot]) * (up_i . xp[slot]) for the slot's expert (interleaved gate/up rows)
+cudaError_t launch_f32_gateup(int H, int E, int I, int Is, int max_slots, const float* xp, const int32_t* slot_exp,
+                              const int* plan, const float* Wgu, const float* Wsgu, float* act, int act_ld,
+                              cudaStream_t s);
+// y[slot][h] = Wd_e[h] . act[slot]
+cudaError_t launch_f32_down(int H, int E, int I, int Is, int max_slots, const float* act, int act_ld,
+                            const int32_t* slot_exp, const int* plan, const float* Wd, const float* Wsd, float* y,
+                            cudaStream_t s);
+cudaError_t launch_f32_lm_logits(int T, int H, int V, const float* hidden, const float* Wlm, float scale,
+                                 float* logits, cudaStream_t s);
+
+// ------------------------------------------------------------------ softmax partials / commit
+constexpr int kLogitTile = 2048;  // vocabulary entries per partial when reducing given logits
+cudaError_t launch_partials_from_logits(const float* logits, int T, int V, float* pmax, int* parg, float* psum,
+                                        cudaStream_t s);
+cudaError_t launch_commit(int R, int P, int n_tiles, const float* pmax, const int* parg, const float* psum,
+                          float threshold, int32_t* tokens, uint8_t* masked, int32_t* choice, float* conf,
+                          uint8_t* accept, int32_t* n_committed, cudaStream_t s);
+
+// ------------------------------------------------------------------ profiling hooks (api.cu)
+void prof_begin(int kid, cudaStream_t s);
+void prof_end(int kid, cudaStream_t s);
+
+}  // namespace moestep

@@ -1,0 +1,411 @@
+// Combine + residual + RMSNorm, block embedding, the fp32 FFMA path (router
+// aside) for fp32 weights, softmax partials of given logits, and the
+// LowConfidence commit.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moestep {
+namespace {
+
+constexpr float kRmsEps = 1e-6f;
+
+__device__ float block_sum_256(float v, float* red) {
+    v = warp_sum(v);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    float t = (threadIdx.x < 8) ? red[threadIdx.x] : 0.f;
+    if (warp == 0) t = warp_sum(t);
+    if (threadIdx.x == 0) red[8] = t;
+    __syncthreads();
+    return red[8];
+}
+
+template <typename T>
+__device__ __forceinline__ void store4(T* p, float4 v);
+template <>
+__device__ __forceinline__ void store4<float>(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+template <>
+__device__ __forceinline__ void store4<bf16>(bf16* p, float4 v) {
+    __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y);
+    __nv_bfloat162 b = __floats2bfloat162_rn(v.z, v.w);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&a);
+    u.y = *reinterpret_cast<uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(p) = u;
+}
+template <typename T>
+__device__ __forceinline__ float4 roundtrip4(float4 v) {
+    return v;
+}
+template <>
+__device__ __forceinline__ float4 roundtrip4<bf16>(float4 v) {
+    return make_float4(__bfloat162float(__float2bfloat16_rn(v.x)), __bfloat162float(__float2bfloat16_rn(v.y)),
+                       __bfloat162float(__float2bfloat16_rn(v.z)), __bfloat162float(__float2bfloat16_rn(v.w)));
+}
+
+// One CTA per token.  MODE 0: out = sum_j gate_rr*y[slot_j] + y[shared slot].
+// MODE 1: h += that; x = RMSNorm(h).  MODE 2: h = h_in; x = RMSNorm(h).
+// The routed terms are added in candidate order j = 0..k-1, then the shared one.
+template <typename T, int MODE>
+__global__ void __launch_bounds__(256) combine_kernel(int H, int k, const float* __restrict__ y,
+                                                      const int32_t* __restrict__ slot_of,
+                                                      const int32_t* __restrict__ slot_sh,
+                                                      const float* __restrict__ gate_rr, int has_shared,
+                                                      const float* __restrict__ h_in, float* __restrict__ h,
+                                                      T* __restrict__ x, float* __restrict__ x_f32,
+                                                      float* __restrict__ out) {
+    __shared__ int s_slot[33];
+    __shared__ float s_g[33];
+    __shared__ float red[9];
+    const int t = blockIdx.x;
+    if (MODE != 2) {
+        if (threadIdx.x < k) {
+            s_slot[threadIdx.x] = slot_of[t * k + threadIdx.x];
+            s_g[threadIdx.x] = gate_rr[t * k + threadIdx.x];
+        }
+        if (threadIdx.x == 32) s_slot[32] = has_shared ? slot_sh[t] : -1;
+        __syncthreads();
+    }
+    float ss = 0.f;
+    const size_t row = static_cast<size_t>(t) * H;
+    for (int c = threadIdx.x * 4; c < H; c += 1024) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (MODE != 2) {
+            for (int j = 0; j < k; ++j) {
+                const int sl = s_slot[j];
+                if (sl >= 0) {
+                    const float g = s_g[j];
+                    const float4 v = *reinterpret_cast<const float4*>(y + static_cast<size_t>(sl) * H + c);
+                    acc.x += g * v.x;
+                    acc.y += g * v.y;
+                    acc.z += g * v.z;
+                    acc.w += g * v.w;
+                }
+            }
+            if (s_slot[32] >= 0) {
+                const float4 v = *reinterpret_cast<const float4*>(y + static_cast<size_t>(s_slot[32]) * H + c);
+                acc.x += v.x;
+                acc.y += v.y;
+                acc.z += v.z;
+                acc.w += v.w;
+            }
+        }
+        if (MODE == 0) {
+            *reinterpret_cast<float4*>(out + row + c) = acc;
+        } else {
+            const float4 base = *reinterpret_cast<const float4*>((MODE == 1 ? h : h_in) + row + c);
+            const float4 v = make_float4(base.x + acc.x, base.y + acc.y, base.z + acc.z, base.w + acc.w);
+            *reinterpret_cast<float4*>(h + row + c) = v;
+            ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+        }
+    }
+    if (MODE == 0) return;
+    const float tot = block_sum_256(ss, red);
+    const float inv = 1.0f / sqrtf(tot / static_cast<float>(H) + kRmsEps);
+    for (int c = threadIdx.x * 4; c < H; c += 1024) {
+        const float4 v = *reinterpret_cast<const float4*>(h + row + c);
+        const float4 n = make_float4(v.x * inv, v.y * inv, v.z * inv, v.w * inv);
+        store4<T>(x + row + c, n);
+        if (x_f32 != nullptr) *reinterpret_cast<float4*>(x_f32 + row + c) = roundtrip4<T>(n);
+    }
+}
+
+// A committed token id outside [0, V) yields a NaN row instead of an out-of-range read.
+template <typename T>
+__global__ void __launch_bounds__(256) embed_kernel(int H, int P, int V, const int32_t* __restrict__ tokens,
+                                                    const uint8_t* __restrict__ masked, const T* __restrict__ emb,
+                                                    const T* __restrict__ pos, int mask_id, float* __restrict__ h) {
+    const int t = blockIdx.x;
+    const int id = masked[t] ? mask_id : tokens[t];
+    if (id < 0 || id >= V) {
+        for (int c = threadIdx.x; c < H; c += blockDim.x) h[static_cast<size_t>(t) * H + c] = __int_as_float(0x7fc00000);
+        return;
+    }
+    const T* er = emb + static_cast<size_t>(id) * H;
+    const T* pr = pos + static_cast<size_t>(t % P) * H;
+    for (int c = threadIdx.x; c < H; c += blockDim.x) h[static_cast<size_t>(t) * H + c] = to_f32(er[c]) + to_f32(pr[c]);
+}
+
+// ------------------------------------------------------------------ fp32 FFMA path
+__device__ __forceinline__ float dot_f32(const float* __restrict__ a, const float* __restrict__ b, int n) {
+    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+    for (int i = 0; i < n; i += 4) {
+        const float4 x = *reinterpret_cast<const float4*>(a + i);
+        const float4 w = *reinterpret_cast<const float4*>(b + i);
+        s0 = fmaf(x.x, w.x, s0);
+        s1 = fmaf(x.y, w.y, s1);
+        s2 = fmaf(x.z, w.z, s2);
+        s3 = fmaf(x.w, w.w, s3);
+    }
+    return (s0 + s1) + (s2 + s3);
+}
+
+__global__ void __launch_bounds__(256) f32_gateup_kernel(int H, int E, int I, int Is, int Imax, int max_slots,
+                                                         const float* __restrict__ xp, const int32_t* __restrict__ slot_exp,
+                                                         const int* __restrict__ plan, const float* __restrict__ Wgu,
+                                                         const float* __restrict__ Wsgu, float* __restrict__ act,
+                                                         int act_ld) {
+    const int n_slots = plan[2];
+    const long long total = static_cast<long long>(max_slots) * Imax;
+    for (long long g = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; g < total;
+         g += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int slot = static_cast<int>(g / Imax);
+        const int i = static_cast<int>(g - static_cast<long long>(slot) * Imax);
+        if (slot >= n_slots) break;
+        const int e = slot_exp[slot];
+        const float* grow;
+        if (e == E) {
+            if (i >= Is) continue;
+            grow = Wsgu + static_cast<size_t>(2 * i) * H;
+        } else {
+            if (i >= I) continue;
+            grow = Wgu + (static_cast<size_t>(e) * 2 * I + 2 * i) * H;
+        }
+        const float* xr = xp + static_cast<size_t>(slot) * H;
+        const float gv = dot_f32(grow, xr, H);
+        const float uv = dot_f32(grow + H, xr, H);
+        act[static_cast<size_t>(slot) * act_ld + i] = gv / (1.0f + expf(-gv)) * uv;
+    }
+}
+
+__global__ void __launch_bounds__(256) f32_down_kernel(int H, int E, int I, int Is, int max_slots,
+                                                       const float* __restrict__ act, int act_ld,
+                                                       const int32_t* __restrict__ slot_exp, const int* __restrict__ plan,
+                                                       const float* __restrict__ Wd, const float* __restrict__ Wsd,
+                                                       float* __restrict__ y) {
+    const int n_slots = plan[2];
+    const long long total = static_cast<long long>(max_slots) * H;
+    for (long long g = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; g < total;
+         g += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int slot = static_cast<int>(g / H);
+        const int hh = static_cast<int>(g - static_cast<long long>(slot) * H);
+        if (slot >= n_slots) break;
+        const int e = slot_exp[slot];
+        const float* ar = act + static_cast<size_t>(slot) * act_ld;
+        float v;
+        if (e == E)
+            v = dot_f32(Wsd + static_cast<size_t>(hh) * Is, ar, Is);
+        else
+            v = dot_f32(Wd + (static_cast<size_t>(e) * H + hh) * I, ar, I);
+        y[static_cast<size_t>(slot) * H + hh] = v;
+    }
+}
+
+__global__ void __launch_bounds__(256) f32_lm_logits_kernel(int T, int H, int V, const float* __restrict__ hidden,
+                                                            const float* __restrict__ Wlm, float scale,
+                                                            float* __restrict__ logits) {
+    const long long total = static_cast<long long>(T) * V;
+    for (long long g = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; g < total;
+         g += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int p = static_cast<int>(g / V);
+        const int v = static_cast<int>(g - static_cast<long long>(p) * V);
+        logits[g] = scale * dot_f32(Wlm + static_cast<size_t>(v) * H, hidden + static_cast<size_t>(p) * H, H);
+    }
+}
+
+// ------------------------------------------------------------------ softmax partials of given logits
+// grid (ceil(V / kLogitTile), T), 256 threads: (max, lowest argmax, sum exp(l - max)) of one tile.
+__global__ void __launch_bounds__(256) partials_kernel(const float* __restrict__ logits, int T, int V,
+                                                       float* __restrict__ pmax, int* __restrict__ parg,
+                                                       float* __restrict__ psum) {
+    __shared__ float sm[8];
+    __shared__ int sa[8];
+    __shared__ float red[9];
+    const int tile = blockIdx.x, p = blockIdx.y;
+    const float* row = logits + static_cast<size_t>(p) * V;
+    const int v0 = tile * kLogitTile;
+    const int v1 = min(V, v0 + kLogitTile);
+    float m = -INFINITY;
+    int a = 0x7fffffff;
+    for (int v = v0 + threadIdx.x; v < v1; v += 256) {
+        const float l = row[v];
+        if (l > m || a == 0x7fffffff) {
+            m = l;
+            a = v;
+        }
+    }
+    warp_argmax(m, a);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) {
+        sm[warp] = m;
+        sa[warp] = a;
+    }
+    __syncthreads();
+    float M = sm[0];
+    int Aidx = sa[0];
+    for (int w = 1; w < 8; ++w)
+        if (sm[w] > M || (sm[w] == M && sa[w] < Aidx)) {
+            M = sm[w];
+            Aidx = sa[w];
+        }
+    float s = 0.f;
+    for (int v = v0 + threadIdx.x; v < v1; v += 256) s += __expf(row[v] - M);
+    s = block_sum_256(s, red);
+    if (threadIdx.x == 0) {
+        const size_t o = static_cast<size_t>(tile) * T + p;
+        pmax[o] = M;
+        parg[o] = Aidx;
+        psum[o] = s;
+    }
+}
+
+// ------------------------------------------------------------------ LowConfidence commit
+// One CTA (1024 threads) per request.  Warps merge each position's partials
+// into conf = 1 / sum exp(l - max) and choice = lowest argmax; warp 0 then
+// commits every masked position with conf >= threshold, or, if there is none,
+// the masked position with the highest conf (lowest position on ties).
+__global__ void __launch_bounds__(1024) commit_kernel(int P, int T, int n_tiles, const float* __restrict__ pmax,
+                                                      const int* __restrict__ parg, const float* __restrict__ psum,
+                                                      float thr, int32_t* __restrict__ tokens,
+                                                      uint8_t* __restrict__ masked, int32_t* __restrict__ choice,
+                                                      float* __restrict__ conf, uint8_t* __restrict__ accept,
+                                                      int32_t* __restrict__ n_committed) {
+    __shared__ float s_conf[1024];
+    __shared__ int s_choice[1024];
+    const int r = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int pp = warp; pp < P; pp += 32) {
+        const int pos = r * P + pp;
+        SoftmaxPartial acc{-INFINITY, 0x7fffffff, 0.f};
+        for (int tl = lane; tl < n_tiles; tl += 32) {
+            const size_t o = static_cast<size_t>(tl) * T + pos;
+            acc = merge_partial(acc, SoftmaxPartial{pmax[o], parg[o], psum[o]});
+        }
+#pragma unroll
+        for (int off = 16; off; off >>= 1) {
+            SoftmaxPartial o;
+            o.m = __shfl_xor_sync(0xffffffffu, acc.m, off);
+            o.a = __shfl_xor_sync(0xffffffffu, acc.a, off);
+            o.s = __shfl_xor_sync(0xffffffffu, acc.s, off);
+            acc = merge_partial(acc, o);
+        }
+        if (lane == 0) {
+            s_conf[pp] = acc.s > 0.f ? 1.0f / acc.s : 0.f;
+            s_choice[pp] = acc.a;
+        }
+    }
+    __syncthreads();
+    if (warp != 0) return;
+    int any = 0;
+    for (int pp = lane; pp < P; pp += 32)
+        if (masked[r * P + pp] && s_conf[pp] >= thr) any = 1;
+    any = __any_sync(0xffffffffu, any);
+    int count = 0;
+    if (any) {
+        for (int pp = lane; pp < P; pp += 32) {
+            const int pos = r * P + pp;
+            const bool ok = masked[pos] && s_conf[pp] >= thr;
+            if (ok) {
+                tokens[pos] = s_choice[pp];
+                masked[pos] = 0;
+                ++count;
+            }
+            accept[pos] = ok ? 1 : 0;
+        }
+    } else {
+        float bv = -INFINITY;
+        int bp = 0x7fffffff;
+        for (int pp = lane; pp < P; pp += 32)
+            if (masked[r * P + pp] && (s_conf[pp] > bv || bp == 0x7fffffff)) {
+                bv = s_conf[pp];
+                bp = pp;
+            }
+        warp_argmax(bv, bp);
+        for (int pp = lane; pp < P; pp += 32) {
+            const int pos = r * P + pp;
+            const bool ok = (pp == bp);
+            if (ok) {
+                tokens[pos] = s_choice[pp];
+                masked[pos] = 0;
+                ++count;
+            }
+            accept[pos] = ok ? 1 : 0;
+        }
+    }
+    count = __reduce_add_sync(0xffffffffu, count);
+    if (lane == 0) n_committed[r] = count;
+    for (int pp = lane; pp < P; pp += 32) {
+        conf[r * P + pp] = s_conf[pp];
+        choice[r * P + pp] = s_choice[pp];
+    }
+}
+
+int grid_1d(long long work, int per_block = 256) {
+    long long g = (work + per_block - 1) / per_block;
+    if (g < 1) g = 1;
+    if (g > 4096) g = 4096;
+    return static_cast<int>(g);
+}
+
+}  // namespace
+
+cudaError_t launch_combine(int mode, int dtype, int T, int H, int k, const float* y, const int32_t* slot_of,
+                           const int32_t* slot_sh, const float* gate_rr, int has_shared, const float* h_in, float* h,
+                           void* x, float* x_f32, float* out, cudaStream_t s) {
+#define MOESTEP_COMBINE(TT, MM)                                                                                  \
+    combine_kernel<TT, MM><<<T, 256, 0, s>>>(H, k, y, slot_of, slot_sh, gate_rr, has_shared, h_in, h,          \
+                                             static_cast<TT*>(x), x_f32, out)
+    if (dtype == MOESTEP_BF16) {
+        if (mode == 0) MOESTEP_COMBINE(bf16, 0);
+        else if (mode == 1) MOESTEP_COMBINE(bf16, 1);
+        else MOESTEP_COMBINE(bf16, 2);
+    } else {
+        if (mode == 0) MOESTEP_COMBINE(float, 0);
+        else if (mode == 1) MOESTEP_COMBINE(float, 1);
+        else MOESTEP_COMBINE(float, 2);
+    }
+#undef MOESTEP_COMBINE
+    return cudaGetLastError();
+}
+
+cudaError_t launch_embed(int dtype, int T, int H, int P, int V, const int32_t* tokens, const uint8_t* masked,
+                         const void* emb, const void* pos, int mask_id, float* h, cudaStream_t s) {
+    if (dtype == MOESTEP_BF16)
+        embed_kernel<bf16><<<T, 256, 0, s>>>(H, P, V, tokens, masked, static_cast<const bf16*>(emb),
+                                             static_cast<const bf16*>(pos), mask_id, h);
+    else
+        embed_kernel<float><<<T, 256, 0, s>>>(H, P, V, tokens, masked, static_cast<const float*>(emb),
+                                              static_cast<const float*>(pos), mask_id, h);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_f32_gateup(int H, int E, int I, int Is, int max_slots, const float* xp, const int32_t* slot_exp,
+                              const int* plan, const float* Wgu, const float* Wsgu, float* act, int act_ld,
+                              cudaStream_t s) {
+    const int Imax = I > Is ? I : Is;
+    f32_gateup_kernel<<<grid_1d(static_cast<long long>(max_slots) * Imax), 256, 0, s>>>(
+        H, E, I, Is, Imax, max_slots, xp, slot_exp, plan, Wgu, Wsgu, act, act_ld);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_f32_down(int H, int E, int I, int Is, int max_slots, const float* act, int act_ld,
+                            const int32_t* slot_exp, const int* plan, const float* Wd, const float* Wsd, float* y,
+                            cudaStream_t s) {
+    f32_down_kernel<<<grid_1d(static_cast<long long>(max_slots) * H), 256, 0, s>>>(H, E, I, Is, max_slots, act,
+                                                                                   act_ld, slot_exp, plan, Wd, Wsd, y);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_f32_lm_logits(int T, int H, int V, const float* hidden, const float* Wlm, float scale,
+                                 float* logits, cudaStream_t s) {
+    f32_lm_logits_kernel<<<grid_1d(static_cast<long long>(T) * V), 256, 0, s>>>(T, H, V, hidden, Wlm, scale, logits);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_partials_from_logits(const float* logits, int T, int V, float* pmax, int* parg, float* psum,
+                                        cudaStream_t s) {
+    const dim3 grid((V + kLogitTile - 1) / kLogitTile, T);
+    partials_kernel<<<grid, 256, 0, s>>>(logits, T, V, pmax, parg, psum);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_commit(int R, int P, int n_tiles, const float* pmax, const int* parg, const float* psum,
+                          float threshold, int32_t* tokens, uint8_t* masked, int32_t* choice, float* conf,
+                          uint8_t* accept, int32_t* n_committed, cudaStream_t s) {
+    commit_kernel<<<R, 1024, 0, s>>>(P, R * P, n_tiles, pmax, parg, psum, threshold, tokens, masked, choice, conf,
+                                     accept, n_committed);
+    return cudaGetLastError();
+}
+
+}  // namespace moestep
