@@ -29,7 +29,8 @@
  *   - Returns MOESTEP_OK (0) or a negative MOESTEP_E* code.  Faults found on
  *     the device (an out-of-range index in fed input, a bounded wait that ran
  *     out) are recorded in the workspace's error word: read it with
- *     moestep_read_device_error().
+ *     moestep_read_device_error().  A new workspace is zeroed once with
+ *     moestep_workspace_init() before its first use.
  *   - Decisions taken on floating point are deterministic: top-k, expert
  *     ranking, argmax and the commit fallback break ties toward the lower
  *     index; coreset sums are exact integers.
@@ -99,6 +100,11 @@ typedef struct {
 /* Bytes of workspace needed by every entry point below for R requests
  * (T = R * P tokens).  *bytes (host) receives the size. */
 int moestep_workspace_size(const moestep_dims* dims, int R, size_t* bytes);
+
+/* Zero the workspace's header (device error word and counters), asynchronously
+ * on `stream`.  Call once on a new workspace before its first use; afterwards
+ * the error word is sticky until moestep_read_device_error() clears it. */
+int moestep_workspace_init(void* ws, size_t ws_bytes, void* stream);
 
 /* (a1) Router [AIT 四]; [GRM coreset section: each token picks its own top-k].
  * z = x Wr^T (fp32 accumulation), p = softmax(z) over E, idx = the k largest z
@@ -194,14 +200,17 @@ int moestep_read_device_error(void* ws, size_t ws_bytes, void* stream, int* word
 const char* moestep_error_string(int code);
 /* The last cudaError_t seen by the library on this host thread. */
 int moestep_last_cuda_error(void);
+/* Number of kernels this library has launched in this process. */
+long long moestep_launch_count(void);
 
 /* Kernel timing with CUDA events on the launching stream (host-side tool for
- * the benchmark).  While enabled, every kernel launch of the library is
- * bracketed by events; moestep_prof_read() synchronises and returns, per
- * kernel id, the number of launches and their summed duration in ms.
- * Kernel ids: 0 route, 1 coreset, 2 gather, 3 expert gate/up, 4 expert down,
- * 5 combine/norm, 6 LM head, 7 commit, 8 other.  Not thread-safe. */
-int moestep_prof_enable(int on);
+ * the benchmark).  Bit i of kernel_mask brackets every launch of kernel id i
+ * with events (0 turns timing off; enabling clears earlier records);
+ * moestep_prof_read() synchronises and returns, per kernel id, the number of
+ * timed launches and their summed duration in ms.  Kernel ids: 0 route,
+ * 1 coreset, 2 gather, 3 expert gate/up, 4 expert down, 5 combine/norm,
+ * 6 LM head, 7 commit, 8 other.  Not thread-safe. */
+int moestep_prof_enable(int kernel_mask);
 int moestep_prof_read(int kernel_id, int* launches, double* total_ms);
 #define MOESTEP_PROF_KERNELS 9
 

@@ -29,10 +29,10 @@ EDEVINPUT = -8
 PROF_KERNELS = ["route", "coreset", "gather", "expert_gateup", "expert_down", "combine", "lm_head", "commit", "other"]
 
 EXPORTS = [
-    "moestep_workspace_size", "moe_block_route", "moe_route_from_logits", "coreset_select", "moe_block_ffn",
+    "moestep_workspace_size", "moestep_workspace_init", "moe_block_route", "moe_route_from_logits", "coreset_select", "moe_block_ffn",
     "lm_head_commit", "lm_commit_from_logits", "block_embed", "block_decode_step", "moestep_read_device_error",
     "moestep_error_string", "moestep_last_cuda_error", "moestep_prof_enable", "moestep_prof_read",
-    "moestep_set_wait_timeout_ns",
+    "moestep_set_wait_timeout_ns", "moestep_launch_count",
 ]
 
 
@@ -72,6 +72,7 @@ def lib():
         D = ctypes.POINTER(Dims)
         sig = {
             "moestep_workspace_size": [D, i, ctypes.POINTER(sz)],
+            "moestep_workspace_init": [vp, sz, vp],
             "moe_block_route": [D, i, vp, vp, vp, vp, vp, vp, vp, sz, vp],
             "moe_route_from_logits": [D, i, vp, vp, vp, vp, vp, sz, vp],
             "coreset_select": [D, i, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp],
@@ -87,11 +88,13 @@ def lib():
             "moestep_prof_enable": [i],
             "moestep_prof_read": [i, ctypes.POINTER(i), ctypes.POINTER(ctypes.c_double)],
             "moestep_set_wait_timeout_ns": [ctypes.c_ulonglong],
+            "moestep_launch_count": [],
         }
         for name, args in sig.items():
             fn = getattr(L, name)
             fn.argtypes = args
-            fn.restype = ctypes.c_char_p if name == "moestep_error_string" else ctypes.c_int
+            fn.restype = {"moestep_error_string": ctypes.c_char_p,
+                          "moestep_launch_count": ctypes.c_longlong}.get(name, ctypes.c_int)
         _LIB = L
     return _LIB
 
@@ -149,9 +152,16 @@ def workspace_size(d: ModelDims, R: int) -> int:
     return n.value
 
 
-def workspace(d: ModelDims, R: int, device="cuda"):
+def workspace_init(ws, stream=None) -> None:
+    _check(lib().moestep_workspace_init(_p(ws), ws.numel(), _s(stream)), "moestep_workspace_init")
+
+
+def workspace(d: ModelDims, R: int, device="cuda", stream=None):
+    """Allocate (through torch) and initialise a workspace for R requests."""
     import torch
-    return torch.empty(workspace_size(d, R), dtype=torch.uint8, device=device)
+    ws = torch.empty(workspace_size(d, R), dtype=torch.uint8, device=device)
+    workspace_init(ws, stream)
+    return ws
 
 
 def moe_block_route(d: ModelDims, x, Wr, idx, mass, gate, ws, logits=None, stream=None) -> None:
@@ -215,8 +225,17 @@ def set_wait_timeout_ns(ns: int) -> None:
     _check(lib().moestep_set_wait_timeout_ns(int(ns)), "moestep_set_wait_timeout_ns")
 
 
-def prof_enable(on: bool) -> None:
-    _check(lib().moestep_prof_enable(1 if on else 0), "moestep_prof_enable")
+def prof_enable(kernels=None) -> None:
+    """Time the named kernels (None = all, [] = off) with CUDA events on their stream."""
+    names = PROF_KERNELS if kernels is None else list(kernels)
+    mask = 0
+    for n in names:
+        mask |= 1 << PROF_KERNELS.index(n)
+    _check(lib().moestep_prof_enable(mask), "moestep_prof_enable")
+
+
+def launch_count() -> int:
+    return int(lib().moestep_launch_count())
 
 
 def prof_read() -> dict:

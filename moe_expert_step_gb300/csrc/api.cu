@@ -8,6 +8,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include <vector>
 
@@ -60,7 +61,7 @@ Layout make_layout(const moestep_dims& d, int R) {
         o = align_up(o + (bytes ? bytes : 1), 256);
         return at;
     };
-    L.hdr = take(256);  // int[0]: error word, int[4..6]: expert work plan
+    L.hdr = take(256);  // int[0]: error word, int[8..15]: where a wait timed out, int[32..34]: expert work plan
     L.counters_bytes = sizeof(int) * (L.route_groups + 1);
     L.counters = take(L.counters_bytes);
     L.logits = take(sizeof(float) * T * d.E);
@@ -183,8 +184,10 @@ int make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uin
 }
 
 // ---------------------------------------------------------------------------- timing
+std::atomic<long long> g_launches{0};
+
 struct Prof {
-    bool on = false;
+    int mask = 0;
     std::vector<cudaEvent_t> pool;
     size_t next = 0;
     cudaEvent_t pending[MOESTEP_PROF_KERNELS] = {};
@@ -210,15 +213,16 @@ struct Ctx {
     int sms;
 };
 
-#define MOESTEP_LAUNCH(kid, call)          \
-    do {                                   \
-        prof_begin((kid), c.s);            \
-        cudaError_t e_ = (call);           \
-        prof_end((kid), c.s);              \
-        if (e_ != cudaSuccess) {           \
+#define MOESTEP_LAUNCH(kid, call)               \
+    do {                                        \
+        prof_begin((kid), c.s);                 \
+        cudaError_t e_ = (call);                \
+        prof_end((kid), c.s);                   \
+        if (e_ != cudaSuccess) {                \
             g_last_cuda = static_cast<int>(e_); \
-            return MOESTEP_ECUDA;          \
-        }                                  \
+            return MOESTEP_ECUDA;               \
+        }                                       \
+        g_launches.fetch_add(1);                \
     } while (0)
 
 int run_route(const Ctx& c, int T, const void* x, const void* Wr, int32_t* idx, float* mass, float* gate,
@@ -251,7 +255,7 @@ int run_coreset(const Ctx& c, int R, const float* top_p, const int32_t* idx, con
     a.slot_tok = at<int32_t>(c.ws, c.L.slot_tok);
     a.slot_exp = at<int32_t>(c.ws, c.L.slot_exp);
     a.chunks = at<int4>(c.ws, c.L.chunks);
-    a.plan = at<int>(c.ws, c.L.hdr) + 4;
+    a.plan = at<int>(c.ws, c.L.hdr) + 32;
     a.counter = at<int>(c.ws, c.L.counters) + c.L.route_groups;
     a.nch = c.L.nch;
     a.has_shared = d->Is > 0;
@@ -264,7 +268,7 @@ int run_coreset(const Ctx& c, int R, const float* top_p, const int32_t* idx, con
 int run_experts(const Ctx& c, int R, const void* x, const moestep_layer* layer) {
     const moestep_dims* d = c.d;
     const Layout& L = c.L;
-    const int* plan = at<int>(c.ws, L.hdr) + 4;
+    const int* plan = at<int>(c.ws, L.hdr) + 32;
     MOESTEP_LAUNCH(2, launch_gather(d->dtype, x, d->H, at<int32_t>(c.ws, L.slot_tok), plan, L.max_slots,
                                     at<void>(c.ws, L.xp), c.s));
     if (d->dtype == MOESTEP_F32) {
@@ -370,13 +374,13 @@ bool thr_ok(float t) { return t > 0.f && t <= 1.f; }
 }  // namespace
 
 void prof_begin(int kid, cudaStream_t s) {
-    if (!g_prof.on || kid < 0 || kid >= MOESTEP_PROF_KERNELS) return;
+    if (kid < 0 || kid >= MOESTEP_PROF_KERNELS || !((g_prof.mask >> kid) & 1)) return;
     cudaEvent_t e = prof_event();
     if (e && cudaEventRecord(e, s) == cudaSuccess) g_prof.pending[kid] = e;
 }
 
 void prof_end(int kid, cudaStream_t s) {
-    if (!g_prof.on || kid < 0 || kid >= MOESTEP_PROF_KERNELS || !g_prof.pending[kid]) return;
+    if (kid < 0 || kid >= MOESTEP_PROF_KERNELS || !((g_prof.mask >> kid) & 1) || !g_prof.pending[kid]) return;
     cudaEvent_t e = prof_event();
     if (e && cudaEventRecord(e, s) == cudaSuccess) {
         g_prof.kid.push_back(kid);
@@ -403,6 +407,12 @@ int moestep_workspace_size(const moestep_dims* dims, int R, size_t* bytes) {
     MOESTEP_TRY(check_R(dims, R));
     if (bytes == nullptr) return MOESTEP_EINVAL;
     *bytes = make_layout(*dims, R).total;
+    return MOESTEP_OK;
+}
+
+int moestep_workspace_init(void* ws, size_t ws_bytes, void* stream) {
+    if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < 512) return MOESTEP_EWORKSPACE;
+    MOESTEP_CK(cudaMemsetAsync(ws, 0, 512, static_cast<cudaStream_t>(stream)));
     return MOESTEP_OK;
 }
 
@@ -436,6 +446,7 @@ int moe_route_from_logits(const moestep_dims* dims, int T, const float* logits, 
     cudaError_t e = launch_topk_from_logits(logits, T, dims->E, dims->k, idx, mass, gate, s);
     prof_end(0, s);
     MOESTEP_CK(e);
+    g_launches.fetch_add(1);
     return MOESTEP_OK;
 }
 
@@ -569,7 +580,7 @@ int moestep_read_device_error(void* ws, size_t ws_bytes, void* stream, int* word
     int bits = 0;
     MOESTEP_CK(cudaMemcpyAsync(&bits, ws, sizeof(int), cudaMemcpyDeviceToHost, s));
     MOESTEP_CK(cudaStreamSynchronize(s));
-    MOESTEP_CK(cudaMemsetAsync(ws, 0, sizeof(int), s));
+    MOESTEP_CK(cudaMemsetAsync(ws, 0, 16 * sizeof(int), s));
     *word = (bits & 0xff) ? MOESTEP_ETIMEOUT : (bits ? MOESTEP_EDEVINPUT : MOESTEP_OK);
     return MOESTEP_OK;
 }
@@ -591,9 +602,11 @@ const char* moestep_error_string(int code) {
 
 int moestep_last_cuda_error(void) { return g_last_cuda; }
 
-int moestep_prof_enable(int on) {
-    g_prof.on = on != 0;
-    if (g_prof.on) {
+long long moestep_launch_count(void) { return g_launches.load(); }
+
+int moestep_prof_enable(int kernel_mask) {
+    g_prof.mask = kernel_mask & ((1 << MOESTEP_PROF_KERNELS) - 1);
+    if (g_prof.mask) {
         g_prof.next = 0;
         g_prof.kid.clear();
         g_prof.start.clear();

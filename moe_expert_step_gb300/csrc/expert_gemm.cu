@@ -96,6 +96,22 @@ __device__ __forceinline__ Unit decode_unit(int u, const GemmParams& p, int nrc)
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
 
+// Where a bounded wait gave up: the first CTA to time out writes
+// {role, block, unit, k-block, stage, phase, units, tokens} after the error word.
+__device__ __forceinline__ void record_timeout(int* err, int role, int u, int kb, int stage, uint32_t phase,
+                                               int n_units, int n) {
+    if (err == nullptr) return;
+    if (atomicCAS(err + 8, 0, role) == 0) {
+        err[9] = blockIdx.x;
+        err[10] = u;
+        err[11] = kb;
+        err[12] = stage;
+        err[13] = static_cast<int>(phase);
+        err[14] = n_units;
+        err[15] = n;
+    }
+}
+
 template <int MODE, int NCH>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA0, const __grid_constant__ CUtensorMap mapA1,
@@ -185,6 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 good = __shfl_sync(0xffffffffu, good, 0);
                 if (!good) {
                     ok = false;
+                    if (lane == 0) record_timeout(p.err, 1, u, kb, stage, phase, n_units, w.n);
                     break;
                 }
                 if (++stage == STAGES) {
@@ -221,6 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             good = __shfl_sync(0xffffffffu, good, 0);
             if (!good) {
                 ok = false;
+                if (lane == 0) record_timeout(p.err, 2, u, -1, buf, aph, n_units, w.n);
                 break;
             }
             tc::fence_after_sync();
@@ -242,6 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 good = __shfl_sync(0xffffffffu, good, 0);
                 if (!good) {
                     ok = false;
+                    if (lane == 0) record_timeout(p.err, 3, u, kb, stage, phase, n_units, w.n);
                     break;
                 }
                 if (++stage == STAGES) {
@@ -277,6 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) {
                     *abort_flag = 1;
                     record_error(p.err, kErrTimeoutEpilogue);
+                    record_timeout(p.err, 4 + sp, u, -1, buf, aph, n_units, w.n);
                 }
                 break;
             }

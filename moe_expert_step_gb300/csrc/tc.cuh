@@ -44,18 +44,29 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Wait for the phase of `parity` to complete, giving up after `limit_ns` or
-// when *abort becomes non-zero.  Returns false if it gave up.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Wait for the phase of `parity` to complete, giving up once `limit_ns` have
+// passed or *abort is non-zero.  The first probe does not block; the clock and
+// the abort flag are checked before every blocking probe, so a limit of 0
+// gives up on any phase that is not already complete.  Returns false if it gave up.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           uint64_t limit_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_test_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
-    for (uint32_t n = 1;; ++n) {
+    for (;;) {
+        if (*abort) return false;
+        if (globaltimer_ns() - t0 >= limit_ns) return false;
         if (mbar_try_wait(bar, parity)) return true;
-        if ((n & 255u) == 0) {
-            if (*abort) return false;
-            if (globaltimer_ns() - t0 > limit_ns) return false;
-        }
     }
 }
 

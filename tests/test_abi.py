@@ -21,7 +21,7 @@ def L():
 def header_functions():
     text = open(os.path.join(ROOT, "include", "moestep.h")).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:int|const char\s*\*)\s+(\w+)\s*\(", text, flags=re.M)))
+    return sorted(set(re.findall(r"^\s*(?:int|long long|const char\s*\*)\s+(\w+)\s*\(", text, flags=re.M)))
 
 
 def test_every_declared_symbol_is_exported(L):
