@@ -1,0 +1,454 @@
+#!/usr/bin/env python
+"""Benchmark of one block-diffusion denoising step on GB300.
+
+A step is one full pass of the hot path over one 32-token block per request:
+for each of the 40 MoE layers x = RMSNorm(h), router top-8 of 256, block
+coreset (top_p 0.9), routed + shared SwiGLU experts, h += out; then RMSNorm,
+LM head (V = 152064) and the LowConfidence commit (threshold 0.95).  That is
+one call of block_decode_step.  Inputs (64.4 GB of bf16 expert weights, the
+LM head, the block's residual stream) are resident in HBM before the timed
+region; every step streams the selected experts' weights from HBM (the
+weights are far larger than L2).
+
+Prints one JSON line (rank 0).  --impl reference times the CPU oracle on a
+bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "block-steps/s (40-layer MoE, B=32) & expert-weight HBM GB/s vs peak; tokens/step"
+UNIT = "block-steps/s"
+THRESHOLD = 0.95
+TOP_P = 0.9
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gpu", "reference"], default="gpu")
+    ap.add_argument("--config", choices=["clover_stack40", "clover_layer"], default="clover_stack40")
+    ap.add_argument("--requests", type=int, default=1, help="concurrent requests (blocks) per GPU")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------------------------------ distributed
+class Dist:
+    def __init__(self, backend: str):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, v: float) -> float:
+        if not self.pg:
+            return v
+        import torch
+        dev = "cuda" if self.pg.get_backend() == "nccl" else "cpu"
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# ------------------------------------------------------------------------------------------ clocks
+class Clocks:
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "100", "-i", gpu_id], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        self.t0 = self.t1 = None
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def result(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = []
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(f[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                rows.append((ts, float(f[2]), float(f[3]), f[5], f[6], f[7], f[8], f[9]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if self.t0 is not None and self.t0 - 1 <= r[0] <= self.t1 + 1]
+        use = inside or rows
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in use:
+            for name, v in zip(names, r[4:]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r[1] for r in use) if use else None,
+                "sm_max_mhz": max(r[2] for r in use) if use else None,
+                "reasons": sorted(reasons), "samples": len(use),
+                "window": "timed region" if inside else "whole run"}
+
+
+# ------------------------------------------------------------------------------------------ workload
+def workload(name: str):
+    from synth import workloads as W
+    return W.CONFIGS[name]
+
+
+def workload_desc(cfg, R: int) -> dict:
+    return {"workload": f"{cfg.name}: {cfg.n_layers}-layer MoE FFN stack (H={cfg.H}, {cfg.E} routed experts top-{cfg.k}, "
+                        f"expert/shared SwiGLU I={cfg.I}, 1 shared expert, bf16 weights, fp32 accumulate), "
+                        f"block of {cfg.P} tokens x {R} request(s), coreset top_p {TOP_P}, RMSNorm eps 1e-6 "
+                        f"between layers, LM head V={cfg.V}, LowConfidence commit threshold {THRESHOLD}",
+            "layers": cfg.n_layers, "block_tokens": cfg.P, "requests": R, "top_p": TOP_P,
+            "threshold": THRESHOLD, "vocab": cfg.V,
+            "l2": "inputs larger than L2: every step streams the selected experts' weights (tens of GB) from HBM",
+            "parallelism": "replicas (one independent block step per GPU)"}
+
+
+def expert_bytes(cfg, unions) -> dict:
+    """Algorithmic HBM bytes of one step: each selected expert's weights once, shared experts,
+    routers and the LM head."""
+    per_expert = 3 * cfg.I * cfg.H * 2
+    shared = 3 * cfg.Is * cfg.H * 2
+    experts = sum(unions) * per_expert + cfg.n_layers * shared
+    return {"expert_weights": experts, "router": cfg.n_layers * cfg.E * cfg.H * 2, "lm_head": cfg.V * cfg.H * 2,
+            "per_expert": per_expert, "shared_per_layer": shared}
+
+
+# ------------------------------------------------------------------------------------------ GPU arm
+def run_gpu(args, dist: Dist):
+    import numpy as np
+    import torch
+
+    import moe_expert_step_gb300 as ms
+    from synth import workloads as W
+
+    torch.cuda.set_device(dist.local)
+    cfg = workload(args.config)
+    R = args.requests
+    T = R * cfg.P
+    d = ms.ModelDims(H=cfg.H, E=cfg.E, k=cfg.k, I=cfg.I, Is=cfg.Is, V=cfg.V, P=cfg.P, dtype=ms.BF16)
+    t_setup = time.time()
+    layers_t = [W.device_layer(cfg, l) for l in range(cfg.n_layers)]
+    layers = [ms.layer(l["Wr"], l["Wgu"], l["Wd"], l["Wsgu"], l["Wsd"]) for l in layers_t]
+    Wlm = W.device_lm_head(cfg)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    h0_host = W.host_h0(cfg, R)
+    masked_host = W.masked_subset(cfg, R).astype(np.uint8)
+    h0 = dev(h0_host)
+    tokens0 = torch.zeros(T, dtype=torch.int32, device="cuda")
+    masked0 = dev(masked_host)
+    top_p = torch.full((R,), TOP_P, dtype=torch.float32, device="cuda")
+    tokens, masked = tokens0.clone(), masked0.clone()
+    choice = torch.zeros(T, dtype=torch.int32, device="cuda")
+    conf = torch.zeros(T, dtype=torch.float32, device="cuda")
+    accept = torch.zeros(T, dtype=torch.uint8, device="cuda")
+    n_comm = torch.zeros(R, dtype=torch.int32, device="cuda")
+    ws = ms.workspace(d, R)
+    torch.cuda.synchronize()
+    t_setup = time.time() - t_setup
+
+    def step(h_in=h0, trace=None):
+        tokens.copy_(tokens0)
+        masked.copy_(masked0)
+        kw = trace or {}
+        ms.block_decode_step(d, R, layers, Wlm, top_p, THRESHOLD, h_in, tokens, masked, choice, conf, accept, n_comm,
+                             ws, **kw)
+
+    # one traced step: per-layer coreset sizes and the union of kept experts
+    n_sel = torch.zeros((cfg.n_layers, R), dtype=torch.int32, device="cuda")
+    sel = torch.zeros((cfg.n_layers, R, cfg.E), dtype=torch.int32, device="cuda")
+    step(trace=dict(trace_n_sel=n_sel, trace_sel=sel))
+    torch.cuda.synchronize()
+    if ms.read_device_error(ws) != ms.OK:
+        raise RuntimeError("device error word set after the traced step")
+    n_sel_h, sel_h = n_sel.cpu().numpy(), sel.cpu().numpy()
+    unions = [len(set().union(*[set(sel_h[l, r, :n_sel_h[l, r]].tolist()) for r in range(R)]))
+              for l in range(cfg.n_layers)]
+    committed_per_step = int(n_comm.sum().item())
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.current_stream()
+    clocks = Clocks("GPU-" + str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid))
+    time.sleep(0.3)
+    # ---------------- timed region (device clock)
+    dist.barrier()
+    torch.cuda.synchronize()
+    launches0 = ms.launch_count()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks.mark_start()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clocks.mark_end()
+    dist.barrier()
+    launches = ms.launch_count() - launches0
+    ms_total = dist.max(e0.elapsed_time(e1))
+    clk = clocks.result()
+
+    # ---------------- roofline pass: events around the expert and LM-head kernels on their stream
+    ms.prof_enable(["expert_gateup", "expert_down", "lm_head"])
+    for _ in range(args.steps):
+        step()
+    torch.cuda.synchronize()
+    prof = ms.prof_read()
+    ms.prof_enable([])
+
+    # ---------------- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        h_pin = torch.from_numpy(h0_host).pin_memory()
+        m_pin = torch.from_numpy(masked_host).pin_memory()
+        t_pin = torch.zeros(T, dtype=torch.int32).pin_memory()
+        tp_pin = torch.full((R,), TOP_P, dtype=torch.float32).pin_memory()
+        out_tok = torch.zeros(T, dtype=torch.int32).pin_memory()
+        out_msk = torch.zeros(T, dtype=torch.uint8).pin_memory()
+        out_n = torch.zeros(R, dtype=torch.int32).pin_memory()
+        h_dev = torch.empty_like(h0)
+
+        def e2e_step():
+            h_dev.copy_(h_pin, non_blocking=True)
+            tokens.copy_(t_pin, non_blocking=True)
+            masked.copy_(m_pin, non_blocking=True)
+            top_p.copy_(tp_pin, non_blocking=True)
+            ms.block_decode_step(d, R, layers, Wlm, top_p, THRESHOLD, h_dev, tokens, masked, choice, conf, accept,
+                                 n_comm, ws)
+            out_tok.copy_(tokens, non_blocking=True)
+            out_msk.copy_(masked, non_blocking=True)
+            out_n.copy_(n_comm, non_blocking=True)
+            stream.synchronize()
+
+        for _ in range(3):
+            e2e_step()
+        dist.barrier()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            e2e_step()
+        t_e2e = dist.max(time.perf_counter() - t0)
+        dist.barrier()
+        h2d = h_pin.numel() * 4 + m_pin.numel() + t_pin.numel() * 4 + tp_pin.numel() * 4
+        d2h = out_tok.numel() * 4 + out_msk.numel() + out_n.numel() * 4
+        e2e = {"value": dist.world * args.steps / t_e2e, "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h,
+               "how": "wall clock over K public-API calls (Python binding -> C ABI), each with pinned H2D inputs, "
+                      "the step, D2H of tokens/masked/n_committed and a stream synchronize"}
+    if ms.read_device_error(ws) != ms.OK:
+        raise RuntimeError("device error word set during the benchmark")
+
+    ms_step = ms_total / args.steps
+    value = dist.world * args.steps / (ms_total / 1e3)
+    eb = expert_bytes(cfg, unions)
+    step_bytes = eb["expert_weights"] + eb["router"] + eb["lm_head"]
+    peaks = load_peaks()
+    hbm_peak = peaks.get("hbm_gbs")
+    # dominant kernel: expert gate/up (2/3 of the weight bytes)
+    gu_n, gu_ms = prof["expert_gateup"]
+    dn_n, dn_ms = prof["expert_down"]
+    steps_prof = args.steps
+    # per gate/up launch: the kept experts' and the shared expert's gate/up weights once, plus the
+    # gathered activations read and the SwiGLU output written (at most T*(k+1) token slots)
+    gu_weights = sum(u * 2 * cfg.I * cfg.H * 2 for u in unions) + cfg.n_layers * 2 * cfg.Is * cfg.H * 2
+    gu_act = cfg.n_layers * T * (cfg.k + 1) * (cfg.H + cfg.I) * 2
+    gu_bytes_launch = (gu_weights + gu_act) / cfg.n_layers
+    gu_avg_ms = gu_ms / max(1, gu_n)
+    achieved = gu_bytes_launch / (gu_avg_ms / 1e3) / 1e9
+    roofline = {"kernel": "tc_gemm_kernel<gate/up> (expert gate/up projections + SwiGLU)",
+                "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                "frac": round(achieved / hbm_peak, 4) if hbm_peak else None, "traffic": load_traffic(),
+                "peak_source": peaks.get("source"),
+                "bytes_per_launch": int(gu_bytes_launch), "avg_launch_ms": round(gu_avg_ms, 5),
+                "launches_timed": gu_n}
+    expert_stream_ms = (gu_ms + dn_ms) / steps_prof
+    step_gbs = step_bytes / (ms_step / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": dist.world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": round(ms_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": workload_desc(cfg, R),
+        "expert_weight_hbm": {
+            "bytes_per_step": step_bytes, "expert_bytes_per_step": eb["expert_weights"],
+            "experts_kept_per_layer": {"mean": round(statistics.mean(unions), 2), "min": min(unions),
+                                       "max": max(unions)},
+            "gbs_whole_step": round(step_gbs, 1),
+            "frac_of_peak_whole_step": round(step_gbs / hbm_peak, 4) if hbm_peak else None,
+            "gbs_expert_kernels": round(eb["expert_weights"] / (expert_stream_ms / 1e3) / 1e9, 1),
+            "frac_of_peak_expert_kernels": round(eb["expert_weights"] / (expert_stream_ms / 1e3) / 1e9 / hbm_peak, 4)
+            if hbm_peak else None,
+            "peak_gbs": hbm_peak},
+        "tokens_per_step": {"measured_synthetic": committed_per_step / R,
+                            "committed_tokens_per_s": {"tau=1": round(value, 2), "tau=10": round(10 * value, 2),
+                                                       "measured": round(value * committed_per_step / R, 2)},
+                            "note": "tau = tokens committed per step; synthetic hidden states have low "
+                                    "confidence, so the measured tau is the fallback's 1"},
+        "roofline": roofline,
+        "kernel_ms_per_step": {k: round(v[1] / steps_prof, 4) for k, v in prof.items() if v[0]},
+        "clocks": clk, "gpu_launches": launches, "e2e": e2e,
+        "setup_s": round(t_setup, 1),
+    }
+    return line, cfg
+
+
+def load_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d.get("hbm_gbs"), "bf16_tflops": d.get("bf16_tflops"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+def load_traffic():
+    """dram bytes per gate/up launch from the committed ncu summary, if it matches the current kernel."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(p):
+        try:
+            return json.load(open(p)).get("gateup_dram_bytes_per_launch")
+        except (ValueError, OSError):
+            return None
+    return None
+
+
+# ------------------------------------------------------------------------------------------ oracle (CPU)
+class OracleSample:
+    """The fp64 oracle on a bounded sample of the step: layer 0 of the stack over the whole
+    block (route, coreset, experts, residual, norm) and the LM head + commit.  Expert
+    weights the sample touches are generated before timing starts."""
+
+    def __init__(self, cfg, R: int):
+        import numpy as np
+
+        import oracle
+        from synth import workloads as W
+        self.cfg, self.R = cfg, R
+        self.h0 = W.host_h0(cfg, R).astype(np.float64)
+        self.masked = W.masked_subset(cfg, R)
+        hl = W.HostLayer(cfg, 0)
+        x = oracle.round_bf16(oracle.rmsnorm(self.h0))
+        idx, mass, _, _ = oracle.route(x, hl.Wr, cfg.k)
+        cs = oracle.coreset_select(idx, mass, TOP_P, cfg.P)
+        used = sorted({int(e) for e in idx[cs.survive]})
+        self.cache = {e: hl.expert(e) for e in used}
+        sh = hl.shared()
+        self.layer = oracle.MoELayer(Wr=hl.Wr, expert=lambda e: self.cache[e], shared=lambda: sh)
+        self.Wlm = W.host_lm_head(cfg)
+
+    def run(self) -> tuple[float, float]:
+        import numpy as np
+
+        import oracle
+        c = self.cfg
+        t0 = time.perf_counter()
+        x = oracle.round_bf16(oracle.rmsnorm(self.h0))
+        idx, mass, _, _ = oracle.route(x, self.layer.Wr, c.k)
+        cs = oracle.coreset_select(idx, mass, TOP_P, c.P)
+        h = self.h0 + oracle.moe_ffn(x, self.layer, idx, cs.gate_rr)
+        t_layer = time.perf_counter() - t0
+        t0 = time.perf_counter()
+        hidden = oracle.round_bf16(oracle.rmsnorm(h))
+        conf, choice = oracle.confidence_and_choice(oracle.lm_logits(hidden, self.Wlm))
+        oracle.lowconfidence_commit(conf, choice, np.zeros(len(conf), np.int32), self.masked, THRESHOLD, c.P)
+        t_head = time.perf_counter() - t0
+        return t_layer, t_head
+
+    def step_seconds(self, t_layer: float, t_head: float) -> float:
+        return self.cfg.n_layers * t_layer + t_head
+
+    def sample_desc(self) -> str:
+        return (f"layer 0 of {self.cfg.n_layers} over the full block (route, coreset, {len(self.cache)} routed "
+                f"experts + shared, residual, RMSNorm) plus the V={self.cfg.V} LM head and commit; step time = "
+                f"{self.cfg.n_layers} x layer + head")
+
+
+def cpu_baseline(cfg, R: int, reps: int = 3) -> dict:
+    s = OracleSample(cfg, R)
+    times = [s.run() for _ in range(reps)]
+    tl = statistics.median(t[0] for t in times)
+    th = statistics.median(t[1] for t in times)
+    return {"value": round(1.0 / s.step_seconds(tl, th), 5), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": s.sample_desc() + f"; median of {reps} repetitions",
+            "layer_s": round(tl, 3), "head_s": round(th, 3)}
+
+
+def run_reference(args, dist: Dist):
+    cfg = workload(args.config)
+    R = args.requests
+    s = OracleSample(cfg, R)
+    for _ in range(args.warmup):
+        s.run()
+    secs = [s.step_seconds(*s.run()) for _ in range(args.steps)]
+    total = sum(secs)
+    value = args.steps / total
+    base = {"value": round(value, 5), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": s.sample_desc() + "; every step one sample"}
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": UNIT, "n_gpus": dist.world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * total / args.steps, 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_desc(cfg, R), "cpu_baseline": base,
+            "e2e": {"value": round(value, 5), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        dist = Dist("gloo")
+        if dist.rank != 0:
+            dist.close()
+            return
+        print(json.dumps(run_reference(args, dist)), flush=True)
+        dist.close()
+        return
+    dist = Dist("nccl")
+    line, cfg = run_gpu(args, dist)
+    if dist.rank == 0:
+        if dist.world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(cfg, args.requests)
+        else:
+            line["cpu_baseline"] = None
+        print(json.dumps(line), flush=True)
+    dist.close()
+
+
+if __name__ == "__main__":
+    main()

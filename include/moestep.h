@@ -95,6 +95,7 @@ typedef struct {
     int32_t* n_sel;  /* [n_layers][R]     experts kept by each request's coreset */
     int32_t* idx;    /* [n_layers][T][k]  router top-k */
     float* hidden;   /* [T][H]            fp32 LM-head input (final RMSNorm output) */
+    int32_t* sel;    /* [n_layers][R][E]  kept experts in ranking order (first n_sel entries) */
 } moestep_trace;
 
 /* Bytes of workspace needed by every entry point below for R requests

@@ -51,7 +51,8 @@ class Layer(ctypes.Structure):
 
 
 class Trace(ctypes.Structure):
-    _fields_ = [("n_sel", ctypes.c_void_p), ("idx", ctypes.c_void_p), ("hidden", ctypes.c_void_p)]
+    _fields_ = [("n_sel", ctypes.c_void_p), ("idx", ctypes.c_void_p), ("hidden", ctypes.c_void_p),
+                ("sel", ctypes.c_void_p)]
 
 
 _LIB = None
@@ -205,9 +206,9 @@ def block_embed(d: ModelDims, R: int, tokens, masked, emb, pos, mask_id: int, h,
 
 def block_decode_step(d: ModelDims, R: int, layers, Wlm, top_p, threshold, h_in, tokens, masked, choice, conf,
                       accept, n_committed, ws, h_out=None, logit_scale=1.0, trace_n_sel=None, trace_idx=None,
-                      trace_hidden=None, stream=None) -> None:
+                      trace_hidden=None, trace_sel=None, stream=None) -> None:
     arr = (Layer * max(1, len(layers)))(*layers)
-    tr = Trace(_p(trace_n_sel), _p(trace_idx), _p(trace_hidden))
+    tr = Trace(_p(trace_n_sel), _p(trace_idx), _p(trace_hidden), _p(trace_sel))
     _check(lib().block_decode_step(ctypes.byref(d.c()), R, len(layers), arr, _p(Wlm), _p(top_p), float(logit_scale),
                                    float(threshold), _p(h_in), _p(h_out), _p(tokens), _p(masked), _p(choice),
                                    _p(conf), _p(accept), _p(n_committed), ctypes.byref(tr), _p(ws), ws.numel(),

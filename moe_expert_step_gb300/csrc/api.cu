@@ -559,8 +559,9 @@ int block_decode_step(const moestep_dims* dims, int R, int n_layers, const moest
     for (int l = 0; l < n_layers; ++l) {
         int32_t* idx = (trace && trace->idx) ? trace->idx + static_cast<size_t>(l) * T * k : at<int32_t>(ws, L.idx);
         int32_t* nsel = (trace && trace->n_sel) ? trace->n_sel + static_cast<size_t>(l) * R : at<int32_t>(ws, L.nsel);
+        int32_t* sel = (trace && trace->sel) ? trace->sel + static_cast<size_t>(l) * R * dims->E : at<int32_t>(ws, L.sel);
         MOESTEP_TRY(run_route(c, T, x, layers[l].Wr, idx, at<float>(ws, L.mass), at<float>(ws, L.gate), nullptr));
-        MOESTEP_TRY(run_coreset(c, R, top_p, idx, at<float>(ws, L.mass), nsel, at<int32_t>(ws, L.sel),
+        MOESTEP_TRY(run_coreset(c, R, top_p, idx, at<float>(ws, L.mass), nsel, sel,
                                 at<uint8_t>(ws, L.survive), at<float>(ws, L.gaterr)));
         MOESTEP_TRY(run_experts(c, R, x, &layers[l]));
         MOESTEP_LAUNCH(5, launch_combine(1, dims->dtype, T, dims->H, k, at<float>(ws, L.y),
