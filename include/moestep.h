@@ -117,6 +117,23 @@ int moestep_workspace_init(void* ws, size_t ws_bytes, void* stream);
 int moe_block_route(const moestep_dims* dims, int T, const void* x, const void* Wr, int32_t* idx,
                     float* mass, float* gate, float* logits, void* ws, size_t ws_bytes, void* stream);
 
+/* The router of moe_block_route for callers that cannot allocate device memory
+ * (no workspace argument).  The pages have no counterpart: this is an
+ * interface for hosts whose device memory is owned elsewhere (an application
+ * allocator, a fixed embedded budget) and that therefore cannot call
+ * cudaMalloc or hand over a scratch buffer.
+ * Scratch (router logits when `logits` is NULL, and the completion counters)
+ * lives in one fixed array inside the library, 516 KiB per device, held by
+ * every GPU that loads the library until the process exits.  Limits:
+ * T * E <= 131072 and T <= 8192; larger calls return MOESTEP_EUNSUPPORTED.
+ * Arguments as in moe_block_route.  The first call on a device looks up the
+ * array's device address (make that call before any stream capture).  The
+ * call allocates nothing and clears the counters it needs on `stream`; all
+ * calls share the one array, so calls whose executions overlap on the GPU
+ * (other streams, other threads) race and must be serialised by the caller. */
+int moe_block_route_noalloc(const moestep_dims* dims, int T, const void* x, const void* Wr, int32_t* idx,
+                            float* mass, float* gate, float* logits, void* stream);
+
 /* Top-k, masses and gates from given router logits [T][E] fp32 (same rules as
  * moe_block_route).  Lets integer outputs be compared on identical inputs. */
 int moe_route_from_logits(const moestep_dims* dims, int T, const float* logits, int32_t* idx,

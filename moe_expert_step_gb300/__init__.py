@@ -32,7 +32,7 @@ EXPORTS = [
     "moestep_workspace_size", "moestep_workspace_init", "moe_block_route", "moe_route_from_logits", "coreset_select", "moe_block_ffn",
     "lm_head_commit", "lm_commit_from_logits", "block_embed", "block_decode_step", "moestep_read_device_error",
     "moestep_error_string", "moestep_last_cuda_error", "moestep_prof_enable", "moestep_prof_read",
-    "moestep_set_wait_timeout_ns", "moestep_launch_count",
+    "moestep_set_wait_timeout_ns", "moestep_launch_count", "moe_block_route_noalloc",
 ]
 
 
@@ -76,6 +76,7 @@ def lib():
             "moestep_workspace_init": [vp, sz, vp],
             "moe_block_route": [D, i, vp, vp, vp, vp, vp, vp, vp, sz, vp],
             "moe_route_from_logits": [D, i, vp, vp, vp, vp, vp, sz, vp],
+            "moe_block_route_noalloc": [D, i, vp, vp, vp, vp, vp, vp, vp],
             "coreset_select": [D, i, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp],
             "moe_block_ffn": [D, i, vp, ctypes.POINTER(Layer), vp, vp, vp, sz, vp],
             "lm_head_commit": [D, i, vp, vp, f, f, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp],
@@ -168,6 +169,13 @@ def workspace(d: ModelDims, R: int, device="cuda", stream=None):
 def moe_block_route(d: ModelDims, x, Wr, idx, mass, gate, ws, logits=None, stream=None) -> None:
     _check(lib().moe_block_route(ctypes.byref(d.c()), x.shape[0], _p(x), _p(Wr), _p(idx), _p(mass), _p(gate),
                                  _p(logits), _p(ws), ws.numel(), _s(stream)), "moe_block_route")
+
+
+def moe_block_route_noalloc(d: ModelDims, x, Wr, idx, mass, gate, logits=None, stream=None) -> None:
+    """The router without a workspace (scratch in a fixed array inside the library); for callers
+    that cannot allocate device memory.  Calls that overlap on the GPU race on that array."""
+    _check(lib().moe_block_route_noalloc(ctypes.byref(d.c()), x.shape[0], _p(x), _p(Wr), _p(idx), _p(mass),
+                                         _p(gate), _p(logits), _s(stream)), "moe_block_route_noalloc")
 
 
 def moe_route_from_logits(d: ModelDims, logits, idx, mass, gate, ws, stream=None) -> None:

@@ -9,7 +9,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 LIB_DIR = os.path.join(HERE, "lib")
 LIB = os.path.join(LIB_DIR, "libmoestep.so")
-SOURCES = ["api.cu", "route.cu", "misc.cu", "expert_gemm.cu"]
+SOURCES = ["api.cu", "route.cu", "misc.cu", "expert_gemm.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -373,6 +373,9 @@ bool thr_ok(float t) { return t > 0.f && t <= 1.f; }
 
 }  // namespace
 
+int validate_dims(const moestep_dims* d) { return check_dims(d); }
+int device_ok(int* sms) { return device_check(sms); }
+
 void prof_begin(int kid, cudaStream_t s) {
     if (kid < 0 || kid >= MOESTEP_PROF_KERNELS || !((g_prof.mask >> kid) & 1)) return;
     cudaEvent_t e = prof_event();

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "moestep.h"
+
 namespace moestep {
 
 // ------------------------------------------------------------------ grouped tcgen05 GEMM
@@ -100,6 +102,10 @@ cudaError_t launch_partials_from_logits(const float* logits, int T, int V, float
 cudaError_t launch_commit(int R, int P, int n_tiles, const float* pmax, const int* parg, const float* psum,
                           float threshold, int32_t* tokens, uint8_t* masked, int32_t* choice, float* conf,
                           uint8_t* accept, int32_t* n_committed, cudaStream_t s);
+
+// ------------------------------------------------------------------ shared host checks (api.cu)
+int validate_dims(const moestep_dims* d);  // MOESTEP_OK or the code every entry point returns
+int device_ok(int* sms);                   // current device is sm_103; *sms = its SM count
 
 // ------------------------------------------------------------------ profiling hooks (api.cu)
 void prof_begin(int kid, cudaStream_t s);
