@@ -42,6 +42,7 @@ def parse():
     ap.add_argument("--requests", type=int, default=1, help="concurrent requests (blocks) per GPU")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--prof-all", action="store_true", help="time every kernel in the roofline pass")
     return ap.parse_args()
 
 
@@ -230,7 +231,7 @@ def run_gpu(args, dist: Dist):
     clk = clocks.result()
 
     # ---------------- roofline pass: events around the expert and LM-head kernels on their stream
-    ms.prof_enable(["expert_gateup", "expert_down", "lm_head"])
+    ms.prof_enable(None if args.prof_all else ["expert_gateup", "expert_down", "lm_head"])
     for _ in range(args.steps):
         step()
     torch.cuda.synchronize()
