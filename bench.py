@@ -298,7 +298,8 @@ def run_gpu(args, dist: Dist):
     achieved = gu_bytes_launch / (gu_avg_ms / 1e3) / 1e9
     roofline = {"kernel": "tc_gemm_kernel<gate/up> (expert gate/up projections + SwiGLU)",
                 "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
-                "frac": round(achieved / hbm_peak, 4) if hbm_peak else None, "traffic": load_traffic(),
+                "frac": round(achieved / hbm_peak, 4) if hbm_peak else None,
+                "traffic": load_traffic(statistics.mean(unions) + -(-T // nch_for(T))),
                 "peak_source": peaks.get("source"),
                 "bytes_per_launch": int(gu_bytes_launch), "avg_launch_ms": round(gu_avg_ms, 5),
                 "launches_timed": gu_n}
@@ -340,15 +341,33 @@ def load_peaks() -> dict:
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
 
 
-def load_traffic():
-    """dram bytes per gate/up launch from the committed ncu summary, if it matches the current kernel."""
-    p = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(p):
-        try:
-            return json.load(open(p)).get("gateup_dram_bytes_per_launch")
-        except (ValueError, OSError):
-            return None
-    return None
+def nch_for(T: int) -> int:
+    """Token chunk of the expert GEMM (the library's rule): experts with more tokens are split."""
+    return 32 if T <= 32 else 64 if T <= 64 else 128 if T <= 128 else 256
+
+
+def kernel_sources_sha() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("expert_gemm.cu", "tc.cuh", "common.cuh"):
+        h.update(open(os.path.join(ROOT, "moe_expert_step_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic(units_per_launch: float):
+    """DRAM bytes per gate/up launch: the ncu capture's bytes per unit (profiles/) scaled to the
+    units of one launch here; None if the kernel sources changed since that capture."""
+    p = os.path.join(ROOT, "profiles", "tc_gemm_clover_layer.md")
+    if not os.path.exists(p):
+        return None
+    vals = {}
+    for line in open(p):
+        if ":" in line and line.split(":")[0].strip() in ("gateup_traffic_bytes_per_unit", "gateup_sources_sha"):
+            k, v = line.split(":", 1)
+            vals[k.strip()] = v.strip()
+    if vals.get("gateup_sources_sha") != kernel_sources_sha() or "gateup_traffic_bytes_per_unit" not in vals:
+        return None
+    return int(float(vals["gateup_traffic_bytes_per_unit"]) * units_per_launch)
 
 
 # ------------------------------------------------------------------------------------------ oracle (CPU)
