@@ -43,6 +43,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--prof-all", action="store_true", help="time every kernel in the roofline pass")
+    ap.add_argument("--no-graph", action="store_true", help="time direct launches instead of CUDA-graph replays")
     return ap.parse_args()
 
 
@@ -141,7 +142,9 @@ def workload_desc(cfg, R: int) -> dict:
             "layers": cfg.n_layers, "block_tokens": cfg.P, "requests": R, "top_p": TOP_P,
             "threshold": THRESHOLD, "vocab": cfg.V,
             "l2": "inputs larger than L2: every step streams the selected experts' weights (tens of GB) from HBM",
-            "parallelism": "replicas (one independent block step per GPU)"}
+            "parallelism": "replicas (one independent block step per GPU)",
+            "launch": "one block_decode_step call per step, replayed as a CUDA graph (programmatic dependent launch "
+                      "between kernels)"}
 
 
 def expert_bytes(cfg, unions) -> dict:
@@ -209,6 +212,29 @@ def run_gpu(args, dist: Dist):
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize()
+    ref_out = (tokens.clone(), masked.clone(), conf.clone())
+
+    # the step is capturable: every launch is asynchronous on the caller's stream
+    run = step
+    per_replay = None
+    if not args.no_graph:
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            step()
+        torch.cuda.current_stream().wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        c0 = ms.launch_count()
+        with torch.cuda.graph(graph):
+            step()
+        per_replay = ms.launch_count() - c0      # library kernels captured into the graph
+        run = graph.replay
+        for _ in range(max(3, args.warmup)):
+            run()
+        torch.cuda.synchronize()
+        for a, b in zip((tokens, masked, conf), ref_out):
+            if not torch.equal(a, b):
+                raise RuntimeError("graph replay differs from a direct call")
 
     stream = torch.cuda.current_stream()
     clocks = Clocks("GPU-" + str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid))
@@ -221,12 +247,12 @@ def run_gpu(args, dist: Dist):
     clocks.mark_start()
     e0.record(stream)
     for _ in range(args.steps):
-        step()
+        run()
     e1.record(stream)
     torch.cuda.synchronize()
     clocks.mark_end()
     dist.barrier()
-    launches = ms.launch_count() - launches0
+    launches = ms.launch_count() - launches0 if per_replay is None else per_replay * args.steps
     ms_total = dist.max(e0.elapsed_time(e1))
     clk = clocks.result()
 
@@ -328,6 +354,7 @@ def run_gpu(args, dist: Dist):
         "roofline": roofline,
         "kernel_ms_per_step": {k: round(v[1] / steps_prof, 4) for k, v in prof.items() if v[0]},
         "clocks": clk, "gpu_launches": launches, "e2e": e2e,
+        "graph": not args.no_graph,
         "setup_s": round(t_setup, 1),
     }
     return line, cfg

@@ -62,7 +62,7 @@ Layout make_layout(const moestep_dims& d, int R) {
         return at;
     };
     L.hdr = take(256);  // int[0]: error word, int[8..15]: where a wait timed out, int[32..34]: expert work plan
-    L.counters_bytes = sizeof(int) * (L.route_groups + 1);
+    L.counters_bytes = sizeof(int) * (L.route_groups + 1 + R);  // router groups, coreset, commit per request
     L.counters = take(L.counters_bytes);
     L.logits = take(sizeof(float) * T * d.E);
     L.idx = take(sizeof(int32_t) * T * d.k);
@@ -357,7 +357,7 @@ int run_lm_commit(const Ctx& c, int R, const void* hidden, const void* Wlm, floa
     }
     MOESTEP_LAUNCH(7, launch_commit(R, d->P, n_tiles, at<float>(c.ws, L.pmax), at<int>(c.ws, L.parg),
                                     at<float>(c.ws, L.psum), thr, tokens, masked, choice, conf, accept, n_committed,
-                                    c.s));
+                                    at<int>(c.ws, L.counters) + L.route_groups + 1, c.s));
     return MOESTEP_OK;
 }
 
@@ -497,6 +497,7 @@ int lm_head_commit(const moestep_dims* dims, int R, const void* hidden, const vo
     int sms = 0;
     MOESTEP_TRY(device_check(&sms));
     Ctx c{dims, make_layout(*dims, R), ws, static_cast<cudaStream_t>(stream), sms};
+    MOESTEP_CK(cudaMemsetAsync(at<char>(ws, c.L.counters), 0, c.L.counters_bytes, c.s));
     return run_lm_commit(c, R, hidden, Wlm, logit_scale, threshold, tokens, masked, choice, conf, accept,
                          n_committed, logits);
 }
@@ -513,11 +514,13 @@ int lm_commit_from_logits(const moestep_dims* dims, int R, const float* logits, 
     MOESTEP_TRY(device_check(&sms));
     Ctx c{dims, make_layout(*dims, R), ws, static_cast<cudaStream_t>(stream), sms};
     const int T = R * dims->P;
+    MOESTEP_CK(cudaMemsetAsync(at<char>(ws, c.L.counters), 0, c.L.counters_bytes, c.s));
     MOESTEP_LAUNCH(8, launch_partials_from_logits(logits, T, dims->V, at<float>(ws, c.L.pmax), at<int>(ws, c.L.parg),
                                                   at<float>(ws, c.L.psum), c.s));
     MOESTEP_LAUNCH(7, launch_commit(R, dims->P, (dims->V + kLogitTile - 1) / kLogitTile, at<float>(ws, c.L.pmax),
                                     at<int>(ws, c.L.parg), at<float>(ws, c.L.psum), threshold, tokens, masked, choice,
-                                    conf, accept, n_committed, c.s));
+                                    conf, accept, n_committed, at<int>(ws, c.L.counters) + c.L.route_groups + 1,
+                                    c.s));
     return MOESTEP_OK;
 }
 

@@ -52,6 +52,14 @@ __device__ __forceinline__ void warp_argmax(float& v, int& i) {
     }
 }
 
+// Programmatic dependent launch.  Every kernel of the library is launched so
+// that the next kernel in the stream may start early; each kernel first lets
+// its own dependents start (trigger), then waits until every preceding kernel
+// has completed and its writes are visible (wait) before touching memory.
+// Because every kernel waits, completion stays transitive along the stream.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void record_error(int* err, int bits) {
     if (err) atomicOr(err, bits);
 }

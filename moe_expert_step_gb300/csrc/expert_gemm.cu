@@ -26,6 +26,7 @@
 // (timeout -> error word, orderly teardown), so no wait can hang the GPU.
 #include "common.cuh"
 #include "kernels.h"
+#include "launch.cuh"
 #include "tc.cuh"
 
 namespace moestep {
@@ -135,14 +136,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    int nrc = 0, n_units;
-    if (MODE == kLmHead) {
-        n_units = p.lm_chunks * p.lm_tiles;
-    } else {
-        nrc = p.plan[0];
-        n_units = nrc * p.routed_tiles + p.plan[1] * p.shared_tiles;
-    }
-
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             tc::mbar_init(&full[s], 1);
@@ -168,6 +161,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem_base = *tmem_holder;
+    // prologue done: let the next kernel start, then wait for the work plan / inputs
+    pdl_trigger();
+    pdl_wait();
+    int nrc = 0, n_units;
+    if (MODE == kLmHead) {
+        n_units = p.lm_chunks * p.lm_tiles;
+    } else {
+        nrc = p.plan[0];
+        n_units = nrc * p.routed_tiles + p.plan[1] * p.shared_tiles;
+    }
     volatile int* abortv = abort_flag;
     const uint64_t tmo = p.timeout_ns;
 
@@ -375,16 +378,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int MODE, int NCH>
 cudaError_t launch_one(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b, const GemmParams& p,
                        int grid, cudaStream_t s) {
-    static bool attr_set = false;  // per instantiation; set once per process
     constexpr int bytes = smem_bytes(NCH);
-    if (!attr_set) {
-        cudaError_t e =
-            cudaFuncSetAttribute(tc_gemm_kernel<MODE, NCH>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
-    tc_gemm_kernel<MODE, NCH><<<grid, kThreads, bytes, s>>>(a0, a1, b, p);
-    return cudaGetLastError();
+    cudaError_t e = ensure_smem(tc_gemm_kernel<MODE, NCH>, bytes);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(tc_gemm_kernel<MODE, NCH>, dim3(grid), dim3(kThreads), bytes, s, a0, a1, b, p);
 }
 
 template <int MODE>

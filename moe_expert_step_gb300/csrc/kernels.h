@@ -101,7 +101,7 @@ cudaError_t launch_partials_from_logits(const float* logits, int T, int V, float
                                         cudaStream_t s);
 cudaError_t launch_commit(int R, int P, int n_tiles, const float* pmax, const int* parg, const float* psum,
                           float threshold, int32_t* tokens, uint8_t* masked, int32_t* choice, float* conf,
-                          uint8_t* accept, int32_t* n_committed, cudaStream_t s);
+                          uint8_t* accept, int32_t* n_committed, int* counters, cudaStream_t s);
 
 // ------------------------------------------------------------------ shared host checks (api.cu)
 int validate_dims(const moestep_dims* d);  // MOESTEP_OK or the code every entry point returns

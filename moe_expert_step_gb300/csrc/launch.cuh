@@ -1,0 +1,41 @@
+// Host-side launch helper: every kernel goes out with programmatic stream
+// serialisation allowed (see pdl_trigger / pdl_wait in common.cuh), and
+// per-device one-time dynamic shared-memory opt-in.
+#pragma once
+#include <cuda_runtime.h>
+
+namespace moestep {
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
+// Raise a kernel's dynamic shared-memory limit once per device (kept per
+// function instantiation), so repeated calls make no attribute calls.
+template <typename K>
+inline cudaError_t ensure_smem(K kern, size_t bytes) {
+    static int done[64] = {};
+    if (bytes <= 48 * 1024) return cudaSuccess;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (done[dev] >= static_cast<int>(bytes)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+    if (e == cudaSuccess) done[dev] = static_cast<int>(bytes);
+    return e;
+}
+
+}  // namespace moestep

@@ -3,6 +3,7 @@
 // LowConfidence commit.
 #include "common.cuh"
 #include "kernels.h"
+#include "launch.cuh"
 
 namespace moestep {
 namespace {
@@ -59,6 +60,8 @@ __global__ void __launch_bounds__(256) combine_kernel(int H, int k, const float*
     __shared__ float s_g[33];
     __shared__ float red[9];
     const int t = blockIdx.x;
+    pdl_trigger();
+    pdl_wait();
     if (MODE != 2) {
         if (threadIdx.x < k) {
             s_slot[threadIdx.x] = slot_of[t * k + threadIdx.x];
@@ -72,15 +75,24 @@ __global__ void __launch_bounds__(256) combine_kernel(int H, int k, const float*
     for (int c = threadIdx.x * 4; c < H; c += 1024) {
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         if (MODE != 2) {
-            for (int j = 0; j < k; ++j) {
-                const int sl = s_slot[j];
-                if (sl >= 0) {
-                    const float g = s_g[j];
-                    const float4 v = *reinterpret_cast<const float4*>(y + static_cast<size_t>(sl) * H + c);
-                    acc.x += g * v.x;
-                    acc.y += g * v.y;
-                    acc.z += g * v.z;
-                    acc.w += g * v.w;
+            // slots in groups of 8 loaded together, added in candidate order
+            for (int j0 = 0; j0 < k; j0 += 8) {
+                float4 v[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const int sl = (j0 + q < k) ? s_slot[j0 + q] : -1;
+                    v[q] = sl >= 0 ? __ldg(reinterpret_cast<const float4*>(y + static_cast<size_t>(sl) * H + c))
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    if (j0 + q < k && s_slot[j0 + q] >= 0) {
+                        const float g = s_g[j0 + q];
+                        acc.x += g * v[q].x;
+                        acc.y += g * v[q].y;
+                        acc.z += g * v[q].z;
+                        acc.w += g * v[q].w;
+                    }
                 }
             }
             if (s_slot[32] >= 0) {
@@ -117,6 +129,8 @@ __global__ void __launch_bounds__(256) embed_kernel(int H, int P, int V, const i
                                                     const uint8_t* __restrict__ masked, const T* __restrict__ emb,
                                                     const T* __restrict__ pos, int mask_id, float* __restrict__ h) {
     const int t = blockIdx.x;
+    pdl_trigger();
+    pdl_wait();
     const int id = masked[t] ? mask_id : tokens[t];
     if (id < 0 || id >= V) {
         for (int c = threadIdx.x; c < H; c += blockDim.x) h[static_cast<size_t>(t) * H + c] = __int_as_float(0x7fc00000);
@@ -146,6 +160,8 @@ __global__ void __launch_bounds__(256) f32_gateup_kernel(int H, int E, int I, in
                                                          const int* __restrict__ plan, const float* __restrict__ Wgu,
                                                          const float* __restrict__ Wsgu, float* __restrict__ act,
                                                          int act_ld) {
+    pdl_trigger();
+    pdl_wait();
     const int n_slots = plan[2];
     const long long total = static_cast<long long>(max_slots) * Imax;
     for (long long g = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; g < total;
@@ -174,6 +190,8 @@ __global__ void __launch_bounds__(256) f32_down_kernel(int H, int E, int I, int 
                                                        const int32_t* __restrict__ slot_exp, const int* __restrict__ plan,
                                                        const float* __restrict__ Wd, const float* __restrict__ Wsd,
                                                        float* __restrict__ y) {
+    pdl_trigger();
+    pdl_wait();
     const int n_slots = plan[2];
     const long long total = static_cast<long long>(max_slots) * H;
     for (long long g = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; g < total;
@@ -195,6 +213,8 @@ __global__ void __launch_bounds__(256) f32_down_kernel(int H, int E, int I, int 
 __global__ void __launch_bounds__(256) f32_lm_logits_kernel(int T, int H, int V, const float* __restrict__ hidden,
                                                             const float* __restrict__ Wlm, float scale,
                                                             float* __restrict__ logits) {
+    pdl_trigger();
+    pdl_wait();
     const long long total = static_cast<long long>(T) * V;
     for (long long g = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; g < total;
          g += static_cast<long long>(gridDim.x) * blockDim.x) {
@@ -213,6 +233,8 @@ __global__ void __launch_bounds__(256) partials_kernel(const float* __restrict__
     __shared__ int sa[8];
     __shared__ float red[9];
     const int tile = blockIdx.x, p = blockIdx.y;
+    pdl_trigger();
+    pdl_wait();
     const float* row = logits + static_cast<size_t>(p) * V;
     const int v0 = tile * kLogitTile;
     const int v1 = min(V, v0 + kLogitTile);
@@ -251,84 +273,104 @@ __global__ void __launch_bounds__(256) partials_kernel(const float* __restrict__
 }
 
 // ------------------------------------------------------------------ LowConfidence commit
-// One CTA (1024 threads) per request.  Warps merge each position's partials
-// into conf = 1 / sum exp(l - max) and choice = lowest argmax; warp 0 then
-// commits every masked position with conf >= threshold, or, if there is none,
-// the masked position with the highest conf (lowest position on ties).
-__global__ void __launch_bounds__(1024) commit_kernel(int P, int T, int n_tiles, const float* __restrict__ pmax,
-                                                      const int* __restrict__ parg, const float* __restrict__ psum,
-                                                      float thr, int32_t* __restrict__ tokens,
-                                                      uint8_t* __restrict__ masked, int32_t* __restrict__ choice,
-                                                      float* __restrict__ conf, uint8_t* __restrict__ accept,
-                                                      int32_t* __restrict__ n_committed) {
-    __shared__ float s_conf[1024];
-    __shared__ int s_choice[1024];
-    const int r = blockIdx.x;
+// grid = T (one CTA of 256 threads per position).  Each CTA merges its
+// position's partials (fixed order: per thread by tile, then a fixed tree) into
+// conf = 1 / sum exp(l - max) and choice = lowest argmax and writes them out.
+// The last CTA of each request (atomic counter, reset by that CTA) then commits:
+// every masked position with conf >= threshold, or, if there is none, the
+// masked position with the highest conf (lowest position on ties).
+__global__ void __launch_bounds__(256) commit_kernel(int P, int T, int n_tiles, const float* __restrict__ pmax,
+                                                     const int* __restrict__ parg, const float* __restrict__ psum,
+                                                     float thr, int32_t* __restrict__ tokens,
+                                                     uint8_t* __restrict__ masked, int32_t* __restrict__ choice,
+                                                     float* __restrict__ conf, uint8_t* __restrict__ accept,
+                                                     int32_t* __restrict__ n_committed, int* __restrict__ counters) {
+    __shared__ SoftmaxPartial wred[8];
+    __shared__ int s_last;
+    const int pos = blockIdx.x;
+    const int r = pos / P;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int pp = warp; pp < P; pp += 32) {
-        const int pos = r * P + pp;
-        SoftmaxPartial acc{-INFINITY, 0x7fffffff, 0.f};
-        for (int tl = lane; tl < n_tiles; tl += 32) {
-            const size_t o = static_cast<size_t>(tl) * T + pos;
-            acc = merge_partial(acc, SoftmaxPartial{pmax[o], parg[o], psum[o]});
+    pdl_trigger();
+    pdl_wait();
+    SoftmaxPartial acc{-INFINITY, 0x7fffffff, 0.f};
+    int tl = threadIdx.x;
+    for (; tl + 3 * 256 < n_tiles; tl += 4 * 256) {
+        SoftmaxPartial q[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const size_t o = static_cast<size_t>(tl + u * 256) * T + pos;
+            q[u] = SoftmaxPartial{pmax[o], parg[o], psum[o]};
         }
 #pragma unroll
-        for (int off = 16; off; off >>= 1) {
-            SoftmaxPartial o;
-            o.m = __shfl_xor_sync(0xffffffffu, acc.m, off);
-            o.a = __shfl_xor_sync(0xffffffffu, acc.a, off);
-            o.s = __shfl_xor_sync(0xffffffffu, acc.s, off);
-            acc = merge_partial(acc, o);
-        }
-        if (lane == 0) {
-            s_conf[pp] = acc.s > 0.f ? 1.0f / acc.s : 0.f;
-            s_choice[pp] = acc.a;
-        }
+        for (int u = 0; u < 4; ++u) acc = merge_partial(acc, q[u]);
+    }
+    for (; tl < n_tiles; tl += 256) {
+        const size_t o = static_cast<size_t>(tl) * T + pos;
+        acc = merge_partial(acc, SoftmaxPartial{pmax[o], parg[o], psum[o]});
+    }
+#pragma unroll
+    for (int off = 16; off; off >>= 1) {
+        SoftmaxPartial o;
+        o.m = __shfl_xor_sync(0xffffffffu, acc.m, off);
+        o.a = __shfl_xor_sync(0xffffffffu, acc.a, off);
+        o.s = __shfl_xor_sync(0xffffffffu, acc.s, off);
+        acc = merge_partial(acc, o);
+    }
+    if (lane == 0) wred[warp] = acc;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        SoftmaxPartial b = wred[0];
+        for (int w = 1; w < 8; ++w) b = merge_partial(b, wred[w]);
+        conf[pos] = b.s > 0.f ? 1.0f / b.s : 0.f;
+        choice[pos] = b.a;
+        __threadfence();
+        const int prev = atomicAdd(&counters[r], 1);
+        s_last = (prev == P - 1);
+        if (s_last) counters[r] = 0;
     }
     __syncthreads();
-    if (warp != 0) return;
+    if (!s_last || warp != 0) return;
+    __threadfence();
     int any = 0;
     for (int pp = lane; pp < P; pp += 32)
-        if (masked[r * P + pp] && s_conf[pp] >= thr) any = 1;
+        if (masked[r * P + pp] && __ldcg(&conf[r * P + pp]) >= thr) any = 1;
     any = __any_sync(0xffffffffu, any);
     int count = 0;
     if (any) {
         for (int pp = lane; pp < P; pp += 32) {
-            const int pos = r * P + pp;
-            const bool ok = masked[pos] && s_conf[pp] >= thr;
+            const int q = r * P + pp;
+            const bool ok = masked[q] && __ldcg(&conf[q]) >= thr;
             if (ok) {
-                tokens[pos] = s_choice[pp];
-                masked[pos] = 0;
+                tokens[q] = __ldcg(&choice[q]);
+                masked[q] = 0;
                 ++count;
             }
-            accept[pos] = ok ? 1 : 0;
+            accept[q] = ok ? 1 : 0;
         }
     } else {
         float bv = -INFINITY;
         int bp = 0x7fffffff;
-        for (int pp = lane; pp < P; pp += 32)
-            if (masked[r * P + pp] && (s_conf[pp] > bv || bp == 0x7fffffff)) {
-                bv = s_conf[pp];
+        for (int pp = lane; pp < P; pp += 32) {
+            const float c = __ldcg(&conf[r * P + pp]);
+            if (masked[r * P + pp] && (c > bv || bp == 0x7fffffff)) {
+                bv = c;
                 bp = pp;
             }
+        }
         warp_argmax(bv, bp);
         for (int pp = lane; pp < P; pp += 32) {
-            const int pos = r * P + pp;
+            const int q = r * P + pp;
             const bool ok = (pp == bp);
             if (ok) {
-                tokens[pos] = s_choice[pp];
-                masked[pos] = 0;
+                tokens[q] = __ldcg(&choice[q]);
+                masked[q] = 0;
                 ++count;
             }
-            accept[pos] = ok ? 1 : 0;
+            accept[q] = ok ? 1 : 0;
         }
     }
     count = __reduce_add_sync(0xffffffffu, count);
     if (lane == 0) n_committed[r] = count;
-    for (int pp = lane; pp < P; pp += 32) {
-        conf[r * P + pp] = s_conf[pp];
-        choice[r * P + pp] = s_choice[pp];
-    }
 }
 
 int grid_1d(long long work, int per_block = 256) {
@@ -343,69 +385,61 @@ int grid_1d(long long work, int per_block = 256) {
 cudaError_t launch_combine(int mode, int dtype, int T, int H, int k, const float* y, const int32_t* slot_of,
                            const int32_t* slot_sh, const float* gate_rr, int has_shared, const float* h_in, float* h,
                            void* x, float* x_f32, float* out, cudaStream_t s) {
-#define MOESTEP_COMBINE(TT, MM)                                                                                  \
-    combine_kernel<TT, MM><<<T, 256, 0, s>>>(H, k, y, slot_of, slot_sh, gate_rr, has_shared, h_in, h,          \
-                                             static_cast<TT*>(x), x_f32, out)
+#define MOESTEP_COMBINE(TT, MM)                                                                                 \
+    launch_pdl(combine_kernel<TT, MM>, dim3(T), dim3(256), 0, s, H, k, y, slot_of, slot_sh, gate_rr, has_shared, \
+               h_in, h, static_cast<TT*>(x), x_f32, out)
     if (dtype == MOESTEP_BF16) {
-        if (mode == 0) MOESTEP_COMBINE(bf16, 0);
-        else if (mode == 1) MOESTEP_COMBINE(bf16, 1);
-        else MOESTEP_COMBINE(bf16, 2);
-    } else {
-        if (mode == 0) MOESTEP_COMBINE(float, 0);
-        else if (mode == 1) MOESTEP_COMBINE(float, 1);
-        else MOESTEP_COMBINE(float, 2);
+        if (mode == 0) return MOESTEP_COMBINE(bf16, 0);
+        if (mode == 1) return MOESTEP_COMBINE(bf16, 1);
+        return MOESTEP_COMBINE(bf16, 2);
     }
+    if (mode == 0) return MOESTEP_COMBINE(float, 0);
+    if (mode == 1) return MOESTEP_COMBINE(float, 1);
+    return MOESTEP_COMBINE(float, 2);
 #undef MOESTEP_COMBINE
-    return cudaGetLastError();
 }
 
 cudaError_t launch_embed(int dtype, int T, int H, int P, int V, const int32_t* tokens, const uint8_t* masked,
                          const void* emb, const void* pos, int mask_id, float* h, cudaStream_t s) {
     if (dtype == MOESTEP_BF16)
-        embed_kernel<bf16><<<T, 256, 0, s>>>(H, P, V, tokens, masked, static_cast<const bf16*>(emb),
-                                             static_cast<const bf16*>(pos), mask_id, h);
-    else
-        embed_kernel<float><<<T, 256, 0, s>>>(H, P, V, tokens, masked, static_cast<const float*>(emb),
-                                              static_cast<const float*>(pos), mask_id, h);
-    return cudaGetLastError();
+        return launch_pdl(embed_kernel<bf16>, dim3(T), dim3(256), 0, s, H, P, V, tokens, masked,
+                          static_cast<const bf16*>(emb), static_cast<const bf16*>(pos), mask_id, h);
+    return launch_pdl(embed_kernel<float>, dim3(T), dim3(256), 0, s, H, P, V, tokens, masked,
+                      static_cast<const float*>(emb), static_cast<const float*>(pos), mask_id, h);
 }
 
 cudaError_t launch_f32_gateup(int H, int E, int I, int Is, int max_slots, const float* xp, const int32_t* slot_exp,
                               const int* plan, const float* Wgu, const float* Wsgu, float* act, int act_ld,
                               cudaStream_t s) {
     const int Imax = I > Is ? I : Is;
-    f32_gateup_kernel<<<grid_1d(static_cast<long long>(max_slots) * Imax), 256, 0, s>>>(
-        H, E, I, Is, Imax, max_slots, xp, slot_exp, plan, Wgu, Wsgu, act, act_ld);
-    return cudaGetLastError();
+    return launch_pdl(f32_gateup_kernel, dim3(grid_1d(static_cast<long long>(max_slots) * Imax)), dim3(256), 0, s,
+                      H, E, I, Is, Imax, max_slots, xp, slot_exp, plan, Wgu, Wsgu, act, act_ld);
 }
 
 cudaError_t launch_f32_down(int H, int E, int I, int Is, int max_slots, const float* act, int act_ld,
                             const int32_t* slot_exp, const int* plan, const float* Wd, const float* Wsd, float* y,
                             cudaStream_t s) {
-    f32_down_kernel<<<grid_1d(static_cast<long long>(max_slots) * H), 256, 0, s>>>(H, E, I, Is, max_slots, act,
-                                                                                   act_ld, slot_exp, plan, Wd, Wsd, y);
-    return cudaGetLastError();
+    return launch_pdl(f32_down_kernel, dim3(grid_1d(static_cast<long long>(max_slots) * H)), dim3(256), 0, s, H, E,
+                      I, Is, max_slots, act, act_ld, slot_exp, plan, Wd, Wsd, y);
 }
 
 cudaError_t launch_f32_lm_logits(int T, int H, int V, const float* hidden, const float* Wlm, float scale,
                                  float* logits, cudaStream_t s) {
-    f32_lm_logits_kernel<<<grid_1d(static_cast<long long>(T) * V), 256, 0, s>>>(T, H, V, hidden, Wlm, scale, logits);
-    return cudaGetLastError();
+    return launch_pdl(f32_lm_logits_kernel, dim3(grid_1d(static_cast<long long>(T) * V)), dim3(256), 0, s, T, H, V,
+                      hidden, Wlm, scale, logits);
 }
 
 cudaError_t launch_partials_from_logits(const float* logits, int T, int V, float* pmax, int* parg, float* psum,
                                         cudaStream_t s) {
     const dim3 grid((V + kLogitTile - 1) / kLogitTile, T);
-    partials_kernel<<<grid, 256, 0, s>>>(logits, T, V, pmax, parg, psum);
-    return cudaGetLastError();
+    return launch_pdl(partials_kernel, grid, dim3(256), 0, s, logits, T, V, pmax, parg, psum);
 }
 
 cudaError_t launch_commit(int R, int P, int n_tiles, const float* pmax, const int* parg, const float* psum,
                           float threshold, int32_t* tokens, uint8_t* masked, int32_t* choice, float* conf,
-                          uint8_t* accept, int32_t* n_committed, cudaStream_t s) {
-    commit_kernel<<<R, 1024, 0, s>>>(P, R * P, n_tiles, pmax, parg, psum, threshold, tokens, masked, choice, conf,
-                                     accept, n_committed);
-    return cudaGetLastError();
+                          uint8_t* accept, int32_t* n_committed, int* counters, cudaStream_t s) {
+    return launch_pdl(commit_kernel, dim3(R * P), dim3(256), 0, s, P, R * P, n_tiles, pmax, parg, psum, threshold,
+                      tokens, masked, choice, conf, accept, n_committed, counters);
 }
 
 }  // namespace moestep

@@ -11,12 +11,13 @@
 // every token to its kept candidates and renormalise its gates.
 #include "common.cuh"
 #include "kernels.h"
+#include "launch.cuh"
 
 namespace moestep {
 namespace {
 
-constexpr int kRouteTokens = 8;    // tokens per router CTA
-constexpr int kRouteExperts = 32;  // experts per router CTA (4 per warp)
+constexpr int kRouteTokens = 8;   // tokens per router CTA
+constexpr int kRouteExperts = 8;  // experts per router CTA (one per warp)
 
 // Top-k of one token's logits by one warp.  `s` holds the E logits (shared memory).
 __device__ void topk_one_token(const float* s, int E, int k, int t, int32_t* idx, float* mass, float* gate) {
@@ -52,29 +53,39 @@ __device__ void topk_one_token(const float* s, int E, int k, int t, int32_t* idx
 }
 
 template <typename T>
-__device__ __forceinline__ void load8(const T* p, float* v);
+struct Vec8;  // 8 consecutive elements loaded with 16-byte accesses
 template <>
-__device__ __forceinline__ void load8<bf16>(const bf16* p, float* v) {
-    const uint4 raw = __ldg(reinterpret_cast<const uint4*>(p));
-    const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+struct Vec8<bf16> {
+    uint4 raw;
+    __device__ __forceinline__ void load(const bf16* p) { raw = __ldg(reinterpret_cast<const uint4*>(p)); }
+    __device__ __forceinline__ void to_f32(float* v) const {
+        const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float2 f = __bfloat1622float2(h2[i]);
-        v[2 * i] = f.x;
-        v[2 * i + 1] = f.y;
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = __bfloat1622float2(h2[i]);
+            v[2 * i] = f.x;
+            v[2 * i + 1] = f.y;
+        }
     }
-}
+};
 template <>
-__device__ __forceinline__ void load8<float>(const float* p, float* v) {
-    const float4 a = __ldg(reinterpret_cast<const float4*>(p));
-    const float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-}
+struct Vec8<float> {
+    float4 a, b;
+    __device__ __forceinline__ void load(const float* p) {
+        a = __ldg(reinterpret_cast<const float4*>(p));
+        b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+    }
+    __device__ __forceinline__ void to_f32(float* v) const {
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    }
+};
 
-// grid (ceil(T/8), ceil(E/32)), 256 threads.  Each CTA computes the logits of
-// 8 tokens x 32 experts; the last CTA to finish a token group (counted with an
-// atomic, self-resetting) runs the softmax/top-k for those tokens.
+// grid (ceil(T/8), ceil(E/8)), 256 threads.  Each CTA stages 8 tokens of x in
+// shared memory; each warp computes one expert's logits for those tokens (every
+// lane's 16-byte weight loads are issued before any is used).  The last CTA to
+// finish a token group (atomic counter, reset by that CTA) runs the softmax and
+// top-k of the group's tokens, one warp per token.
 template <typename T>
 __global__ void __launch_bounds__(256) route_kernel(const T* __restrict__ x, const T* __restrict__ Wr, int ntok, int H,
                                                     int E, int k, float* __restrict__ logits, int32_t* idx,
@@ -84,53 +95,80 @@ __global__ void __launch_bounds__(256) route_kernel(const T* __restrict__ x, con
     __shared__ int last;
     const int t0 = blockIdx.x * kRouteTokens;
     const int nt = min(kRouteTokens, ntok - t0);
-    for (int i = threadIdx.x; i < kRouteTokens * H; i += blockDim.x) {
-        const int tt = i / H;
-        xs[i] = tt < nt ? to_f32(x[static_cast<size_t>(t0 + tt) * H + (i - tt * H)]) : 0.f;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int e = blockIdx.y * kRouteExperts + warp;
+    const int nchunk = (H + 255) >> 8;  // warp-wide passes of 256 elements (8 per lane)
+    const T* wrow = Wr + static_cast<size_t>(e < E ? e : 0) * H;
+    pdl_trigger();
+    pdl_wait();  // nothing is read before every earlier kernel in the stream has finished
+    // the first 8 passes' weight loads go out together with the staging loads of x
+    Vec8<T> w[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const int hb = q * 256 + lane * 8;
+        if (e < E && hb < H) w[q].load(wrow + hb);
+    }
+    {
+        const int vec = (kRouteTokens * H) >> 3;  // 8-element vectors of the token tile
+#pragma unroll 4
+        for (int i = threadIdx.x; i < vec; i += blockDim.x) {
+            const int tt = (i * 8) / H;
+            float v[8];
+            if (tt < nt) {
+                Vec8<T> xv;
+                xv.load(x + static_cast<size_t>(t0) * H + static_cast<size_t>(i) * 8);
+                xv.to_f32(v);
+            } else {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) v[q] = 0.f;
+            }
+            *reinterpret_cast<float4*>(&xs[i * 8]) = make_float4(v[0], v[1], v[2], v[3]);
+            *reinterpret_cast<float4*>(&xs[i * 8 + 4]) = make_float4(v[4], v[5], v[6], v[7]);
+        }
     }
     __syncthreads();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int ebase = blockIdx.y * kRouteExperts + warp * 4;
-    float acc[4][kRouteTokens];
+    if (e < E) {
+        float acc[kRouteTokens];
 #pragma unroll
-    for (int a = 0; a < 4; ++a)
+        for (int tt = 0; tt < kRouteTokens; ++tt) acc[tt] = 0.f;
+        for (int c0 = 0; c0 < nchunk; c0 += 8) {
+            if (c0 > 0) {
 #pragma unroll
-        for (int b = 0; b < kRouteTokens; ++b) acc[a][b] = 0.f;
-    for (int hb = lane * 8; hb < H; hb += 256) {
-        float xv[kRouteTokens][8];
+                for (int q = 0; q < 8; ++q) {
+                    const int hb = (c0 + q) * 256 + lane * 8;
+                    if (hb < H) w[q].load(wrow + hb);
+                }
+            }
 #pragma unroll
-        for (int tt = 0; tt < kRouteTokens; ++tt) {
-            const float4 a = *reinterpret_cast<const float4*>(&xs[tt * H + hb]);
-            const float4 b = *reinterpret_cast<const float4*>(&xs[tt * H + hb + 4]);
-            xv[tt][0] = a.x; xv[tt][1] = a.y; xv[tt][2] = a.z; xv[tt][3] = a.w;
-            xv[tt][4] = b.x; xv[tt][5] = b.y; xv[tt][6] = b.z; xv[tt][7] = b.w;
-        }
+            for (int q = 0; q < 8; ++q) {
+                const int hb = (c0 + q) * 256 + lane * 8;
+                if (hb < H) {
+                    float wv[8];
+                    w[q].to_f32(wv);
 #pragma unroll
-        for (int ee = 0; ee < 4; ++ee) {
-            const int e = ebase + ee;
-            if (e < E) {
-                float w[8];
-                load8<T>(Wr + static_cast<size_t>(e) * H + hb, w);
-#pragma unroll
-                for (int tt = 0; tt < kRouteTokens; ++tt)
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) acc[ee][tt] = fmaf(w[q], xv[tt][q], acc[ee][tt]);
+                    for (int tt = 0; tt < kRouteTokens; ++tt) {
+                        const float4 a = *reinterpret_cast<const float4*>(&xs[tt * H + hb]);
+                        const float4 b = *reinterpret_cast<const float4*>(&xs[tt * H + hb + 4]);
+                        float sacc = acc[tt];
+                        sacc = fmaf(wv[0], a.x, sacc); sacc = fmaf(wv[1], a.y, sacc);
+                        sacc = fmaf(wv[2], a.z, sacc); sacc = fmaf(wv[3], a.w, sacc);
+                        sacc = fmaf(wv[4], b.x, sacc); sacc = fmaf(wv[5], b.y, sacc);
+                        sacc = fmaf(wv[6], b.z, sacc); sacc = fmaf(wv[7], b.w, sacc);
+                        acc[tt] = sacc;
+                    }
+                }
             }
         }
-    }
-#pragma unroll
-    for (int ee = 0; ee < 4; ++ee) {
 #pragma unroll
         for (int tt = 0; tt < kRouteTokens; ++tt) {
-            const float v = warp_sum(acc[ee][tt]);
-            const int e = ebase + ee;
-            if (lane == 0 && e < E && tt < nt) logits[static_cast<size_t>(t0 + tt) * E + e] = v;
+            const float v = warp_sum(acc[tt]);
+            if (lane == tt && tt < nt) logits[static_cast<size_t>(t0 + tt) * E + e] = v;
         }
     }
     // ---- last CTA of this token group does the softmax / top-k
+    __threadfence();
+    __syncthreads();
     if (gridDim.y > 1) {
-        __threadfence();
-        __syncthreads();
         if (threadIdx.x == 0) {
             const int prev = atomicAdd(&counters[blockIdx.x], 1);
             last = (prev == static_cast<int>(gridDim.y) - 1);
@@ -139,13 +177,11 @@ __global__ void __launch_bounds__(256) route_kernel(const T* __restrict__ x, con
         __syncthreads();
         if (!last) return;
         __threadfence();
-    } else {
-        __threadfence();
-        __syncthreads();
     }
     float* zs = xs;  // reuse: [8][E]
-    __syncthreads();
-    for (int i = threadIdx.x; i < nt * E; i += blockDim.x) zs[i] = __ldcg(&logits[static_cast<size_t>(t0) * E + i]);
+    const int n = nt * E;
+#pragma unroll 8
+    for (int i = threadIdx.x; i < n; i += blockDim.x) zs[i] = __ldcg(&logits[static_cast<size_t>(t0) * E + i]);
     __syncthreads();
     if (warp < nt) topk_one_token(zs + warp * E, E, k, t0 + warp, idx, mass, gate);
 }
@@ -155,6 +191,8 @@ __global__ void __launch_bounds__(256) topk_from_logits_kernel(const float* __re
                                                                int k, int32_t* idx, float* mass, float* gate) {
     extern __shared__ __align__(16) uint8_t topk_smem[];
     float* zs = reinterpret_cast<float*>(topk_smem);  // [8][E]
+    pdl_trigger();
+    pdl_wait();
     const int warp = threadIdx.x >> 5;
     const int t = blockIdx.x * 8 + warp;
     if (t >= ntok) return;
@@ -210,6 +248,8 @@ __global__ void __launch_bounds__(kCoresetThreads) coreset_kernel(CoresetArgs a)
     const int tid = threadIdx.x;
     const int r = blockIdx.x;
     const int E = a.E, k = a.k, P = a.P;
+    pdl_trigger();
+    pdl_wait();
     // ---------------- phase 1
     if (tid < E) {
         A[tid] = 0;
@@ -264,16 +304,36 @@ __global__ void __launch_bounds__(kCoresetThreads) coreset_kernel(CoresetArgs a)
     __syncthreads();
     for (int tt = tid; tt < P; tt += blockDim.x) {
         const int t = r * P + tt;
+        // candidates in groups of 8 loaded together; the renormaliser is summed in candidate order
         float denom = 0.f;
-        for (int j = 0; j < k; ++j) {
-            const int e = a.idx[t * k + j];
-            if (e >= 0 && e < E && keep[e]) denom += a.mass[t * k + j];
+        for (int j0 = 0; j0 < k; j0 += 8) {
+            int ev[8];
+            float mv[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                ev[q] = (j0 + q < k) ? a.idx[t * k + j0 + q] : -1;
+                mv[q] = (j0 + q < k) ? a.mass[t * k + j0 + q] : 0.f;
+            }
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                if (ev[q] >= 0 && ev[q] < E && keep[ev[q]]) denom += mv[q];
         }
-        for (int j = 0; j < k; ++j) {
-            const int e = a.idx[t * k + j];
-            const bool s = e >= 0 && e < E && keep[e];
-            a.survive[t * k + j] = s ? 1 : 0;
-            a.gate_rr[t * k + j] = (s && denom > 0.f) ? a.mass[t * k + j] / denom : 0.f;
+        for (int j0 = 0; j0 < k; j0 += 8) {
+            int ev[8];
+            float mv[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                ev[q] = (j0 + q < k) ? a.idx[t * k + j0 + q] : -1;
+                mv[q] = (j0 + q < k) ? a.mass[t * k + j0 + q] : 0.f;
+            }
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                if (j0 + q < k) {
+                    const bool sv = ev[q] >= 0 && ev[q] < E && keep[ev[q]];
+                    a.survive[t * k + j0 + q] = sv ? 1 : 0;
+                    a.gate_rr[t * k + j0 + q] = (sv && denom > 0.f) ? mv[q] / denom : 0.f;
+                }
+            }
         }
     }
     // ---------------- phase 2 (one CTA)
@@ -362,6 +422,8 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint4* __restrict__ x
                                                      const int32_t* __restrict__ slot_tok, const int* __restrict__ plan,
                                                      uint4* __restrict__ xp) {
     const int slot = blockIdx.x;
+    pdl_trigger();
+    pdl_wait();
     if (slot >= plan[2]) return;
     const int t = slot_tok[slot];
     for (int i = threadIdx.x; i < row_vec; i += blockDim.x)
@@ -375,51 +437,40 @@ cudaError_t launch_route(int dtype, const void* x, const void* Wr, int T, int H,
     (void)err;
     const dim3 grid((T + kRouteTokens - 1) / kRouteTokens, (E + kRouteExperts - 1) / kRouteExperts);
     const size_t smem = static_cast<size_t>(kRouteTokens) * (H > E ? H : E) * sizeof(float);
+    cudaError_t e;
     if (dtype == MOESTEP_BF16) {
-        if (smem > 48 * 1024) {
-            cudaError_t e = cudaFuncSetAttribute(route_kernel<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 static_cast<int>(smem));
-            if (e != cudaSuccess) return e;
-        }
-        route_kernel<bf16><<<grid, 256, smem, s>>>(static_cast<const bf16*>(x), static_cast<const bf16*>(Wr), T, H,
-                                                   E, k, logits, idx, mass, gate, counters);
-    } else {
-        if (smem > 48 * 1024) {
-            cudaError_t e = cudaFuncSetAttribute(route_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 static_cast<int>(smem));
-            if (e != cudaSuccess) return e;
-        }
-        route_kernel<float><<<grid, 256, smem, s>>>(static_cast<const float*>(x), static_cast<const float*>(Wr), T,
-                                                    H, E, k, logits, idx, mass, gate, counters);
+        if ((e = ensure_smem(route_kernel<bf16>, smem)) != cudaSuccess) return e;
+        return launch_pdl(route_kernel<bf16>, grid, dim3(256), smem, s, static_cast<const bf16*>(x),
+                          static_cast<const bf16*>(Wr), T, H, E, k, logits, idx, mass, gate, counters);
     }
-    return cudaGetLastError();
+    if ((e = ensure_smem(route_kernel<float>, smem)) != cudaSuccess) return e;
+    return launch_pdl(route_kernel<float>, grid, dim3(256), smem, s, static_cast<const float*>(x),
+                      static_cast<const float*>(Wr), T, H, E, k, logits, idx, mass, gate, counters);
 }
 
 cudaError_t launch_topk_from_logits(const float* logits, int T, int E, int k, int32_t* idx, float* mass, float* gate,
                                     cudaStream_t s) {
     const size_t smem = 8ull * E * sizeof(float);
-    topk_from_logits_kernel<<<(T + 7) / 8, 256, smem, s>>>(logits, T, E, k, idx, mass, gate);
-    return cudaGetLastError();
+    cudaError_t e = ensure_smem(topk_from_logits_kernel, smem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(topk_from_logits_kernel, dim3((T + 7) / 8), dim3(256), smem, s, logits, T, E, k, idx, mass,
+                      gate);
 }
 
 int coreset_smem_bytes(int E, int T) { return E * ((T + 31) / 32) * 4; }
 
 cudaError_t launch_coreset(const CoresetArgs& a, cudaStream_t s) {
-    const int smem = coreset_smem_bytes(a.E, a.T);
-    if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(coreset_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-    }
-    coreset_kernel<<<a.R, kCoresetThreads, smem, s>>>(a);
-    return cudaGetLastError();
+    const size_t smem = coreset_smem_bytes(a.E, a.T);
+    cudaError_t e = ensure_smem(coreset_kernel, smem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(coreset_kernel, dim3(a.R), dim3(kCoresetThreads), smem, s, a);
 }
 
 cudaError_t launch_gather(int dtype, const void* x, int H, const int32_t* slot_tok, const int* plan, int max_slots,
                           void* xp, cudaStream_t s) {
     const int row_vec = H * (dtype == MOESTEP_BF16 ? 2 : 4) / 16;
-    gather_kernel<<<max_slots, 256, 0, s>>>(static_cast<const uint4*>(x), row_vec, slot_tok, plan,
-                                            static_cast<uint4*>(xp));
-    return cudaGetLastError();
+    return launch_pdl(gather_kernel, dim3(max_slots), dim3(256), 0, s, static_cast<const uint4*>(x), row_vec,
+                      slot_tok, plan, static_cast<uint4*>(xp));
 }
 
 }  // namespace moestep
