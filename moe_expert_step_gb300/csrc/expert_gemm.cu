@@ -379,7 +379,8 @@ template <int MODE, int NCH>
 cudaError_t launch_one(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b, const GemmParams& p,
                        int grid, cudaStream_t s) {
     constexpr int bytes = smem_bytes(NCH);
-    cudaError_t e = ensure_smem(tc_gemm_kernel<MODE, NCH>, bytes);
+    static int done[64] = {};
+    cudaError_t e = ensure_smem(tc_gemm_kernel<MODE, NCH>, bytes, done);
     if (e != cudaSuccess) return e;
     return launch_pdl(tc_gemm_kernel<MODE, NCH>, dim3(grid), dim3(kThreads), bytes, s, a0, a1, b, p);
 }

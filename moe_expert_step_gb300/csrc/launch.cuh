@@ -22,11 +22,11 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
     return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 
-// Raise a kernel's dynamic shared-memory limit once per device (kept per
-// function instantiation), so repeated calls make no attribute calls.
+// Raise a kernel's dynamic shared-memory limit once per device, so repeated
+// calls make no attribute calls.  `done` is the caller's per-kernel record
+// (one static array per kernel instantiation).
 template <typename K>
-inline cudaError_t ensure_smem(K kern, size_t bytes) {
-    static int done[64] = {};
+inline cudaError_t ensure_smem(K kern, size_t bytes, int (&done)[64]) {
     if (bytes <= 48 * 1024) return cudaSuccess;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);

@@ -438,12 +438,13 @@ cudaError_t launch_route(int dtype, const void* x, const void* Wr, int T, int H,
     const dim3 grid((T + kRouteTokens - 1) / kRouteTokens, (E + kRouteExperts - 1) / kRouteExperts);
     const size_t smem = static_cast<size_t>(kRouteTokens) * (H > E ? H : E) * sizeof(float);
     cudaError_t e;
+    static int done_bf16[64] = {}, done_f32[64] = {};
     if (dtype == MOESTEP_BF16) {
-        if ((e = ensure_smem(route_kernel<bf16>, smem)) != cudaSuccess) return e;
+        if ((e = ensure_smem(route_kernel<bf16>, smem, done_bf16)) != cudaSuccess) return e;
         return launch_pdl(route_kernel<bf16>, grid, dim3(256), smem, s, static_cast<const bf16*>(x),
                           static_cast<const bf16*>(Wr), T, H, E, k, logits, idx, mass, gate, counters);
     }
-    if ((e = ensure_smem(route_kernel<float>, smem)) != cudaSuccess) return e;
+    if ((e = ensure_smem(route_kernel<float>, smem, done_f32)) != cudaSuccess) return e;
     return launch_pdl(route_kernel<float>, grid, dim3(256), smem, s, static_cast<const float*>(x),
                       static_cast<const float*>(Wr), T, H, E, k, logits, idx, mass, gate, counters);
 }
@@ -451,7 +452,8 @@ cudaError_t launch_route(int dtype, const void* x, const void* Wr, int T, int H,
 cudaError_t launch_topk_from_logits(const float* logits, int T, int E, int k, int32_t* idx, float* mass, float* gate,
                                     cudaStream_t s) {
     const size_t smem = 8ull * E * sizeof(float);
-    cudaError_t e = ensure_smem(topk_from_logits_kernel, smem);
+    static int done[64] = {};
+    cudaError_t e = ensure_smem(topk_from_logits_kernel, smem, done);
     if (e != cudaSuccess) return e;
     return launch_pdl(topk_from_logits_kernel, dim3((T + 7) / 8), dim3(256), smem, s, logits, T, E, k, idx, mass,
                       gate);
@@ -461,7 +463,8 @@ int coreset_smem_bytes(int E, int T) { return E * ((T + 31) / 32) * 4; }
 
 cudaError_t launch_coreset(const CoresetArgs& a, cudaStream_t s) {
     const size_t smem = coreset_smem_bytes(a.E, a.T);
-    cudaError_t e = ensure_smem(coreset_kernel, smem);
+    static int done[64] = {};
+    cudaError_t e = ensure_smem(coreset_kernel, smem, done);
     if (e != cudaSuccess) return e;
     return launch_pdl(coreset_kernel, dim3(a.R), dim3(kCoresetThreads), smem, s, a);
 }
