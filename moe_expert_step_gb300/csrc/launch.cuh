@@ -23,11 +23,12 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
 }
 
 // Raise a kernel's dynamic shared-memory limit once per device, so repeated
-// calls make no attribute calls.  `done` is the caller's per-kernel record
-// (one static array per kernel instantiation).
+// calls make no attribute calls (the opt-in is needed whenever static plus
+// dynamic shared memory exceeds 48 KiB).  `done` is the caller's per-kernel
+// record (one static array per kernel instantiation).
 template <typename K>
 inline cudaError_t ensure_smem(K kern, size_t bytes, int (&done)[64]) {
-    if (bytes <= 48 * 1024) return cudaSuccess;
+    if (bytes == 0) return cudaSuccess;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;

@@ -58,6 +58,9 @@ template <>
 struct Vec8<bf16> {
     uint4 raw;
     __device__ __forceinline__ void load(const bf16* p) { raw = __ldg(reinterpret_cast<const uint4*>(p)); }
+    __device__ __forceinline__ void load_shared(const bf16* p) { raw = *reinterpret_cast<const uint4*>(p); }
+    __device__ __forceinline__ void store(bf16* p) const { *reinterpret_cast<uint4*>(p) = raw; }
+    __device__ __forceinline__ static void zero(bf16* p) { *reinterpret_cast<uint4*>(p) = make_uint4(0, 0, 0, 0); }
     __device__ __forceinline__ void to_f32(float* v) const {
         const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
 #pragma unroll
@@ -75,6 +78,18 @@ struct Vec8<float> {
         a = __ldg(reinterpret_cast<const float4*>(p));
         b = __ldg(reinterpret_cast<const float4*>(p) + 1);
     }
+    __device__ __forceinline__ void load_shared(const float* p) {
+        a = *reinterpret_cast<const float4*>(p);
+        b = *(reinterpret_cast<const float4*>(p) + 1);
+    }
+    __device__ __forceinline__ void store(float* p) const {
+        *reinterpret_cast<float4*>(p) = a;
+        *(reinterpret_cast<float4*>(p) + 1) = b;
+    }
+    __device__ __forceinline__ static void zero(float* p) {
+        *reinterpret_cast<float4*>(p) = make_float4(0.f, 0.f, 0.f, 0.f);
+        *(reinterpret_cast<float4*>(p) + 1) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     __device__ __forceinline__ void to_f32(float* v) const {
         v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
         v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
@@ -91,7 +106,7 @@ __global__ void __launch_bounds__(256) route_kernel(const T* __restrict__ x, con
                                                     int E, int k, float* __restrict__ logits, int32_t* idx,
                                                     float* mass, float* gate, int* counters) {
     extern __shared__ __align__(16) uint8_t route_smem[];
-    float* xs = reinterpret_cast<float*>(route_smem);  // [8][H]
+    T* xs = reinterpret_cast<T*>(route_smem);  // [8][H] staged in the input type
     __shared__ int last;
     const int t0 = blockIdx.x * kRouteTokens;
     const int nt = min(kRouteTokens, ntok - t0);
@@ -110,20 +125,16 @@ __global__ void __launch_bounds__(256) route_kernel(const T* __restrict__ x, con
     }
     {
         const int vec = (kRouteTokens * H) >> 3;  // 8-element vectors of the token tile
-#pragma unroll 4
+#pragma unroll 8
         for (int i = threadIdx.x; i < vec; i += blockDim.x) {
             const int tt = (i * 8) / H;
-            float v[8];
+            Vec8<T> xv;
             if (tt < nt) {
-                Vec8<T> xv;
                 xv.load(x + static_cast<size_t>(t0) * H + static_cast<size_t>(i) * 8);
-                xv.to_f32(v);
+                xv.store(xs + static_cast<size_t>(i) * 8);
             } else {
-#pragma unroll
-                for (int q = 0; q < 8; ++q) v[q] = 0.f;
+                Vec8<T>::zero(xs + static_cast<size_t>(i) * 8);
             }
-            *reinterpret_cast<float4*>(&xs[i * 8]) = make_float4(v[0], v[1], v[2], v[3]);
-            *reinterpret_cast<float4*>(&xs[i * 8 + 4]) = make_float4(v[4], v[5], v[6], v[7]);
         }
     }
     __syncthreads();
@@ -147,13 +158,13 @@ __global__ void __launch_bounds__(256) route_kernel(const T* __restrict__ x, con
                     w[q].to_f32(wv);
 #pragma unroll
                     for (int tt = 0; tt < kRouteTokens; ++tt) {
-                        const float4 a = *reinterpret_cast<const float4*>(&xs[tt * H + hb]);
-                        const float4 b = *reinterpret_cast<const float4*>(&xs[tt * H + hb + 4]);
+                        Vec8<T> xv;
+                        xv.load_shared(xs + static_cast<size_t>(tt) * H + hb);
+                        float xf[8];
+                        xv.to_f32(xf);
                         float sacc = acc[tt];
-                        sacc = fmaf(wv[0], a.x, sacc); sacc = fmaf(wv[1], a.y, sacc);
-                        sacc = fmaf(wv[2], a.z, sacc); sacc = fmaf(wv[3], a.w, sacc);
-                        sacc = fmaf(wv[4], b.x, sacc); sacc = fmaf(wv[5], b.y, sacc);
-                        sacc = fmaf(wv[6], b.z, sacc); sacc = fmaf(wv[7], b.w, sacc);
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) sacc = fmaf(wv[u], xf[u], sacc);
                         acc[tt] = sacc;
                     }
                 }
@@ -178,7 +189,7 @@ __global__ void __launch_bounds__(256) route_kernel(const T* __restrict__ x, con
         if (!last) return;
         __threadfence();
     }
-    float* zs = xs;  // reuse: [8][E]
+    float* zs = reinterpret_cast<float*>(route_smem);  // reuse: [8][E]
     const int n = nt * E;
 #pragma unroll 8
     for (int i = threadIdx.x; i < n; i += blockDim.x) zs[i] = __ldcg(&logits[static_cast<size_t>(t0) * E + i]);
@@ -231,6 +242,8 @@ __device__ V block_inclusive_scan(V v, V* warp_tot) {
     return v;
 }
 
+constexpr int kCandCache = 2048;  // candidates of one request kept in shared memory
+
 // grid R, 1024 threads.  Phase 1 (every CTA): the coreset of request blockIdx.x.
 // Phase 2 (the last CTA to finish, or the only one): the grouped-by-expert
 // work plan over the union of all requests' kept experts.
@@ -240,14 +253,20 @@ __global__ void __launch_bounds__(kCoresetThreads) coreset_kernel(CoresetArgs a)
     __shared__ int cnt[1024];
     __shared__ int order[1024];
     __shared__ int keep[1024];
+    __shared__ int cidx[kCandCache];
+    __shared__ float cmass[kCandCache];
+    __shared__ uint8_t csurv[kCandCache];
     __shared__ long long wtot64[32];
     __shared__ int wtot32[32];
-    __shared__ int s_last;
+    __shared__ int s_last, s_nr, s_nrc;
     extern __shared__ uint32_t masks[];  // phase 2: [E][ceil(T/32)]
 
     const int tid = threadIdx.x;
     const int r = blockIdx.x;
     const int E = a.E, k = a.k, P = a.P;
+    const int nc = P * k;                    // candidates of this request
+    const bool cached = nc <= kCandCache;
+    const int base = r * nc;                 // first candidate of this request in idx/mass
     pdl_trigger();
     pdl_wait();
     // ---------------- phase 1
@@ -256,30 +275,45 @@ __global__ void __launch_bounds__(kCoresetThreads) coreset_kernel(CoresetArgs a)
         cnt[tid] = 0;
     }
     __syncthreads();
-    for (int c = tid; c < P * k; c += blockDim.x) {
-        const int t = r * P + c / k;
-        const int j = c - (c / k) * k;
-        const int e = a.idx[t * k + j];
+    for (int c = tid; c < nc; c += blockDim.x) {
+        const int e = a.idx[base + c];
+        const float ms = a.mass[base + c];
+        if (cached) {
+            cidx[c] = e;
+            cmass[c] = ms;
+        }
         if (e < 0 || e >= E) {
             record_error(a.err, kErrBadInput);
             continue;
         }
-        const long long q = __float2ll_rn(a.mass[t * k + j] * 0x1p54f);
+        const long long q = __float2ll_rn(ms * 0x1p54f);
         atomicAdd(reinterpret_cast<unsigned long long*>(&A[e]), static_cast<unsigned long long>(q));
         atomicAdd(&cnt[e], 1);
     }
     __syncthreads();
-    // rank of every candidate expert: (aggregate desc, id asc)
-    int my_rank = -1;
-    if (tid < E && cnt[tid] > 0) {
-        const long long mine = A[tid];
+    // rank of every candidate expert, (aggregate desc, id asc): `parts` threads share one expert
+    int parts = 1;
+    while (parts < 32 && parts * 2 * E <= kCoresetThreads) parts *= 2;
+    {
+        const int e = tid / parts, part = tid % parts;
         int rk = 0;
-        for (int e2 = 0; e2 < E; ++e2)
-            if (cnt[e2] > 0 && (A[e2] > mine || (A[e2] == mine && e2 < tid))) ++rk;
-        my_rank = rk;
-        order[rk] = tid;
+        const bool mine_valid = e < E && cnt[e] > 0;
+        if (mine_valid) {
+            const long long mine = A[e];
+            const int per = (E + parts - 1) / parts;
+            const int lo = part * per, hi = min(E, lo + per);
+            for (int e2 = lo; e2 < hi; ++e2)
+                if (cnt[e2] > 0 && (A[e2] > mine || (A[e2] == mine && e2 < e))) ++rk;
+        }
+        for (int o = 1; o < parts; o <<= 1) rk += __shfl_xor_sync(0xffffffffu, rk, o);
+        if (mine_valid && part == 0) order[rk] = e;
+        if (part == 0 && e < E) keep[e] = mine_valid ? rk : -1;  // rank for now, flag below
     }
-    const int nC = __syncthreads_count(my_rank >= 0);
+    int nC = 0;
+    {
+        const int e = tid;
+        nC = __syncthreads_count(e < E && cnt[e] > 0);
+    }
     long long v = (tid < nC) ? A[order[tid]] : 0;
     v = block_inclusive_scan<long long>(v, wtot64);
     if (tid < nC) cum[tid] = v;
@@ -298,21 +332,23 @@ __global__ void __launch_bounds__(kCoresetThreads) coreset_kernel(CoresetArgs a)
         m = 1 + __syncthreads_count(tid < nC && cum[tid] < target);
         m = m > nC ? nC : m;
     }
-    if (tid < E) keep[tid] = (my_rank >= 0 && my_rank < m);
+    if (tid < E) keep[tid] = (keep[tid] >= 0 && keep[tid] < m);
     if (tid < m) a.sel[r * E + tid] = order[tid];
     if (tid == 0) a.n_sel[r] = m;
     __syncthreads();
     for (int tt = tid; tt < P; tt += blockDim.x) {
-        const int t = r * P + tt;
-        // candidates in groups of 8 loaded together; the renormaliser is summed in candidate order
+        const int c0 = tt * k;
+        // candidates in groups of 8; the renormaliser is summed in candidate order
         float denom = 0.f;
         for (int j0 = 0; j0 < k; j0 += 8) {
             int ev[8];
             float mv[8];
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
-                ev[q] = (j0 + q < k) ? a.idx[t * k + j0 + q] : -1;
-                mv[q] = (j0 + q < k) ? a.mass[t * k + j0 + q] : 0.f;
+                const int c = c0 + j0 + q;
+                const bool in = j0 + q < k;
+                ev[q] = in ? (cached ? cidx[c] : a.idx[base + c]) : -1;
+                mv[q] = in ? (cached ? cmass[c] : a.mass[base + c]) : 0.f;
             }
 #pragma unroll
             for (int q = 0; q < 8; ++q)
@@ -323,20 +359,25 @@ __global__ void __launch_bounds__(kCoresetThreads) coreset_kernel(CoresetArgs a)
             float mv[8];
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
-                ev[q] = (j0 + q < k) ? a.idx[t * k + j0 + q] : -1;
-                mv[q] = (j0 + q < k) ? a.mass[t * k + j0 + q] : 0.f;
+                const int c = c0 + j0 + q;
+                const bool in = j0 + q < k;
+                ev[q] = in ? (cached ? cidx[c] : a.idx[base + c]) : -1;
+                mv[q] = in ? (cached ? cmass[c] : a.mass[base + c]) : 0.f;
             }
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
+                const int c = c0 + j0 + q;
                 if (j0 + q < k) {
                     const bool sv = ev[q] >= 0 && ev[q] < E && keep[ev[q]];
-                    a.survive[t * k + j0 + q] = sv ? 1 : 0;
-                    a.gate_rr[t * k + j0 + q] = (sv && denom > 0.f) ? mv[q] / denom : 0.f;
+                    a.survive[base + c] = sv ? 1 : 0;
+                    a.gate_rr[base + c] = (sv && denom > 0.f) ? mv[q] / denom : 0.f;
+                    if (cached) csurv[c] = sv ? 1 : 0;
                 }
             }
         }
     }
     // ---------------- phase 2 (one CTA)
+    const bool local = gridDim.x == 1 && cached;  // the whole block's candidates are in shared memory
     if (gridDim.x > 1) {
         __threadfence();
         __syncthreads();
@@ -358,8 +399,9 @@ __global__ void __launch_bounds__(kCoresetThreads) coreset_kernel(CoresetArgs a)
     if (tid < E) cnt[tid] = 0;
     __syncthreads();
     for (int c = tid; c < T * k; c += blockDim.x) {
-        if (__ldcg(&a.survive[c])) {
-            const int e = __ldcg(&a.idx[c]);
+        const bool sv = local ? csurv[c] != 0 : __ldcg(&a.survive[c]) != 0;
+        if (sv) {
+            const int e = local ? cidx[c] : __ldcg(&a.idx[c]);
             const int t = c / k;
             atomicAdd(&cnt[e], 1);
             atomicOr(&masks[e * TW + (t >> 5)], 1u << (t & 31));
@@ -377,7 +419,6 @@ __global__ void __launch_bounds__(kCoresetThreads) coreset_kernel(CoresetArgs a)
         for (int i = 0; i < my_nch; ++i)
             a.chunks[chunk_base + i] = make_int4(tid, slot_base + i * a.nch, min(a.nch, my_cnt - i * a.nch), 0);
     }
-    __shared__ int s_nr, s_nrc;
     if (tid == kCoresetThreads - 1) {
         s_nr = slot_end;
         s_nrc = chunk_end;
@@ -385,8 +426,9 @@ __global__ void __launch_bounds__(kCoresetThreads) coreset_kernel(CoresetArgs a)
     __syncthreads();
     const int NR = s_nr, nrc = s_nrc;
     for (int c = tid; c < T * k; c += blockDim.x) {
-        if (__ldcg(&a.survive[c])) {
-            const int e = __ldcg(&a.idx[c]);
+        const bool sv = local ? csurv[c] != 0 : __ldcg(&a.survive[c]) != 0;
+        if (sv) {
+            const int e = local ? cidx[c] : __ldcg(&a.idx[c]);
             const int t = c / k;
             const int w = t >> 5;
             int pos = order[e];
@@ -436,7 +478,10 @@ cudaError_t launch_route(int dtype, const void* x, const void* Wr, int T, int H,
                          int32_t* idx, float* mass, float* gate, int* counters, int* err, cudaStream_t s) {
     (void)err;
     const dim3 grid((T + kRouteTokens - 1) / kRouteTokens, (E + kRouteExperts - 1) / kRouteExperts);
-    const size_t smem = static_cast<size_t>(kRouteTokens) * (H > E ? H : E) * sizeof(float);
+    const size_t esz = dtype == MOESTEP_BF16 ? 2 : 4;
+    const size_t xs_bytes = static_cast<size_t>(kRouteTokens) * H * esz;
+    const size_t zs_bytes = static_cast<size_t>(kRouteTokens) * E * sizeof(float);
+    const size_t smem = xs_bytes > zs_bytes ? xs_bytes : zs_bytes;
     cudaError_t e;
     static int done_bf16[64] = {}, done_f32[64] = {};
     if (dtype == MOESTEP_BF16) {
