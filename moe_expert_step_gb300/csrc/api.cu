@@ -264,15 +264,15 @@ int run_coreset(const Ctx& c, int R, const float* top_p, const int32_t* idx, con
     return MOESTEP_OK;
 }
 
-// experts (fp32: gather + FFMA; bf16: tcgen05 gate/up reading token rows of x
-// by TMA gather, then down); leaves y (per slot) in the workspace
+// gather + experts (fp32: FFMA; bf16: tcgen05 gate/up then down); leaves y
+// (per slot) in the workspace
 int run_experts(const Ctx& c, int R, const void* x, const moestep_layer* layer) {
     const moestep_dims* d = c.d;
     const Layout& L = c.L;
     const int* plan = at<int>(c.ws, L.hdr) + 32;
+    MOESTEP_LAUNCH(2, launch_gather(d->dtype, x, d->H, at<int32_t>(c.ws, L.slot_tok), plan, L.max_slots,
+                                    at<void>(c.ws, L.xp), c.s));
     if (d->dtype == MOESTEP_F32) {
-        MOESTEP_LAUNCH(2, launch_gather(d->dtype, x, d->H, at<int32_t>(c.ws, L.slot_tok), plan, L.max_slots,
-                                        at<void>(c.ws, L.xp), c.s));
         MOESTEP_LAUNCH(3, launch_f32_gateup(d->H, d->E, d->I, d->Is, L.max_slots, at<float>(c.ws, L.xp),
                                             at<int32_t>(c.ws, L.slot_exp), plan, static_cast<const float*>(layer->Wgu),
                                             static_cast<const float*>(layer->Wsgu), at<float>(c.ws, L.act), L.act_ld,
@@ -284,19 +284,17 @@ int run_experts(const Ctx& c, int R, const void* x, const moestep_layer* layer) 
     }
     if (get_encode() != MOESTEP_OK) return MOESTEP_ECUDA;
     const bool sh = d->Is > 0;
-    CUtensorMap mgu, msgu, mx, md, msd, mact;
+    CUtensorMap mgu, msgu, mxp, md, msd, mact;
     int rc;
     if ((rc = make_map(&mgu, layer->Wgu, d->H, 2ull * d->E * d->I, 64))) return rc;
     if ((rc = make_map(&msgu, sh ? layer->Wsgu : layer->Wgu, d->H, sh ? 2ull * d->Is : 128, 64))) return rc;
-    if ((rc = make_map(&mx, x, d->H, L.T, 1))) return rc;
+    if ((rc = make_map(&mxp, at<void>(c.ws, L.xp), d->H, L.max_slots, 16))) return rc;
     if ((rc = make_map(&md, layer->Wd, d->I, 1ull * d->E * d->H, 64))) return rc;
     if ((rc = make_map(&msd, sh ? layer->Wsd : layer->Wd, sh ? d->Is : d->I, d->H, 64))) return rc;
     if ((rc = make_map(&mact, at<void>(c.ws, L.act), L.act_ld, L.max_slots, 16))) return rc;
     GemmParams g{};
     g.plan = plan;
     g.chunks = at<int4>(c.ws, L.chunks);
-    g.slot_tok = at<int32_t>(c.ws, L.slot_tok);
-    g.n_tok = L.T;
     g.err = at<int>(c.ws, L.hdr);
     g.timeout_ns = g_timeout_ns;
     g.tile_rows = 128;
@@ -308,7 +306,7 @@ int run_experts(const Ctx& c, int R, const void* x, const moestep_layer* layer) 
     g.rows_per_expert = 2 * d->I;
     g.out = at<void>(c.ws, L.act);
     g.out_ld = L.act_ld;
-    MOESTEP_LAUNCH(3, launch_tc_gemm(kGateUp, L.nch, mgu, msgu, mx, g, c.sms, c.s));
+    MOESTEP_LAUNCH(3, launch_tc_gemm(kGateUp, L.nch, mgu, msgu, mxp, g, c.sms, c.s));
     // down: 128-row tiles of the hidden dimension
     g.routed_tiles = d->H / 128;
     g.shared_tiles = d->H / 128;

@@ -185,56 +185,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             const Unit w = decode_unit<MODE, NCH>(u, p, nrc);
             const int nb = (w.n + 15) >> 4;
             const CUtensorMap* mA = w.shared ? &mapA1 : &mapA0;
-            // gate/up: token row of each of this chunk's slots (lane j holds slots j, j+32, ...);
-            // padding rows repeat a valid row and only feed accumulator columns nobody reads
-            int tok[NCH / 32];
-            if (MODE == kGateUp) {
-#pragma unroll
-                for (int q = 0; q < NCH / 32; ++q) {
-                    const int j = lane + 32 * q;
-                    const int t = (j < w.n) ? p.slot_tok[w.slot0 + j] : 0;
-                    tok[q] = (t >= 0 && t < p.n_tok) ? t : 0;
-                }
-            }
             for (int kb = 0; kb < w.kb; ++kb) {
                 int good = 1;
-                if (lane == 0) good = tc::mbar_wait(&empty[stage], phase ^ 1u, abortv, tmo);
+                if (lane == 0) {
+                    good = tc::mbar_wait(&empty[stage], phase ^ 1u, abortv, tmo);
+                    if (good) {
+                        uint8_t* sa = smem + stage * SB;
+                        tc::mbar_arrive_expect_tx(&full[stage], kABytes + nb * kBoxBBytes);
+                        tc::tma_load_2d_hint(sa, mA, &full[stage], kb * 64, w.rowA0, pol);
+                        tc::tma_load_2d_hint(sa + kABytes / 2, mA, &full[stage], kb * 64, w.rowA1, pol);
+                        for (int b = 0; b < nb; ++b)
+                            tc::tma_load_2d(sa + kABytes + b * kBoxBBytes, &mapB, &full[stage], kb * 64,
+                                            w.slot0 + 16 * b);
+                        issued |= 1u << stage;
+                        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                    }
+                }
                 good = __shfl_sync(0xffffffffu, good, 0);
                 if (!good) {
                     ok = false;
                     if (lane == 0) record_timeout(p.err, 1, u, kb, stage, phase, n_units, w.n);
                     break;
                 }
-                uint8_t* sa = smem + stage * SB;
-                if (lane == 0) {
-                    tc::mbar_arrive_expect_tx(&full[stage], kABytes + nb * kBoxBBytes);
-                    tc::tma_load_2d_hint(sa, mA, &full[stage], kb * 64, w.rowA0, pol);
-                    tc::tma_load_2d_hint(sa + kABytes / 2, mA, &full[stage], kb * 64, w.rowA1, pol);
-                    if (MODE != kGateUp)
-                        for (int b = 0; b < nb; ++b)
-                            tc::tma_load_2d(sa + kABytes + b * kBoxBBytes, &mapB, &full[stage], kb * 64,
-                                            w.slot0 + 16 * b);
-                    issued |= 1u << stage;
-                    issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-                }
-                if (MODE == kGateUp) {
-#pragma unroll
-                    for (int q = 0; q < NCH / 32; ++q) {
-                        for (int g8 = 0; g8 < 8; ++g8) {  // groups of 4 rows
-                            const int g = q * 8 + g8;
-                            if (g >= 4 * nb) break;
-                            const int l0 = g8 * 4;
-                            const int r0 = __shfl_sync(0xffffffffu, tok[q], l0);
-                            const int r1 = __shfl_sync(0xffffffffu, tok[q], l0 + 1);
-                            const int r2 = __shfl_sync(0xffffffffu, tok[q], l0 + 2);
-                            const int r3 = __shfl_sync(0xffffffffu, tok[q], l0 + 3);
-                            if (lane == 0)
-                                tc::tma_gather4(sa + kABytes + g * 512, &mapB, &full[stage], kb * 64, r0, r1, r2,
-                                                r3);
-                        }
-                    }
-                }
-                __syncwarp();
                 if (++stage == STAGES) {
                     stage = 0;
                     phase ^= 1u;

@@ -32,9 +32,6 @@ struct GemmParams {
     int* parg;
     float* psum;
     float* logits;         // optional [n_pos][V]
-    // gate/up: B rows are gathered from the layer input by token (slot -> token map)
-    const int32_t* slot_tok;
-    int n_tok;             // rows of the layer input (valid gather rows)
     // outputs of expert modes: act (bf16, gate/up) or y (fp32, down)
     void* out;
     int out_ld;
@@ -42,8 +39,7 @@ struct GemmParams {
     unsigned long long timeout_ns;
 };
 
-// mapA0: routed weights (or LM head), mapA1: shared-expert weights, mapB: activations
-// (gate/up: the layer input [T][H] with a one-row box, read by token gather).
+// mapA0: routed weights (or LM head), mapA1: shared-expert weights, mapB: activations.
 cudaError_t launch_tc_gemm(int mode, int nch, const CUtensorMap& a0, const CUtensorMap& a1,
                            const CUtensorMap& b, const GemmParams& p, int grid, cudaStream_t s);
 int tc_gemm_smem_bytes(int nch);

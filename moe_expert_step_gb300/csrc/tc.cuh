@@ -83,17 +83,7 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m, uin
         "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_addr(bar)), "r"(x), "r"(y)
         : "memory");
 }
-// Gather four rows (r0..r3) of a 2D tensor whose map has a one-row box: 4 x
-// 128 bytes land as four consecutive rows of the 128-byte swizzled layout.
-__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* m, uint64_t* bar, int x, int r0, int r1,
-                                            int r2, int r3) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%3, "
-        "%4, %5, %6, %7}], [%2];" ::"r"(smem_addr(dst)),
-        "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_addr(bar)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
-        : "memory");
-}
-// Same as tma_load_2d, with an L2 eviction-priority policy (for data read exactly once).
+// Same, with an L2 eviction-priority policy (for data read exactly once).
 __device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* m, uint64_t* bar, int x, int y,
                                                  uint64_t policy) {
     asm volatile(
