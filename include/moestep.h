@@ -123,7 +123,7 @@ int moe_block_route(const moestep_dims* dims, int T, const void* x, const void* 
  * allocator, a fixed embedded budget) and that therefore cannot call
  * cudaMalloc or hand over a scratch buffer.
  * Scratch (router logits when `logits` is NULL, and the completion counters)
- * lives in one fixed array inside the library, 516 KiB per device, held by
+ * lives in one fixed array inside the library, 520 KiB per device, held by
  * every GPU that loads the library until the process exits.  Limits:
  * T * E <= 131072 and T <= 8192; larger calls return MOESTEP_EUNSUPPORTED.
  * Arguments as in moe_block_route.  The first call on a device looks up the

@@ -51,7 +51,7 @@ Layout make_layout(const moestep_dims& d, int R) {
     L.max_chunks = T * d.k + d.E + T + 1;
     L.act_ld = d.I > d.Is ? d.I : d.Is;
     L.nch = nch_for(T);
-    L.route_groups = (T + 7) / 8;
+    L.route_groups = (T + kRouteTokensPerCta - 1) / kRouteTokensPerCta;
     const int tiles_tc = (d.V + 127) / 128 * 4;
     const int tiles_logit = (d.V + kLogitTile - 1) / kLogitTile;
     L.n_ptiles = tiles_tc > tiles_logit ? tiles_tc : tiles_logit;
@@ -235,7 +235,7 @@ int run_route(const Ctx& c, int T, const void* x, const void* Wr, int32_t* idx, 
 }
 
 int run_coreset(const Ctx& c, int R, const float* top_p, const int32_t* idx, const float* mass, int32_t* n_sel,
-                int32_t* sel, uint8_t* survive, float* gate_rr) {
+                int32_t* sel, uint8_t* survive, float* gate_rr, const void* prefetch_wgu = nullptr) {
     const moestep_dims* d = c.d;
     CoresetArgs a{};
     a.R = R;
@@ -260,6 +260,12 @@ int run_coreset(const Ctx& c, int R, const float* top_p, const int32_t* idx, con
     a.nch = c.L.nch;
     a.has_shared = d->Is > 0;
     a.err = at<int>(c.ws, c.L.hdr);
+    if (prefetch_wgu != nullptr && d->dtype == MOESTEP_BF16) {
+        a.pf_base = static_cast<const char*>(prefetch_wgu);
+        a.pf_stride = 2ll * d->I * d->H * 2;
+        a.pf_experts = (a.pf_stride % (64 * 1024) == 0) ? kPrefetchExperts : 0;
+        if (a.pf_experts == 0) a.pf_base = nullptr;
+    }
     MOESTEP_LAUNCH(1, launch_coreset(a, c.s));
     return MOESTEP_OK;
 }
@@ -569,7 +575,7 @@ int block_decode_step(const moestep_dims* dims, int R, int n_layers, const moest
         int32_t* sel = (trace && trace->sel) ? trace->sel + static_cast<size_t>(l) * R * dims->E : at<int32_t>(ws, L.sel);
         MOESTEP_TRY(run_route(c, T, x, layers[l].Wr, idx, at<float>(ws, L.mass), at<float>(ws, L.gate), nullptr));
         MOESTEP_TRY(run_coreset(c, R, top_p, idx, at<float>(ws, L.mass), nsel, sel,
-                                at<uint8_t>(ws, L.survive), at<float>(ws, L.gaterr)));
+                                at<uint8_t>(ws, L.survive), at<float>(ws, L.gaterr), layers[l].Wgu));
         MOESTEP_TRY(run_experts(c, R, x, &layers[l]));
         MOESTEP_LAUNCH(5, launch_combine(1, dims->dtype, T, dims->H, k, at<float>(ws, L.y),
                                          at<int32_t>(ws, L.slot_of), at<int32_t>(ws, L.slot_sh),

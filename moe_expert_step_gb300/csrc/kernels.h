@@ -45,6 +45,7 @@ cudaError_t launch_tc_gemm(int mode, int nch, const CUtensorMap& a0, const CUten
 int tc_gemm_smem_bytes(int nch);
 
 // ------------------------------------------------------------------ routing / coreset / plan
+constexpr int kRouteTokensPerCta = 4;  // tokens per router CTA = tokens per completion counter
 struct CoresetArgs {
     int R, P, k, E, T;
     const float* top_p;
@@ -64,7 +65,12 @@ struct CoresetArgs {
     int nch;
     int has_shared;
     int* err;
+    // optional L2 prefetch of the top-ranked kept experts' gate/up weights
+    const char* pf_base;   // Wgu of the layer (NULL: no prefetch)
+    long long pf_stride;   // bytes per expert
+    int pf_experts;        // experts to prefetch per launch
 };
+constexpr int kPrefetchExperts = 16;  // 64 MiB of gate/up weights at the Clover layer shape
 
 cudaError_t launch_route(int dtype, const void* x, const void* Wr, int T, int H, int E, int k, float* logits,
                          int32_t* idx, float* mass, float* gate, int* counters, int* err, cudaStream_t s);

@@ -72,7 +72,10 @@ __global__ void __launch_bounds__(256) combine_kernel(int H, int k, const float*
     }
     float ss = 0.f;
     const size_t row = static_cast<size_t>(t) * H;
-    for (int c = threadIdx.x * 4; c < H; c += 1024) {
+    constexpr int kKeep = 4;  // float4 columns per thread kept in registers (H <= 4096)
+    float4 hv[kKeep];
+    int i = 0;
+    for (int c = threadIdx.x * 4; c < H; c += 1024, ++i) {
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         if (MODE != 2) {
             // slots in groups of 8 loaded together, added in candidate order
@@ -110,20 +113,30 @@ __global__ void __launch_bounds__(256) combine_kernel(int H, int k, const float*
             const float4 v = make_float4(base.x + acc.x, base.y + acc.y, base.z + acc.z, base.w + acc.w);
             *reinterpret_cast<float4*>(h + row + c) = v;
             ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+#pragma unroll
+            for (int q = 0; q < kKeep; ++q)
+                if (q == i) hv[q] = v;
         }
     }
     if (MODE == 0) return;
     const float tot = block_sum_256(ss, red);
     const float inv = 1.0f / sqrtf(tot / static_cast<float>(H) + kRmsEps);
-    for (int c = threadIdx.x * 4; c < H; c += 1024) {
-        const float4 v = *reinterpret_cast<const float4*>(h + row + c);
+    i = 0;
+    for (int c = threadIdx.x * 4; c < H; c += 1024, ++i) {
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (i < kKeep) {
+#pragma unroll
+            for (int q = 0; q < kKeep; ++q)
+                if (q == i) v = hv[q];
+        } else {
+            v = *reinterpret_cast<const float4*>(h + row + c);
+        }
         const float4 n = make_float4(v.x * inv, v.y * inv, v.z * inv, v.w * inv);
         store4<T>(x + row + c, n);
         if (x_f32 != nullptr) *reinterpret_cast<float4*>(x_f32 + row + c) = roundtrip4<T>(n);
     }
 }
 
-// A committed token id outside [0, V) yields a NaN row instead of an out-of-range read.
 template <typename T>
 __global__ void __launch_bounds__(256) embed_kernel(int H, int P, int V, const int32_t* __restrict__ tokens,
                                                     const uint8_t* __restrict__ masked, const T* __restrict__ emb,

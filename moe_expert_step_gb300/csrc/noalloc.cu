@@ -18,7 +18,7 @@
 namespace {
 
 constexpr int kMaxLogits = 131072;  // T * E of one call (512 KiB of fp32 logits)
-constexpr int kMaxGroups = 1024;    // ceil(T / 8) completion counters
+constexpr int kMaxGroups = 2048;    // completion counters, one per kRouteTokensPerCta tokens
 
 struct RouteScratch {
     float logits[kMaxLogits];
@@ -55,13 +55,14 @@ extern "C" int moe_block_route_noalloc(const moestep_dims* dims, int T, const vo
     if (rc != MOESTEP_OK) return rc;
     if (T <= 0 || !x || !Wr || !idx || !mass || !gate) return MOESTEP_EINVAL;
     if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(Wr)) & 15u) return MOESTEP_EALIGN;
-    if (static_cast<long long>(T) * dims->E > kMaxLogits || (T + 7) / 8 > kMaxGroups) return MOESTEP_EUNSUPPORTED;
+    const int groups = (T + moestep::kRouteTokensPerCta - 1) / moestep::kRouteTokensPerCta;
+    if (static_cast<long long>(T) * dims->E > kMaxLogits || groups > kMaxGroups) return MOESTEP_EUNSUPPORTED;
     if ((rc = moestep::device_ok(nullptr)) != MOESTEP_OK) return rc;
     RouteScratch* s = nullptr;
     if ((rc = scratch_address(&s)) != MOESTEP_OK) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     // the completion counters must start at zero; the logits are fully written before they are read
-    if (cudaMemsetAsync(s->counters, 0, sizeof(int) * ((T + 7) / 8), st) != cudaSuccess) return MOESTEP_ECUDA;
+    if (cudaMemsetAsync(s->counters, 0, sizeof(int) * groups, st) != cudaSuccess) return MOESTEP_ECUDA;
     float* lg = logits ? logits : s->logits;
     if (moestep::launch_route(dims->dtype, x, Wr, T, dims->H, dims->E, dims->k, lg, idx, mass, gate, s->counters,
                               nullptr, st) != cudaSuccess)

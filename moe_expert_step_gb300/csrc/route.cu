@@ -16,7 +16,7 @@
 namespace moestep {
 namespace {
 
-constexpr int kRouteTokens = 8;   // tokens per router CTA
+constexpr int kRouteTokens = kRouteTokensPerCta;
 constexpr int kRouteExperts = 8;  // experts per router CTA (one per warp)
 
 // Top-k of one token's logits by one warp.  `s` holds the E logits (shared memory).
@@ -243,6 +243,12 @@ __device__ V block_inclusive_scan(V v, V* warp_tot) {
 }
 
 constexpr int kCandCache = 2048;  // candidates of one request kept in shared memory
+constexpr int kPrefetchPiece = 64 * 1024;
+
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
+                 : "memory");
+}
 
 // grid R, 1024 threads.  Phase 1 (every CTA): the coreset of request blockIdx.x.
 // Phase 2 (the last CTA to finish, or the only one): the grouped-by-expert
@@ -267,13 +273,19 @@ __global__ void __launch_bounds__(kCoresetThreads) coreset_kernel(CoresetArgs a)
     const int nc = P * k;                    // candidates of this request
     const bool cached = nc <= kCandCache;
     const int base = r * nc;                 // first candidate of this request in idx/mass
+    // one request whose candidates all fit in shared memory: the plan reuses phase 1's counts
+    const bool local = gridDim.x == 1 && cached;
+    const int TWl = (P + 31) >> 5;
     pdl_trigger();
     pdl_wait();
+    const float tp = a.top_p[r];
     // ---------------- phase 1
     if (tid < E) {
         A[tid] = 0;
         cnt[tid] = 0;
     }
+    if (local)
+        for (int i = tid; i < E * TWl; i += blockDim.x) masks[i] = 0u;
     __syncthreads();
     for (int c = tid; c < nc; c += blockDim.x) {
         const int e = a.idx[base + c];
@@ -289,6 +301,10 @@ __global__ void __launch_bounds__(kCoresetThreads) coreset_kernel(CoresetArgs a)
         const long long q = __float2ll_rn(ms * 0x1p54f);
         atomicAdd(reinterpret_cast<unsigned long long*>(&A[e]), static_cast<unsigned long long>(q));
         atomicAdd(&cnt[e], 1);
+        if (local) {
+            const int t = c / k;
+            atomicOr(&masks[e * TWl + (t >> 5)], 1u << (t & 31));
+        }
     }
     __syncthreads();
     // rank of every candidate expert, (aggregate desc, id asc): `parts` threads share one expert
@@ -319,7 +335,6 @@ __global__ void __launch_bounds__(kCoresetThreads) coreset_kernel(CoresetArgs a)
     if (tid < nC) cum[tid] = v;
     __syncthreads();
     const long long total = nC > 0 ? cum[nC - 1] : 0;
-    const float tp = a.top_p[r];
     int m;
     if (!(tp > 0.0f)) {  // NaN or non-positive fraction: keep everything and flag the input
         if (tid == 0) record_error(a.err, kErrBadInput);
@@ -335,6 +350,17 @@ __global__ void __launch_bounds__(kCoresetThreads) coreset_kernel(CoresetArgs a)
     if (tid < E) keep[tid] = (keep[tid] >= 0 && keep[tid] < m);
     if (tid < m) a.sel[r * E + tid] = order[tid];
     if (tid == 0) a.n_sel[r] = m;
+    if (a.pf_base != nullptr) {
+        // pull the highest-ranked kept experts' gate/up weights into L2 while HBM is otherwise idle
+        const int ne = min(m, max(1, a.pf_experts / static_cast<int>(gridDim.x)));
+        const int pieces = static_cast<int>(a.pf_stride / kPrefetchPiece);
+        for (int i = tid; i < ne * pieces; i += blockDim.x) {
+            const int rank = i / pieces, piece = i - rank * pieces;
+            prefetch_l2(a.pf_base + static_cast<long long>(order[rank]) * a.pf_stride +
+                            static_cast<long long>(piece) * kPrefetchPiece,
+                        kPrefetchPiece);
+        }
+    }
     __syncthreads();
     for (int tt = tid; tt < P; tt += blockDim.x) {
         const int c0 = tt * k;
@@ -377,7 +403,6 @@ __global__ void __launch_bounds__(kCoresetThreads) coreset_kernel(CoresetArgs a)
         }
     }
     // ---------------- phase 2 (one CTA)
-    const bool local = gridDim.x == 1 && cached;  // the whole block's candidates are in shared memory
     if (gridDim.x > 1) {
         __threadfence();
         __syncthreads();
@@ -395,20 +420,22 @@ __global__ void __launch_bounds__(kCoresetThreads) coreset_kernel(CoresetArgs a)
     }
     const int T = a.T;
     const int TW = (T + 31) >> 5;
-    for (int i = tid; i < E * TW; i += blockDim.x) masks[i] = 0u;
-    if (tid < E) cnt[tid] = 0;
-    __syncthreads();
-    for (int c = tid; c < T * k; c += blockDim.x) {
-        const bool sv = local ? csurv[c] != 0 : __ldcg(&a.survive[c]) != 0;
-        if (sv) {
-            const int e = local ? cidx[c] : __ldcg(&a.idx[c]);
-            const int t = c / k;
-            atomicAdd(&cnt[e], 1);
-            atomicOr(&masks[e * TW + (t >> 5)], 1u << (t & 31));
+    if (!local) {  // count survivors per expert over every request
+        for (int i = tid; i < E * TW; i += blockDim.x) masks[i] = 0u;
+        if (tid < E) cnt[tid] = 0;
+        __syncthreads();
+        for (int c = tid; c < T * k; c += blockDim.x) {
+            if (__ldcg(&a.survive[c]) != 0) {
+                const int e = __ldcg(&a.idx[c]);
+                const int t = c / k;
+                atomicAdd(&cnt[e], 1);
+                atomicOr(&masks[e * TW + (t >> 5)], 1u << (t & 31));
+            }
         }
+        __syncthreads();
     }
-    __syncthreads();
-    const int my_cnt = tid < E ? cnt[tid] : 0;
+    // one request: every candidate of a kept expert survives, so phase 1's counts and masks hold
+    const int my_cnt = tid < E ? ((local && !keep[tid]) ? 0 : cnt[tid]) : 0;
     const int my_nch = (my_cnt + a.nch - 1) / a.nch;
     const int slot_end = block_inclusive_scan<int>(my_cnt, wtot32);
     const int chunk_end = block_inclusive_scan<int>(my_nch, wtot32);
