@@ -235,7 +235,7 @@ int run_route(const Ctx& c, int T, const void* x, const void* Wr, int32_t* idx, 
 }
 
 int run_coreset(const Ctx& c, int R, const float* top_p, const int32_t* idx, const float* mass, int32_t* n_sel,
-                int32_t* sel, uint8_t* survive, float* gate_rr, const void* prefetch_wgu = nullptr) {
+                int32_t* sel, uint8_t* survive, float* gate_rr) {
     const moestep_dims* d = c.d;
     CoresetArgs a{};
     a.R = R;
@@ -260,12 +260,6 @@ int run_coreset(const Ctx& c, int R, const float* top_p, const int32_t* idx, con
     a.nch = c.L.nch;
     a.has_shared = d->Is > 0;
     a.err = at<int>(c.ws, c.L.hdr);
-    if (prefetch_wgu != nullptr && d->dtype == MOESTEP_BF16) {
-        a.pf_base = static_cast<const char*>(prefetch_wgu);
-        a.pf_stride = 2ll * d->I * d->H * 2;
-        a.pf_experts = (a.pf_stride % (64 * 1024) == 0) ? kPrefetchExperts : 0;
-        if (a.pf_experts == 0) a.pf_base = nullptr;
-    }
     MOESTEP_LAUNCH(1, launch_coreset(a, c.s));
     return MOESTEP_OK;
 }
@@ -276,8 +270,10 @@ int run_experts(const Ctx& c, int R, const void* x, const moestep_layer* layer) 
     const moestep_dims* d = c.d;
     const Layout& L = c.L;
     const int* plan = at<int>(c.ws, L.hdr) + 32;
+    const bool pf = d->dtype == MOESTEP_BF16;
     MOESTEP_LAUNCH(2, launch_gather(d->dtype, x, d->H, at<int32_t>(c.ws, L.slot_tok), plan, L.max_slots,
-                                    at<void>(c.ws, L.xp), c.s));
+                                    at<void>(c.ws, L.xp), at<int4>(c.ws, L.chunks), pf ? layer->Wgu : nullptr,
+                                    2ll * d->I * d->H * 2, kPrefetchChunks, c.s));
     if (d->dtype == MOESTEP_F32) {
         MOESTEP_LAUNCH(3, launch_f32_gateup(d->H, d->E, d->I, d->Is, L.max_slots, at<float>(c.ws, L.xp),
                                             at<int32_t>(c.ws, L.slot_exp), plan, static_cast<const float*>(layer->Wgu),
@@ -575,7 +571,7 @@ int block_decode_step(const moestep_dims* dims, int R, int n_layers, const moest
         int32_t* sel = (trace && trace->sel) ? trace->sel + static_cast<size_t>(l) * R * dims->E : at<int32_t>(ws, L.sel);
         MOESTEP_TRY(run_route(c, T, x, layers[l].Wr, idx, at<float>(ws, L.mass), at<float>(ws, L.gate), nullptr));
         MOESTEP_TRY(run_coreset(c, R, top_p, idx, at<float>(ws, L.mass), nsel, sel,
-                                at<uint8_t>(ws, L.survive), at<float>(ws, L.gaterr), layers[l].Wgu));
+                                at<uint8_t>(ws, L.survive), at<float>(ws, L.gaterr)));
         MOESTEP_TRY(run_experts(c, R, x, &layers[l]));
         MOESTEP_LAUNCH(5, launch_combine(1, dims->dtype, T, dims->H, k, at<float>(ws, L.y),
                                          at<int32_t>(ws, L.slot_of), at<int32_t>(ws, L.slot_sh),

@@ -65,12 +65,7 @@ struct CoresetArgs {
     int nch;
     int has_shared;
     int* err;
-    // optional L2 prefetch of the top-ranked kept experts' gate/up weights
-    const char* pf_base;   // Wgu of the layer (NULL: no prefetch)
-    long long pf_stride;   // bytes per expert
-    int pf_experts;        // experts to prefetch per launch
 };
-constexpr int kPrefetchExperts = 16;  // 64 MiB of gate/up weights at the Clover layer shape
 
 cudaError_t launch_route(int dtype, const void* x, const void* Wr, int T, int H, int E, int k, float* logits,
                          int32_t* idx, float* mass, float* gate, int* counters, int* err, cudaStream_t s);
@@ -78,8 +73,12 @@ cudaError_t launch_topk_from_logits(const float* logits, int T, int E, int k, in
                                     float* gate, cudaStream_t s);
 cudaError_t launch_coreset(const CoresetArgs& a, cudaStream_t s);
 int coreset_smem_bytes(int E, int T);
+// xp[slot] = x[slot_tok[slot]]; optionally hints into L2 the gate/up weights (pf_wgu, pf_stride bytes per
+// expert) of the plan's first pf_chunks chunks
 cudaError_t launch_gather(int dtype, const void* x, int H, const int32_t* slot_tok, const int* plan,
-                          int max_slots, void* xp, cudaStream_t s);
+                          int max_slots, void* xp, const int4* chunks, const void* pf_wgu, long long pf_stride,
+                          int pf_chunks, cudaStream_t s);
+constexpr int kPrefetchChunks = 10;  // ~40 MiB of gate/up weights at the Clover layer shape
 
 // ------------------------------------------------------------------ combine / norm / embed
 // mode 0: out = routed + shared; mode 1: h += routed + shared, x = RMSNorm(h); mode 2: h = h_in, x = RMSNorm(h)

@@ -243,12 +243,6 @@ __device__ V block_inclusive_scan(V v, V* warp_tot) {
 }
 
 constexpr int kCandCache = 2048;  // candidates of one request kept in shared memory
-constexpr int kPrefetchPiece = 64 * 1024;
-
-__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
-                 : "memory");
-}
 
 // grid R, 1024 threads.  Phase 1 (every CTA): the coreset of request blockIdx.x.
 // Phase 2 (the last CTA to finish, or the only one): the grouped-by-expert
@@ -350,17 +344,6 @@ __global__ void __launch_bounds__(kCoresetThreads) coreset_kernel(CoresetArgs a)
     if (tid < E) keep[tid] = (keep[tid] >= 0 && keep[tid] < m);
     if (tid < m) a.sel[r * E + tid] = order[tid];
     if (tid == 0) a.n_sel[r] = m;
-    if (a.pf_base != nullptr) {
-        // pull the highest-ranked kept experts' gate/up weights into L2 while HBM is otherwise idle
-        const int ne = min(m, max(1, a.pf_experts / static_cast<int>(gridDim.x)));
-        const int pieces = static_cast<int>(a.pf_stride / kPrefetchPiece);
-        for (int i = tid; i < ne * pieces; i += blockDim.x) {
-            const int rank = i / pieces, piece = i - rank * pieces;
-            prefetch_l2(a.pf_base + static_cast<long long>(order[rank]) * a.pf_stride +
-                            static_cast<long long>(piece) * kPrefetchPiece,
-                        kPrefetchPiece);
-        }
-    }
     __syncthreads();
     for (int tt = tid; tt < P; tt += blockDim.x) {
         const int c0 = tt * k;
@@ -486,17 +469,36 @@ __global__ void __launch_bounds__(kCoresetThreads) coreset_kernel(CoresetArgs a)
     }
 }
 
-// one CTA per slot: xp[slot] = x[slot_tok[slot]]
+// One CTA per slot: xp[slot] = x[slot_tok[slot]].  Then, while HBM would
+// otherwise idle until the expert GEMM starts streaming, every thread hints a
+// few 128-byte lines of the gate/up weights of the first chunks in the plan
+// (the experts the GEMM processes first) into L2.  The hints are
+// fire-and-forget: nothing waits for them.
 __global__ void __launch_bounds__(256) gather_kernel(const uint4* __restrict__ x, int row_vec,
                                                      const int32_t* __restrict__ slot_tok, const int* __restrict__ plan,
-                                                     uint4* __restrict__ xp) {
+                                                     uint4* __restrict__ xp, const int4* __restrict__ chunks,
+                                                     const char* __restrict__ pf_base, long long pf_stride,
+                                                     int pf_chunks) {
     const int slot = blockIdx.x;
     pdl_trigger();
     pdl_wait();
-    if (slot >= plan[2]) return;
-    const int t = slot_tok[slot];
-    for (int i = threadIdx.x; i < row_vec; i += blockDim.x)
-        xp[static_cast<size_t>(slot) * row_vec + i] = x[static_cast<size_t>(t) * row_vec + i];
+    if (slot < plan[2]) {
+        const int t = slot_tok[slot];
+        for (int i = threadIdx.x; i < row_vec; i += blockDim.x)
+            xp[static_cast<size_t>(slot) * row_vec + i] = x[static_cast<size_t>(t) * row_vec + i];
+    }
+    if (pf_base != nullptr) {
+        const int nc = min(pf_chunks, plan[0]);
+        const long long lines_per = pf_stride >> 7;
+        const long long total = lines_per * nc;
+        const long long nthreads = static_cast<long long>(gridDim.x) * blockDim.x;
+        for (long long l = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; l < total; l += nthreads) {
+            const int c = static_cast<int>(l / lines_per);
+            const long long off = (l - c * lines_per) << 7;
+            const char* p = pf_base + static_cast<long long>(chunks[c].x) * pf_stride + off;
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+        }
+    }
 }
 
 }  // namespace
@@ -542,10 +544,12 @@ cudaError_t launch_coreset(const CoresetArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_gather(int dtype, const void* x, int H, const int32_t* slot_tok, const int* plan, int max_slots,
-                          void* xp, cudaStream_t s) {
+                          void* xp, const int4* chunks, const void* pf_wgu, long long pf_stride, int pf_chunks,
+                          cudaStream_t s) {
     const int row_vec = H * (dtype == MOESTEP_BF16 ? 2 : 4) / 16;
     return launch_pdl(gather_kernel, dim3(max_slots), dim3(256), 0, s, static_cast<const uint4*>(x), row_vec,
-                      slot_tok, plan, static_cast<uint4*>(xp));
+                      slot_tok, plan, static_cast<uint4*>(xp), chunks, static_cast<const char*>(pf_wgu), pf_stride,
+                      pf_chunks);
 }
 
 }  // namespace moestep
