@@ -257,7 +257,7 @@ def run_gpu(args, dist: Dist):
     clk = clocks.result()
 
     # ---------------- roofline pass: events around the expert and LM-head kernels on their stream
-    ms.prof_enable(None if args.prof_all else ["expert_gateup", "expert_down", "lm_head"])
+    ms.prof_enable(None if args.prof_all else ["expert_ffn", "lm_head"])
     for _ in range(args.steps):
         step()
     torch.cuda.synchronize()
@@ -311,25 +311,25 @@ def run_gpu(args, dist: Dist):
     step_bytes = eb["expert_weights"] + eb["router"] + eb["lm_head"]
     peaks = load_peaks()
     hbm_peak = peaks.get("hbm_gbs")
-    # dominant kernel: expert gate/up (2/3 of the weight bytes)
-    gu_n, gu_ms = prof["expert_gateup"]
-    dn_n, dn_ms = prof["expert_down"]
+    # dominant kernel: the fused expert FFN launch (gate/up + SwiGLU + down, all expert weight bytes)
+    ff_n, ff_ms = prof["expert_ffn"]
     steps_prof = args.steps
-    # per gate/up launch: the kept experts' and the shared expert's gate/up weights once, plus the
-    # gathered activations read and the SwiGLU output written (at most T*(k+1) token slots)
-    gu_weights = sum(u * 2 * cfg.I * cfg.H * 2 for u in unions) + cfg.n_layers * 2 * cfg.Is * cfg.H * 2
-    gu_act = cfg.n_layers * T * (cfg.k + 1) * (cfg.H + cfg.I) * 2
-    gu_bytes_launch = (gu_weights + gu_act) / cfg.n_layers
-    gu_avg_ms = gu_ms / max(1, gu_n)
-    achieved = gu_bytes_launch / (gu_avg_ms / 1e3) / 1e9
-    roofline = {"kernel": "tc_gemm_kernel<gate/up> (expert gate/up projections + SwiGLU)",
+    # per launch: every kept expert's and the shared expert's weights once, plus the gathered
+    # activations read, the SwiGLU rows written and read back, and the per-slot outputs written
+    # (at most T*(k+1) token slots)
+    slots = T * (cfg.k + 1)
+    ff_act = slots * (cfg.H * 2 + 2 * max(cfg.I, cfg.Is) * 2 + cfg.H * 4)
+    ff_bytes_launch = eb["expert_weights"] / cfg.n_layers + ff_act
+    ff_avg_ms = ff_ms / max(1, ff_n)
+    achieved = ff_bytes_launch / (ff_avg_ms / 1e3) / 1e9
+    roofline = {"kernel": "tc_gemm_kernel<experts> (routed + shared expert gate/up, SwiGLU and down in one launch)",
                 "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                 "frac": round(achieved / hbm_peak, 4) if hbm_peak else None,
-                "traffic": load_traffic(statistics.mean(unions) + -(-T // nch_for(T))),
+                "traffic": load_traffic(statistics.mean(unions) + 1),
                 "peak_source": peaks.get("source"),
-                "bytes_per_launch": int(gu_bytes_launch), "avg_launch_ms": round(gu_avg_ms, 5),
-                "launches_timed": gu_n}
-    expert_stream_ms = (gu_ms + dn_ms) / steps_prof
+                "bytes_per_launch": int(ff_bytes_launch), "avg_launch_ms": round(ff_avg_ms, 5),
+                "launches_timed": ff_n}
+    expert_stream_ms = ff_ms / steps_prof
     step_gbs = step_bytes / (ms_step / 1e3) / 1e9
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": dist.world, "steps": args.steps,
@@ -381,20 +381,20 @@ def kernel_sources_sha() -> str:
     return h.hexdigest()[:16]
 
 
-def load_traffic(units_per_launch: float):
-    """DRAM bytes per gate/up launch: the ncu capture's bytes per unit (profiles/) scaled to the
-    units of one launch here; None if the kernel sources changed since that capture."""
+def load_traffic(experts_per_launch: float):
+    """DRAM bytes per expert-FFN launch: the ncu capture's bytes per expert (profiles/) scaled to
+    the experts of one launch here; None if the kernel sources changed since that capture."""
     p = os.path.join(ROOT, "profiles", "tc_gemm_clover_layer.md")
     if not os.path.exists(p):
         return None
     vals = {}
     for line in open(p):
-        if ":" in line and line.split(":")[0].strip() in ("gateup_traffic_bytes_per_unit", "gateup_sources_sha"):
+        if ":" in line and line.split(":")[0].strip() in ("experts_traffic_bytes_per_expert", "kernel_sources_sha"):
             k, v = line.split(":", 1)
             vals[k.strip()] = v.strip()
-    if vals.get("gateup_sources_sha") != kernel_sources_sha() or "gateup_traffic_bytes_per_unit" not in vals:
+    if vals.get("kernel_sources_sha") != kernel_sources_sha() or "experts_traffic_bytes_per_expert" not in vals:
         return None
-    return int(float(vals["gateup_traffic_bytes_per_unit"]) * units_per_launch)
+    return int(float(vals["experts_traffic_bytes_per_expert"]) * experts_per_launch)
 
 
 # ------------------------------------------------------------------------------------------ oracle (CPU)

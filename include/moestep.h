@@ -226,8 +226,9 @@ long long moestep_launch_count(void);
  * with events (0 turns timing off; enabling clears earlier records);
  * moestep_prof_read() synchronises and returns, per kernel id, the number of
  * timed launches and their summed duration in ms.  Kernel ids: 0 route,
- * 1 coreset, 2 gather, 3 expert gate/up, 4 expert down, 5 combine/norm,
- * 6 LM head, 7 commit, 8 other.  Not thread-safe. */
+ * 1 coreset, 2 gather, 3 expert FFN (bf16: gate/up + SwiGLU + down in one
+ * launch; fp32: gate/up), 4 fp32 expert down, 5 combine/norm, 6 LM head,
+ * 7 commit, 8 other.  Not thread-safe. */
 int moestep_prof_enable(int kernel_mask);
 int moestep_prof_read(int kernel_id, int* launches, double* total_ms);
 #define MOESTEP_PROF_KERNELS 9

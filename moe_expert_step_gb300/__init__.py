@@ -26,7 +26,7 @@ EUNSUPPORTED = -6
 ETIMEOUT = -7
 EDEVINPUT = -8
 
-PROF_KERNELS = ["route", "coreset", "gather", "expert_gateup", "expert_down", "combine", "lm_head", "commit", "other"]
+PROF_KERNELS = ["route", "coreset", "gather", "expert_ffn", "expert_down", "combine", "lm_head", "commit", "other"]
 
 EXPORTS = [
     "moestep_workspace_size", "moestep_workspace_init", "moe_block_route", "moe_route_from_logits", "coreset_select", "moe_block_ffn",

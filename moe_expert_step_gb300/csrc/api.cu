@@ -39,7 +39,7 @@ int nch_for(int T) { return T <= 32 ? 32 : T <= 64 ? 64 : T <= 128 ? 128 : 256; 
 struct Layout {
     int T, max_slots, max_chunks, act_ld, n_ptiles, nch, route_groups;
     size_t hdr, counters, counters_bytes, logits, idx, mass, gate, nsel, sel, survive, gaterr, slot_of, slot_sh,
-        slot_tok, slot_exp, chunks, xp, act, y, hres, x, pmax, parg, psum, lmlogits, total;
+        slot_tok, slot_exp, chunks, done, xp, act, y, hres, x, pmax, parg, psum, lmlogits, total;
 };
 
 Layout make_layout(const moestep_dims& d, int R) {
@@ -77,6 +77,7 @@ Layout make_layout(const moestep_dims& d, int R) {
     L.slot_tok = take(sizeof(int32_t) * L.max_slots);
     L.slot_exp = take(sizeof(int32_t) * L.max_slots);
     L.chunks = take(sizeof(int4) * L.max_chunks);
+    L.done = take(sizeof(int) * L.max_chunks);
     L.xp = take(esz * L.max_slots * d.H);
     L.act = take(esz * L.max_slots * L.act_ld);
     L.y = take(sizeof(float) * L.max_slots * d.H);
@@ -270,10 +271,11 @@ int run_experts(const Ctx& c, int R, const void* x, const moestep_layer* layer) 
     const moestep_dims* d = c.d;
     const Layout& L = c.L;
     const int* plan = at<int>(c.ws, L.hdr) + 32;
-    const bool pf = d->dtype == MOESTEP_BF16;
+    const bool tc = d->dtype == MOESTEP_BF16;
     MOESTEP_LAUNCH(2, launch_gather(d->dtype, x, d->H, at<int32_t>(c.ws, L.slot_tok), plan, L.max_slots,
-                                    at<void>(c.ws, L.xp), at<int4>(c.ws, L.chunks), pf ? layer->Wgu : nullptr,
-                                    2ll * d->I * d->H * 2, kPrefetchChunks, c.s));
+                                    at<void>(c.ws, L.xp), at<int4>(c.ws, L.chunks), tc ? layer->Wgu : nullptr,
+                                    2ll * d->I * d->H * 2, kPrefetchChunks, tc ? at<int>(c.ws, L.done) : nullptr,
+                                    L.max_chunks, c.s));
     if (d->dtype == MOESTEP_F32) {
         MOESTEP_LAUNCH(3, launch_f32_gateup(d->H, d->E, d->I, d->Is, L.max_slots, at<float>(c.ws, L.xp),
                                             at<int32_t>(c.ws, L.slot_exp), plan, static_cast<const float*>(layer->Wgu),
@@ -286,14 +288,14 @@ int run_experts(const Ctx& c, int R, const void* x, const moestep_layer* layer) 
     }
     if (get_encode() != MOESTEP_OK) return MOESTEP_ECUDA;
     const bool sh = d->Is > 0;
-    CUtensorMap mgu, msgu, mxp, md, msd, mact;
+    TensorMaps m;
     int rc;
-    if ((rc = make_map(&mgu, layer->Wgu, d->H, 2ull * d->E * d->I, 64))) return rc;
-    if ((rc = make_map(&msgu, sh ? layer->Wsgu : layer->Wgu, d->H, sh ? 2ull * d->Is : 128, 64))) return rc;
-    if ((rc = make_map(&mxp, at<void>(c.ws, L.xp), d->H, L.max_slots, 16))) return rc;
-    if ((rc = make_map(&md, layer->Wd, d->I, 1ull * d->E * d->H, 64))) return rc;
-    if ((rc = make_map(&msd, sh ? layer->Wsd : layer->Wd, sh ? d->Is : d->I, d->H, 64))) return rc;
-    if ((rc = make_map(&mact, at<void>(c.ws, L.act), L.act_ld, L.max_slots, 16))) return rc;
+    if ((rc = make_map(&m.a[0], layer->Wgu, d->H, 2ull * d->E * d->I, 64))) return rc;
+    if ((rc = make_map(&m.a[1], sh ? layer->Wsgu : layer->Wgu, d->H, sh ? 2ull * d->Is : 128, 64))) return rc;
+    if ((rc = make_map(&m.a[2], layer->Wd, d->I, 1ull * d->E * d->H, 64))) return rc;
+    if ((rc = make_map(&m.a[3], sh ? layer->Wsd : layer->Wd, sh ? d->Is : d->I, d->H, 64))) return rc;
+    if ((rc = make_map(&m.b[0], at<void>(c.ws, L.xp), d->H, L.max_slots, 16))) return rc;
+    if ((rc = make_map(&m.b[1], at<void>(c.ws, L.act), L.act_ld, L.max_slots, 16))) return rc;
     GemmParams g{};
     g.plan = plan;
     g.chunks = at<int4>(c.ws, L.chunks);
@@ -308,16 +310,16 @@ int run_experts(const Ctx& c, int R, const void* x, const moestep_layer* layer) 
     g.rows_per_expert = 2 * d->I;
     g.out = at<void>(c.ws, L.act);
     g.out_ld = L.act_ld;
-    MOESTEP_LAUNCH(3, launch_tc_gemm(kGateUp, L.nch, mgu, msgu, mxp, g, c.sms, c.s));
     // down: 128-row tiles of the hidden dimension
-    g.routed_tiles = d->H / 128;
-    g.shared_tiles = d->H / 128;
-    g.routed_kb = d->I / 64;
-    g.shared_kb = d->Is / 64;
-    g.rows_per_expert = d->H;
-    g.out = at<void>(c.ws, L.y);
-    g.out_ld = d->H;
-    MOESTEP_LAUNCH(4, launch_tc_gemm(kDown, L.nch, md, msd, mact, g, c.sms, c.s));
+    g.dn_routed_tiles = d->H / 128;
+    g.dn_shared_tiles = d->H / 128;
+    g.dn_routed_kb = d->I / 64;
+    g.dn_shared_kb = d->Is / 64;
+    g.dn_rows_per_expert = d->H;
+    g.out2 = at<void>(c.ws, L.y);
+    g.out2_ld = d->H;
+    g.done = at<int>(c.ws, L.done);
+    MOESTEP_LAUNCH(3, launch_tc_gemm(kExperts, L.nch, m, g, c.sms, c.s));
     return MOESTEP_OK;
 }
 
@@ -330,10 +332,12 @@ int run_lm_commit(const Ctx& c, int R, const void* hidden, const void* Wlm, floa
     int n_tiles;
     if (d->dtype == MOESTEP_BF16) {
         if (get_encode() != MOESTEP_OK) return MOESTEP_ECUDA;
-        CUtensorMap mw, mh;
+        TensorMaps m;
         int rc;
-        if ((rc = make_map(&mw, Wlm, d->H, d->V, 64))) return rc;
-        if ((rc = make_map(&mh, hidden, d->H, T, 16))) return rc;
+        if ((rc = make_map(&m.a[0], Wlm, d->H, d->V, 64))) return rc;
+        if ((rc = make_map(&m.b[0], hidden, d->H, T, 16))) return rc;
+        m.a[1] = m.a[2] = m.a[3] = m.a[0];
+        m.b[1] = m.b[0];
         GemmParams g{};
         g.routed_kb = d->H / 64;
         g.lm_chunks = (T + L.nch - 1) / L.nch;
@@ -348,7 +352,7 @@ int run_lm_commit(const Ctx& c, int R, const void* hidden, const void* Wlm, floa
         g.err = at<int>(c.ws, L.hdr);
         g.timeout_ns = g_timeout_ns;
         const int units = g.lm_chunks * g.lm_tiles;
-        MOESTEP_LAUNCH(6, launch_tc_gemm(kLmHead, L.nch, mw, mw, mh, g, units < c.sms ? units : c.sms, c.s));
+        MOESTEP_LAUNCH(6, launch_tc_gemm(kLmHead, L.nch, m, g, units < c.sms ? units : c.sms, c.s));
         n_tiles = g.lm_tiles * 4;
     } else {
         float* lg = logits ? logits : at<float>(c.ws, L.lmlogits);

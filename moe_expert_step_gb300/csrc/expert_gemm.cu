@@ -3,7 +3,14 @@
 // One persistent CTA per SM walks a list of work units.  A unit is one
 // 128-row tile of one weight matrix (an expert's gate/up pair, an expert's
 // down projection, or a block of LM-head vocabulary rows) applied to the
-// tokens that use it: the operands are swapped so the weight rows are the MMA's
+// tokens that use it.  The expert launch holds the whole routed + shared FFN:
+// every gate/up unit first, then every down unit; a down unit's producer
+// waits (bounded) on a per-chunk counter that the chunk's gate/up epilogues
+// raise after their SwiGLU rows are stored, so the gate/up tail overlaps the
+// first down units instead of idling before a second launch.  Each CTA issues
+// all of its gate/up units before any down unit, and its epilogue drains them
+// without waiting on the producer, so the counters always complete.  The
+// operands are swapped so the weight rows are the MMA's
 // M = 128 and the block tokens are its N (16..NCH), because a 32-token block
 // gives every expert only a handful of tokens.  Each weight element is read
 // from HBM exactly once per block ([AIT 五]: the block's speed-up comes from
@@ -45,12 +52,12 @@ __host__ __device__ constexpr int num_stages(int nch) {
 __host__ __device__ constexpr int smem_bytes(int nch) { return num_stages(nch) * stage_bytes(nch) + 512 + 1024; }
 
 struct Unit {
-    int kb, rowA0, rowA1, slot0, n, mt;
-    bool shared;
+    int kb, rowA0, rowA1, slot0, n, mt, c;
+    bool shared, dn;
 };
 
 template <int MODE, int NCH>
-__device__ __forceinline__ Unit decode_unit(int u, const GemmParams& p, int nrc) {
+__device__ __forceinline__ Unit decode_unit(int u, const GemmParams& p, int nrc, int nsc) {
     Unit w;
     if (MODE == kLmHead) {
         const int mt = u / p.lm_chunks;
@@ -60,20 +67,36 @@ __device__ __forceinline__ Unit decode_unit(int u, const GemmParams& p, int nrc)
         w.rowA1 = w.rowA0 + 64;
         w.kb = p.routed_kb;
         w.shared = false;
+        w.dn = false;
+        w.c = c;
         w.slot0 = c * NCH;
         w.n = min(NCH, p.n_pos - w.slot0);
         return w;
     }
-    const int routed_units = nrc * p.routed_tiles;
+    int rt = p.routed_tiles, st = p.shared_tiles, rkb = p.routed_kb, skb = p.shared_kb, rpe = p.rows_per_expert;
+    bool dn = MODE == kDown;
+    if (MODE == kExperts) {
+        const int n_gu = nrc * p.routed_tiles + nsc * p.shared_tiles;
+        if (u >= n_gu) {  // second half of the unit list: down projections
+            u -= n_gu;
+            dn = true;
+            rt = p.dn_routed_tiles;
+            st = p.dn_shared_tiles;
+            rkb = p.dn_routed_kb;
+            skb = p.dn_shared_kb;
+            rpe = p.dn_rows_per_expert;
+        }
+    }
+    const int routed_units = nrc * rt;
     int c, mt;
     if (u < routed_units) {
-        c = u / p.routed_tiles;
-        mt = u - c * p.routed_tiles;
+        c = u / rt;
+        mt = u - c * rt;
         w.shared = false;
     } else {
         const int v = u - routed_units;
-        const int cs = v / p.shared_tiles;
-        mt = v - cs * p.shared_tiles;
+        const int cs = v / st;
+        mt = v - cs * st;
         c = nrc + cs;
         w.shared = true;
     }
@@ -81,18 +104,35 @@ __device__ __forceinline__ Unit decode_unit(int u, const GemmParams& p, int nrc)
     w.slot0 = ch.y;
     w.n = ch.z;
     w.mt = mt;
-    if (!w.shared) {
-        const int base = ch.x * p.rows_per_expert + mt * p.tile_rows;
-        w.rowA0 = base;
-        w.rowA1 = base + 64;
-        w.kb = p.routed_kb;
-    } else {
-        const int base = mt * p.tile_rows;
-        w.rowA0 = base;
-        w.rowA1 = base + 64;
-        w.kb = p.shared_kb;
-    }
+    w.c = c;
+    w.dn = dn;
+    const int base = (w.shared ? 0 : ch.x * rpe) + mt * p.tile_rows;
+    w.rowA0 = base;
+    w.rowA1 = base + 64;
+    w.kb = w.shared ? skb : rkb;
     return w;
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* ptr) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+    return v;
+}
+
+// Wait (bounded, like the mbarrier waits) until *ctr >= need; then order this
+// thread's later TMA (async-proxy) reads after what the counter published.
+__device__ __forceinline__ bool wait_count(const int* ctr, int need, volatile int* abort, uint64_t limit_ns) {
+    if (ld_acquire_gpu(ctr) < need) {
+        const uint64_t t0 = tc::globaltimer_ns();
+        for (;;) {
+            if (*abort) return false;
+            if (tc::globaltimer_ns() - t0 >= limit_ns) return false;
+            __nanosleep(100);
+            if (ld_acquire_gpu(ctr) >= need) break;
+        }
+    }
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    return true;
 }
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
@@ -115,8 +155,7 @@ __device__ __forceinline__ void record_timeout(int* err, int role, int u, int kb
 
 template <int MODE, int NCH>
 __global__ void __launch_bounds__(kThreads, 1)
-    tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA0, const __grid_constant__ CUtensorMap mapA1,
-                   const __grid_constant__ CUtensorMap mapB, const GemmParams p) {
+    tc_gemm_kernel(const __grid_constant__ TensorMaps maps, const GemmParams p) {
     constexpr int STAGES = num_stages(NCH);
     constexpr int SB = stage_bytes(NCH);
     constexpr uint32_t TMEM_COLS = (2 * NCH < 32) ? 32u : static_cast<uint32_t>(2 * NCH);
@@ -149,9 +188,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 0;
         *zero_flag = 0;
         tc::fence_mbar_init();
-        tc::prefetch_tmap(&mapA0);
-        tc::prefetch_tmap(&mapA1);
-        tc::prefetch_tmap(&mapB);
+        tc::prefetch_tmap(&maps.a[0]);
+        tc::prefetch_tmap(&maps.b[0]);
+        if (MODE != kLmHead) {
+            tc::prefetch_tmap(&maps.a[1]);
+            if (MODE == kExperts) {
+                tc::prefetch_tmap(&maps.a[2]);
+                tc::prefetch_tmap(&maps.a[3]);
+                tc::prefetch_tmap(&maps.b[1]);
+            }
+        }
     }
     if (warp == 0) {
         tc::tmem_alloc(tmem_holder, TMEM_COLS);
@@ -164,12 +210,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // prologue done: let the next kernel start, then wait for the work plan / inputs
     pdl_trigger();
     pdl_wait();
-    int nrc = 0, n_units;
+    int nrc = 0, nsc = 0, n_units;
     if (MODE == kLmHead) {
         n_units = p.lm_chunks * p.lm_tiles;
     } else {
         nrc = p.plan[0];
-        n_units = nrc * p.routed_tiles + p.plan[1] * p.shared_tiles;
+        nsc = p.plan[1];
+        n_units = nrc * p.routed_tiles + nsc * p.shared_tiles;
+        if (MODE == kExperts) n_units += nrc * p.dn_routed_tiles + nsc * p.dn_shared_tiles;
     }
     volatile int* abortv = abort_flag;
     const uint64_t tmo = p.timeout_ns;
@@ -182,9 +230,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t phase = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-            const Unit w = decode_unit<MODE, NCH>(u, p, nrc);
+            const Unit w = decode_unit<MODE, NCH>(u, p, nrc, nsc);
             const int nb = (w.n + 15) >> 4;
-            const CUtensorMap* mA = w.shared ? &mapA1 : &mapA0;
+            const CUtensorMap* mA = &maps.a[(w.dn && MODE == kExperts ? 2 : 0) + (w.shared ? 1 : 0)];
+            const CUtensorMap* mB = &maps.b[w.dn && MODE == kExperts ? 1 : 0];
+            if (MODE == kExperts && w.dn) {
+                // the SwiGLU rows of this chunk come from gate/up units of other CTAs
+                int good = 1;
+                if (lane == 0)
+                    good = wait_count(&p.done[w.c], 4 * (w.shared ? p.shared_tiles : p.routed_tiles), abortv, tmo);
+                good = __shfl_sync(0xffffffffu, good, 0);
+                if (!good) {
+                    ok = false;
+                    if (lane == 0) record_timeout(p.err, 6, u, -1, -1, 0, n_units, w.n);
+                    break;
+                }
+            }
             for (int kb = 0; kb < w.kb; ++kb) {
                 int good = 1;
                 if (lane == 0) {
@@ -195,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc::tma_load_2d_hint(sa, mA, &full[stage], kb * 64, w.rowA0, pol);
                         tc::tma_load_2d_hint(sa + kABytes / 2, mA, &full[stage], kb * 64, w.rowA1, pol);
                         for (int b = 0; b < nb; ++b)
-                            tc::tma_load_2d(sa + kABytes + b * kBoxBBytes, &mapB, &full[stage], kb * 64,
+                            tc::tma_load_2d(sa + kABytes + b * kBoxBBytes, mB, &full[stage], kb * 64,
                                             w.slot0 + 16 * b);
                         issued |= 1u << stage;
                         issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -230,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         int it = 0;
         for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++it) {
-            const Unit w = decode_unit<MODE, NCH>(u, p, nrc);
+            const Unit w = decode_unit<MODE, NCH>(u, p, nrc, nsc);
             const int buf = it & 1;
             const uint32_t aph = (it >> 1) & 1;
             const int N = ((w.n + 15) >> 4) << 4;
@@ -290,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int sp = warp & 3;  // TMEM sub-partition this warp may access: lanes 32*sp .. 32*sp+31
         int it = 0;
         for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++it) {
-            const Unit w = decode_unit<MODE, NCH>(u, p, nrc);
+            const Unit w = decode_unit<MODE, NCH>(u, p, nrc, nsc);
             const int buf = it & 1;
             const uint32_t aph = (it >> 1) & 1;
             int good = tc::mbar_wait(&tfull[buf], aph, abortv, tmo);
@@ -310,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float v[32];
                 tc::tmem_ld32(tb + c0, v);
                 const int cnt = min(32, w.n - c0);
-                if (MODE == kGateUp) {
+                if (MODE == kGateUp || (MODE == kExperts && !w.dn)) {
                     // rows alternate gate / up of one intermediate index: partner lane holds the other half
                     bf16* act = static_cast<bf16*>(p.out);
                     const int i = w.mt * 64 + (L >> 1);
@@ -325,12 +386,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 __float2bfloat16_rn(silu_f(g) * up);
                         }
                     }
-                } else if (MODE == kDown) {
-                    float* y = static_cast<float*>(p.out);
+                } else if (MODE == kDown || MODE == kExperts) {
+                    float* y = static_cast<float*>(MODE == kExperts ? p.out2 : p.out);
+                    const int ld = MODE == kExperts ? p.out2_ld : p.out_ld;
                     const int h = w.mt * 128 + L;
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
-                        if (j < cnt) y[static_cast<size_t>(w.slot0 + c0 + j) * p.out_ld + h] = v[j];
+                        if (j < cnt) y[static_cast<size_t>(w.slot0 + c0 + j) * ld + h] = v[j];
                 } else {
                     // per (position, 32-row slice): max logit, its lowest row, sum of exp(l - max)
                     const int row = w.mt * 128 + L;
@@ -362,6 +424,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
+            if (MODE == kExperts && !w.dn) {
+                // publish this warp's SwiGLU rows to the down units of the chunk (any CTA)
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) atomicAdd(&p.done[w.c], 1);
+            }
             tc::fence_before_sync();
             tc::mbar_arrive(&tempty[buf]);
         }
@@ -376,23 +444,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int MODE, int NCH>
-cudaError_t launch_one(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b, const GemmParams& p,
-                       int grid, cudaStream_t s) {
+cudaError_t launch_one(const TensorMaps& maps, const GemmParams& p, int grid, cudaStream_t s) {
     constexpr int bytes = smem_bytes(NCH);
     static int done[64] = {};
     cudaError_t e = ensure_smem(tc_gemm_kernel<MODE, NCH>, bytes, done);
     if (e != cudaSuccess) return e;
-    return launch_pdl(tc_gemm_kernel<MODE, NCH>, dim3(grid), dim3(kThreads), bytes, s, a0, a1, b, p);
+    return launch_pdl(tc_gemm_kernel<MODE, NCH>, dim3(grid), dim3(kThreads), bytes, s, maps, p);
 }
 
 template <int MODE>
-cudaError_t launch_mode(int nch, const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b,
-                        const GemmParams& p, int grid, cudaStream_t s) {
+cudaError_t launch_mode(int nch, const TensorMaps& maps, const GemmParams& p, int grid, cudaStream_t s) {
     switch (nch) {
-        case 32: return launch_one<MODE, 32>(a0, a1, b, p, grid, s);
-        case 64: return launch_one<MODE, 64>(a0, a1, b, p, grid, s);
-        case 128: return launch_one<MODE, 128>(a0, a1, b, p, grid, s);
-        case 256: return launch_one<MODE, 256>(a0, a1, b, p, grid, s);
+        case 32: return launch_one<MODE, 32>(maps, p, grid, s);
+        case 64: return launch_one<MODE, 64>(maps, p, grid, s);
+        case 128: return launch_one<MODE, 128>(maps, p, grid, s);
+        case 256: return launch_one<MODE, 256>(maps, p, grid, s);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -401,12 +467,10 @@ cudaError_t launch_mode(int nch, const CUtensorMap& a0, const CUtensorMap& a1, c
 
 int tc_gemm_smem_bytes(int nch) { return smem_bytes(nch); }
 
-cudaError_t launch_tc_gemm(int mode, int nch, const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b,
-                           const GemmParams& p, int grid, cudaStream_t s) {
+cudaError_t launch_tc_gemm(int mode, int nch, const TensorMaps& maps, const GemmParams& p, int grid, cudaStream_t s) {
     switch (mode) {
-        case kGateUp: return launch_mode<kGateUp>(nch, a0, a1, b, p, grid, s);
-        case kDown: return launch_mode<kDown>(nch, a0, a1, b, p, grid, s);
-        case kLmHead: return launch_mode<kLmHead>(nch, a0, a1, b, p, grid, s);
+        case kExperts: return launch_mode<kExperts>(nch, maps, p, grid, s);
+        case kLmHead: return launch_mode<kLmHead>(nch, maps, p, grid, s);
         default: return cudaErrorInvalidValue;
     }
 }

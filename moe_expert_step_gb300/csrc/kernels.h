@@ -10,7 +10,16 @@
 namespace moestep {
 
 // ------------------------------------------------------------------ grouped tcgen05 GEMM
-enum GemmMode { kGateUp = 0, kDown = 1, kLmHead = 2 };
+enum GemmMode { kGateUp = 0, kDown = 1, kLmHead = 2, kExperts = 3 };
+
+// kExperts: one persistent launch runs every gate/up unit (a[0] routed / a[1]
+// shared weights, b[0] gathered activations), then every down unit (a[2] / a[3],
+// b[1] = SwiGLU output); a down unit of a chunk starts once all of that
+// chunk's gate/up units have signalled completion.  kLmHead uses a[0] and b[0].
+struct TensorMaps {
+    CUtensorMap a[4];
+    CUtensorMap b[2];
+};
 
 struct GemmParams {
     // expert modes: work plan written by the coreset kernel
@@ -35,13 +44,17 @@ struct GemmParams {
     // outputs of expert modes: act (bf16, gate/up) or y (fp32, down)
     void* out;
     int out_ld;
+    // kExperts: the down half (tiles / K blocks / rows per expert / output y) and the per-chunk
+    // completion counters of the gate/up half (zeroed by the gather kernel before the launch)
+    int dn_routed_tiles, dn_shared_tiles, dn_routed_kb, dn_shared_kb, dn_rows_per_expert;
+    void* out2;
+    int out2_ld;
+    int* done;
     int* err;
     unsigned long long timeout_ns;
 };
 
-// mapA0: routed weights (or LM head), mapA1: shared-expert weights, mapB: activations.
-cudaError_t launch_tc_gemm(int mode, int nch, const CUtensorMap& a0, const CUtensorMap& a1,
-                           const CUtensorMap& b, const GemmParams& p, int grid, cudaStream_t s);
+cudaError_t launch_tc_gemm(int mode, int nch, const TensorMaps& maps, const GemmParams& p, int grid, cudaStream_t s);
 int tc_gemm_smem_bytes(int nch);
 
 // ------------------------------------------------------------------ routing / coreset / plan
@@ -73,11 +86,11 @@ cudaError_t launch_topk_from_logits(const float* logits, int T, int E, int k, in
                                     float* gate, cudaStream_t s);
 cudaError_t launch_coreset(const CoresetArgs& a, cudaStream_t s);
 int coreset_smem_bytes(int E, int T);
-// xp[slot] = x[slot_tok[slot]]; optionally hints into L2 the gate/up weights (pf_wgu, pf_stride bytes per
+// xp[slot] = x[slot_tok[slot]]; zeroes done[0..n_done) (fused expert kernel counters); optionally hints into L2 the gate/up weights (pf_wgu, pf_stride bytes per
 // expert) of the plan's first pf_chunks chunks
 cudaError_t launch_gather(int dtype, const void* x, int H, const int32_t* slot_tok, const int* plan,
                           int max_slots, void* xp, const int4* chunks, const void* pf_wgu, long long pf_stride,
-                          int pf_chunks, cudaStream_t s);
+                          int pf_chunks, int* done, int n_done, cudaStream_t s);
 constexpr int kPrefetchChunks = 10;  // ~40 MiB of gate/up weights at the Clover layer shape
 
 // ------------------------------------------------------------------ combine / norm / embed

@@ -478,10 +478,12 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint4* __restrict__ x
                                                      const int32_t* __restrict__ slot_tok, const int* __restrict__ plan,
                                                      uint4* __restrict__ xp, const int4* __restrict__ chunks,
                                                      const char* __restrict__ pf_base, long long pf_stride,
-                                                     int pf_chunks) {
+                                                     int pf_chunks, int* __restrict__ done, int n_done) {
     const int slot = blockIdx.x;
     pdl_trigger();
     pdl_wait();
+    if (done != nullptr && blockIdx.x == 0)
+        for (int i = threadIdx.x; i < n_done; i += blockDim.x) done[i] = 0;
     if (slot < plan[2]) {
         const int t = slot_tok[slot];
         for (int i = threadIdx.x; i < row_vec; i += blockDim.x)
@@ -545,11 +547,11 @@ cudaError_t launch_coreset(const CoresetArgs& a, cudaStream_t s) {
 
 cudaError_t launch_gather(int dtype, const void* x, int H, const int32_t* slot_tok, const int* plan, int max_slots,
                           void* xp, const int4* chunks, const void* pf_wgu, long long pf_stride, int pf_chunks,
-                          cudaStream_t s) {
+                          int* done, int n_done, cudaStream_t s) {
     const int row_vec = H * (dtype == MOESTEP_BF16 ? 2 : 4) / 16;
     return launch_pdl(gather_kernel, dim3(max_slots), dim3(256), 0, s, static_cast<const uint4*>(x), row_vec,
                       slot_tok, plan, static_cast<uint4*>(xp), chunks, static_cast<const char*>(pf_wgu), pf_stride,
-                      pf_chunks);
+                      pf_chunks, done, n_done);
 }
 
 }  // namespace moestep
