@@ -61,8 +61,7 @@ Layout make_layout(const moestep_dims& d, int R) {
         o = align_up(o + (bytes ? bytes : 1), 256);
         return at;
     };
-    L.hdr = take(256);  // int[0]: error word, int[8..15]: where a wait timed out, int[32..34]: expert work plan,
-                        // int[40..41]: grid barrier of the expert launch
+    L.hdr = take(256);  // int[0]: error word, int[8..15]: where a wait timed out, int[32..34]: expert work plan
     L.counters_bytes = sizeof(int) * (L.route_groups + 1 + R);  // router groups, coreset, commit per request
     L.counters = take(L.counters_bytes);
     L.logits = take(sizeof(float) * T * d.E);
@@ -266,16 +265,18 @@ int run_coreset(const Ctx& c, int R, const float* top_p, const int32_t* idx, con
     return MOESTEP_OK;
 }
 
-// experts (fp32: gather + FFMA gate/up + down; bf16: one fused tcgen05 launch);
-// leaves y (per slot) in the workspace
+// gather + experts (fp32: FFMA; bf16: tcgen05 gate/up then down); leaves y
+// (per slot) in the workspace
 int run_experts(const Ctx& c, int R, const void* x, const moestep_layer* layer) {
     const moestep_dims* d = c.d;
     const Layout& L = c.L;
     const int* plan = at<int>(c.ws, L.hdr) + 32;
+    const bool tc = d->dtype == MOESTEP_BF16;
+    MOESTEP_LAUNCH(2, launch_gather(d->dtype, x, d->H, at<int32_t>(c.ws, L.slot_tok), plan, L.max_slots,
+                                    at<void>(c.ws, L.xp), at<int4>(c.ws, L.chunks), tc ? layer->Wgu : nullptr,
+                                    2ll * d->I * d->H * 2, kPrefetchChunks, tc ? at<int>(c.ws, L.done) : nullptr,
+                                    L.max_chunks, c.s));
     if (d->dtype == MOESTEP_F32) {
-        MOESTEP_LAUNCH(2, launch_gather(d->dtype, x, d->H, at<int32_t>(c.ws, L.slot_tok), plan, L.max_slots,
-                                        at<void>(c.ws, L.xp), at<int4>(c.ws, L.chunks), nullptr, 0, 0, nullptr, 0,
-                                        c.s));
         MOESTEP_LAUNCH(3, launch_f32_gateup(d->H, d->E, d->I, d->Is, L.max_slots, at<float>(c.ws, L.xp),
                                             at<int32_t>(c.ws, L.slot_exp), plan, static_cast<const float*>(layer->Wgu),
                                             static_cast<const float*>(layer->Wsgu), at<float>(c.ws, L.act), L.act_ld,
@@ -285,7 +286,6 @@ int run_experts(const Ctx& c, int R, const void* x, const moestep_layer* layer) 
                                           static_cast<const float*>(layer->Wsd), at<float>(c.ws, L.y), c.s));
         return MOESTEP_OK;
     }
-    // bf16: one persistent tensor-core launch gathers, runs gate/up + SwiGLU, then down
     if (get_encode() != MOESTEP_OK) return MOESTEP_ECUDA;
     const bool sh = d->Is > 0;
     TensorMaps m;
@@ -319,15 +319,6 @@ int run_experts(const Ctx& c, int R, const void* x, const moestep_layer* layer) 
     g.out2 = at<void>(c.ws, L.y);
     g.out2_ld = d->H;
     g.done = at<int>(c.ws, L.done);
-    g.gx = static_cast<const uint4*>(x);
-    g.gxp = at<uint4>(c.ws, L.xp);
-    g.slot_tok = at<int32_t>(c.ws, L.slot_tok);
-    g.row_vec = d->H * 2 / 16;
-    g.max_chunks = L.max_chunks;
-    g.bar = at<int>(c.ws, L.hdr) + 40;
-    g.pf_base = static_cast<const char*>(layer->Wgu);
-    g.pf_stride = 2ll * d->I * d->H * 2;
-    g.pf_chunks = kPrefetchChunks;
     MOESTEP_LAUNCH(3, launch_tc_gemm(kExperts, L.nch, m, g, c.sms, c.s));
     return MOESTEP_OK;
 }

@@ -113,10 +113,6 @@ __device__ __forceinline__ Unit decode_unit(int u, const GemmParams& p, int nrc,
     return w;
 }
 
-__device__ __forceinline__ void st_release_gpu(int* ptr, int v) {
-    asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
-}
-
 __device__ __forceinline__ int ld_acquire_gpu(const int* ptr) {
     int v;
     asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
@@ -155,30 +151,6 @@ __device__ __forceinline__ void record_timeout(int* err, int role, int u, int kb
         err[14] = n_units;
         err[15] = n;
     }
-}
-
-// All CTAs of the launch meet here (one thread per CTA; every CTA of the
-// persistent grid is resident or becomes resident once earlier kernels'
-// blocks retire, so the wait ends).  bar[0] counts arrivals, bar[1] is a
-// generation number: the last arrival resets the count and advances the
-// generation, so no reset is needed between launches.  Bounded like every
-// other wait; false if it gave up.
-__device__ __forceinline__ bool grid_barrier(int* bar, volatile int* abort, uint64_t limit_ns) {
-    const int gen = ld_acquire_gpu(bar + 1);
-    __threadfence();
-    if (atomicAdd(bar, 1) == static_cast<int>(gridDim.x) - 1) {
-        atomicExch(bar, 0);
-        __threadfence();
-        st_release_gpu(bar + 1, gen + 1);
-        return true;
-    }
-    const uint64_t t0 = tc::globaltimer_ns();
-    while (ld_acquire_gpu(bar + 1) == gen) {
-        if (*abort) return false;
-        if (tc::globaltimer_ns() - t0 >= limit_ns) return false;
-        __nanosleep(64);
-    }
-    return true;
 }
 
 template <int MODE, int NCH>
@@ -249,42 +221,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     volatile int* abortv = abort_flag;
     const uint64_t tmo = p.timeout_ns;
-    if (MODE == kExperts) {
-        // gather this CTA's share of the token rows, zero the chunk counters, hint the first
-        // planned experts into L2, then wait for every CTA's rows before any TMA reads them
-        const int n_slots = p.plan[2];
-        for (int sl = blockIdx.x; sl < n_slots; sl += gridDim.x) {
-            const int t = p.slot_tok[sl];
-            for (int i = threadIdx.x; i < p.row_vec; i += blockDim.x)
-                p.gxp[static_cast<size_t>(sl) * p.row_vec + i] = p.gx[static_cast<size_t>(t) * p.row_vec + i];
-        }
-        if (blockIdx.x == 0)
-            for (int i = threadIdx.x; i < p.max_chunks; i += blockDim.x) p.done[i] = 0;
-        if (p.pf_base != nullptr) {
-            const int nc = min(p.pf_chunks, nrc);
-            const long long lines_per = p.pf_stride >> 7;
-            const long long total = lines_per * nc;
-            const long long nthr = static_cast<long long>(gridDim.x) * blockDim.x;
-            for (long long l = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; l < total; l += nthr) {
-                const int c = static_cast<int>(l / lines_per);
-                const char* a = p.pf_base + static_cast<long long>(p.chunks[c].x) * p.pf_stride +
-                                ((l - c * lines_per) << 7);
-                asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
-            }
-        }
-        __threadfence();  // this thread's gathered rows and zeroed counters, before the CTA arrives
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            if (!grid_barrier(p.bar, abortv, tmo)) {
-                *abort_flag = 1;
-                record_error(p.err, kErrTimeoutProducer);
-                record_timeout(p.err, 7, -1, -1, -1, 0, n_units, 0);
-            }
-            asm volatile("fence.proxy.async.global;" ::: "memory");
-        }
-        __syncthreads();
-        if (*abortv) n_units = 0;  // nothing issued yet: skip straight to teardown
-    }
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer

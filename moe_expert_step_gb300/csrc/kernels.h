@@ -50,18 +50,6 @@ struct GemmParams {
     void* out2;
     int out2_ld;
     int* done;
-    // kExperts: the launch also gathers its B operand, xp[slot] = x[slot_tok[slot]], before a grid
-    // barrier (count and generation words in the workspace header), and hints the first planned
-    // experts' gate/up weights into L2
-    const uint4* gx;        // layer input rows
-    uint4* gxp;             // gathered rows
-    const int32_t* slot_tok;
-    int row_vec;            // 16-byte vectors per row
-    int max_chunks;         // counters to zero
-    int* bar;               // [0] arrivals, [1] generation
-    const char* pf_base;    // gate/up weights of the layer (NULL: no hints)
-    long long pf_stride;    // bytes per expert
-    int pf_chunks;
     int* err;
     unsigned long long timeout_ns;
 };
