@@ -298,7 +298,7 @@ def run_gpu(args, dist: Dist):
         dist.barrier()
         h2d = h_pin.numel() * 4 + m_pin.numel() + t_pin.numel() * 4 + tp_pin.numel() * 4
         d2h = out_tok.numel() * 4 + out_msk.numel() + out_n.numel() * 4
-        e2e = {"value": dist.world * args.steps / t_e2e, "unit": UNIT, "h2d_bytes_per_step": h2d,
+        e2e = {"value": dist.world * args.steps * R / t_e2e, "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h,
                "how": "wall clock over K public-API calls (Python binding -> C ABI), each with pinned H2D inputs, "
                       "the step, D2H of tokens/masked/n_committed and a stream synchronize"}
@@ -306,7 +306,7 @@ def run_gpu(args, dist: Dist):
         raise RuntimeError("device error word set during the benchmark")
 
     ms_step = ms_total / args.steps
-    value = dist.world * args.steps / (ms_total / 1e3)
+    value = dist.world * args.steps * R / (ms_total / 1e3)   # one step advances R blocks
     eb = expert_bytes(cfg, unions)
     step_bytes = eb["expert_weights"] + eb["router"] + eb["lm_head"]
     peaks = load_peaks()
@@ -370,7 +370,7 @@ def load_peaks() -> dict:
 
 def nch_for(T: int) -> int:
     """Token chunk of the expert GEMM (the library's rule): experts with more tokens are split."""
-    return 32 if T <= 32 else 64 if T <= 64 else 128 if T <= 128 else 256
+    return 32 if T <= 32 else 64
 
 
 def kernel_sources_sha() -> str:
@@ -453,7 +453,7 @@ def cpu_baseline(cfg, R: int, reps: int = 3) -> dict:
     times = [s.run() for _ in range(reps)]
     tl = statistics.median(t[0] for t in times)
     th = statistics.median(t[1] for t in times)
-    return {"value": round(1.0 / s.step_seconds(tl, th), 5), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+    return {"value": round(R / s.step_seconds(tl, th), 5), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
             "sample": s.sample_desc() + f"; median of {reps} repetitions",
             "layer_s": round(tl, 3), "head_s": round(th, 3)}
 
@@ -466,7 +466,7 @@ def run_reference(args, dist: Dist):
         s.run()
     secs = [s.step_seconds(*s.run()) for _ in range(args.steps)]
     total = sum(secs)
-    value = args.steps / total
+    value = args.steps * R / total   # one step advances R blocks
     base = {"value": round(value, 5), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
             "sample": s.sample_desc() + "; every step one sample"}
     return {"impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": UNIT, "n_gpus": dist.world,

@@ -33,11 +33,17 @@ unsigned long long g_timeout_ns = 2000000000ull;  // bounded waits inside the tc
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int nch_for(int T) { return T <= 32 ? 32 : T <= 64 ? 64 : T <= 128 ? 128 : 256; }
+// Token chunk of a unit (the MMA's N is at most this).  The expert GEMM caps it
+// at 64 so the shared-memory ring keeps >= 8 stages (more weight bytes in
+// flight); an expert with more tokens is split into chunks whose weight tiles
+// are re-read from L2.  The LM head streams one tile per position chunk, so it
+// keeps wide chunks.
+int nch_for(int T) { return T <= 32 ? 32 : 64; }
+int lm_nch_for(int T) { return T <= 32 ? 32 : T <= 64 ? 64 : T <= 128 ? 128 : 256; }
 
 // ---------------------------------------------------------------------------- workspace
 struct Layout {
-    int T, max_slots, max_chunks, act_ld, n_ptiles, nch, route_groups;
+    int T, max_slots, max_chunks, act_ld, n_ptiles, nch, lm_nch, route_groups;
     size_t hdr, counters, counters_bytes, logits, idx, mass, gate, nsel, sel, survive, gaterr, slot_of, slot_sh,
         slot_tok, slot_exp, chunks, done, xp, act, y, hres, x, pmax, parg, psum, lmlogits, total;
 };
@@ -51,6 +57,7 @@ Layout make_layout(const moestep_dims& d, int R) {
     L.max_chunks = T * d.k + d.E + T + 1;
     L.act_ld = d.I > d.Is ? d.I : d.Is;
     L.nch = nch_for(T);
+    L.lm_nch = lm_nch_for(T);
     L.route_groups = (T + kRouteTokensPerCta - 1) / kRouteTokensPerCta;
     const int tiles_tc = (d.V + 127) / 128 * 4;
     const int tiles_logit = (d.V + kLogitTile - 1) / kLogitTile;
@@ -340,7 +347,7 @@ int run_lm_commit(const Ctx& c, int R, const void* hidden, const void* Wlm, floa
         m.b[1] = m.b[0];
         GemmParams g{};
         g.routed_kb = d->H / 64;
-        g.lm_chunks = (T + L.nch - 1) / L.nch;
+        g.lm_chunks = (T + L.lm_nch - 1) / L.lm_nch;
         g.lm_tiles = (d->V + 127) / 128;
         g.n_pos = T;
         g.V = d->V;
@@ -352,7 +359,7 @@ int run_lm_commit(const Ctx& c, int R, const void* hidden, const void* Wlm, floa
         g.err = at<int>(c.ws, L.hdr);
         g.timeout_ns = g_timeout_ns;
         const int units = g.lm_chunks * g.lm_tiles;
-        MOESTEP_LAUNCH(6, launch_tc_gemm(kLmHead, L.nch, m, g, units < c.sms ? units : c.sms, c.s));
+        MOESTEP_LAUNCH(6, launch_tc_gemm(kLmHead, L.lm_nch, m, g, units < c.sms ? units : c.sms, c.s));
         n_tiles = g.lm_tiles * 4;
     } else {
         float* lg = logits ? logits : at<float>(c.ws, L.lmlogits);

@@ -312,22 +312,8 @@ __global__ void __launch_bounds__(kCoresetThreads) coreset_kernel(CoresetArgs a)
             const long long mine = A[e];
             const int per = (E + parts - 1) / parts;
             const int lo = part * per, hi = min(E, lo + per);
-            // 8 independent probes per step so the shared-memory loads overlap
-            for (int e0 = lo; e0 < hi; e0 += 8) {
-                int cv[8];
-                long long av[8];
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const int e2 = e0 + q;
-                    cv[q] = e2 < hi ? cnt[e2] : 0;
-                    av[q] = e2 < hi ? A[e2] : 0;
-                }
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const int e2 = e0 + q;
-                    rk += (cv[q] > 0 && (av[q] > mine || (av[q] == mine && e2 < e))) ? 1 : 0;
-                }
-            }
+            for (int e2 = lo; e2 < hi; ++e2)
+                if (cnt[e2] > 0 && (A[e2] > mine || (A[e2] == mine && e2 < e))) ++rk;
         }
         for (int o = 1; o < parts; o <<= 1) rk += __shfl_xor_sync(0xffffffffu, rk, o);
         if (mine_valid && part == 0) order[rk] = e;
