@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--prof-all", action="store_true", help="time every kernel in the roofline pass")
     ap.add_argument("--no-graph", action="store_true", help="time direct launches instead of CUDA-graph replays")
+    ap.add_argument("--route-fusion", action="store_true",
+                    help="one request: one cluster launch between expert launches instead of four")
     return ap.parse_args()
 
 
@@ -187,6 +189,7 @@ def run_gpu(args, dist: Dist):
     accept = torch.zeros(T, dtype=torch.uint8, device="cuda")
     n_comm = torch.zeros(R, dtype=torch.int32, device="cuda")
     ws = ms.workspace(d, R)
+    ms.set_route_fusion(args.route_fusion)
     torch.cuda.synchronize()
     t_setup = time.time() - t_setup
 
@@ -335,7 +338,7 @@ def run_gpu(args, dist: Dist):
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": dist.world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": round(ms_step, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": workload_desc(cfg, R),
+        "config": {**workload_desc(cfg, R), "route_fusion": R == 1 and args.route_fusion},
         "expert_weight_hbm": {
             "bytes_per_step": step_bytes, "expert_bytes_per_step": eb["expert_weights"],
             "experts_kept_per_layer": {"mean": round(statistics.mean(unions), 2), "min": min(unions),

@@ -32,7 +32,7 @@ EXPORTS = [
     "moestep_workspace_size", "moestep_workspace_init", "moe_block_route", "moe_route_from_logits", "coreset_select", "moe_block_ffn",
     "lm_head_commit", "lm_commit_from_logits", "block_embed", "block_decode_step", "moestep_read_device_error",
     "moestep_error_string", "moestep_last_cuda_error", "moestep_prof_enable", "moestep_prof_read",
-    "moestep_set_wait_timeout_ns", "moestep_launch_count", "moe_block_route_noalloc",
+    "moestep_set_wait_timeout_ns", "moestep_set_route_fusion", "moestep_launch_count", "moe_block_route_noalloc",
 ]
 
 
@@ -90,6 +90,7 @@ def lib():
             "moestep_prof_enable": [i],
             "moestep_prof_read": [i, ctypes.POINTER(i), ctypes.POINTER(ctypes.c_double)],
             "moestep_set_wait_timeout_ns": [ctypes.c_ulonglong],
+            "moestep_set_route_fusion": [ctypes.c_int],
             "moestep_launch_count": [],
         }
         for name, args in sig.items():
@@ -228,6 +229,12 @@ def read_device_error(ws, stream=None) -> int:
     _check(lib().moestep_read_device_error(_p(ws), ws.numel(), _s(stream), ctypes.byref(w)),
            "moestep_read_device_error")
     return w.value
+
+
+def set_route_fusion(on: bool) -> None:
+    """One request in block_decode_step: one cluster launch between expert launches (True) or
+    the separate combine / router / coreset / gather launches (False, the default)."""
+    _check(lib().moestep_set_route_fusion(1 if on else 0), "moestep_set_route_fusion")
 
 
 def set_wait_timeout_ns(ns: int) -> None:

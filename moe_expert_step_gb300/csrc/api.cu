@@ -20,6 +20,7 @@ namespace {
 
 thread_local int g_last_cuda = 0;
 unsigned long long g_timeout_ns = 2000000000ull;  // bounded waits inside the tcgen05 kernels
+bool g_route_plan = false;  // one request: the single cluster launch between expert launches
 
 #define MOESTEP_CK(expr)                             \
     do {                                             \
@@ -242,8 +243,8 @@ int run_route(const Ctx& c, int T, const void* x, const void* Wr, int32_t* idx, 
     return MOESTEP_OK;
 }
 
-int run_coreset(const Ctx& c, int R, const float* top_p, const int32_t* idx, const float* mass, int32_t* n_sel,
-                int32_t* sel, uint8_t* survive, float* gate_rr) {
+CoresetArgs coreset_args(const Ctx& c, int R, const float* top_p, const int32_t* idx, const float* mass,
+                         int32_t* n_sel, int32_t* sel, uint8_t* survive, float* gate_rr) {
     const moestep_dims* d = c.d;
     CoresetArgs a{};
     a.R = R;
@@ -268,18 +269,57 @@ int run_coreset(const Ctx& c, int R, const float* top_p, const int32_t* idx, con
     a.nch = c.L.nch;
     a.has_shared = d->Is > 0;
     a.err = at<int>(c.ws, c.L.hdr);
+    return a;
+}
+
+int run_coreset(const Ctx& c, int R, const float* top_p, const int32_t* idx, const float* mass, int32_t* n_sel,
+                int32_t* sel, uint8_t* survive, float* gate_rr) {
+    const CoresetArgs a = coreset_args(c, R, top_p, idx, mass, n_sel, sel, survive, gate_rr);
     MOESTEP_LAUNCH(1, launch_coreset(a, c.s));
+    return MOESTEP_OK;
+}
+
+// one request: the previous layer's combine (or the input norm), router, top-k,
+// coreset, plan and gather in one cluster launch
+int run_route_plan(const Ctx& c, int mode, const float* h_in, const void* Wr, const void* Wr_next, const float* top_p,
+                   int32_t* idx, int32_t* n_sel, int32_t* sel) {
+    const moestep_dims* d = c.d;
+    const Layout& L = c.L;
+    RoutePlanArgs a{};
+    a.mode = mode;
+    a.y = at<float>(c.ws, L.y);
+    a.slot_of = at<int32_t>(c.ws, L.slot_of);
+    a.slot_sh = at<int32_t>(c.ws, L.slot_sh);
+    a.gate_rr_prev = at<float>(c.ws, L.gaterr);
+    a.has_shared = d->Is > 0;
+    a.h_in = h_in;
+    a.hres = at<float>(c.ws, L.hres);
+    a.x = at<__nv_bfloat16>(c.ws, L.x);
+    a.Wr = static_cast<const __nv_bfloat16*>(Wr);
+    a.wr_next = static_cast<const __nv_bfloat16*>(Wr_next);
+    a.T = L.T;
+    a.H = d->H;
+    a.E = d->E;
+    a.idx = idx;
+    a.mass = at<float>(c.ws, L.mass);
+    a.gate = at<float>(c.ws, L.gate);
+    a.cs = coreset_args(c, 1, top_p, idx, a.mass, n_sel, sel, at<uint8_t>(c.ws, L.survive), at<float>(c.ws, L.gaterr));
+    a.xp = at<uint4>(c.ws, L.xp);
+    a.row_vec = d->H / 8;
+    a.done = at<int>(c.ws, L.done);
+    a.n_done = L.max_chunks;
+    MOESTEP_LAUNCH(0, launch_route_plan(a, c.s));
     return MOESTEP_OK;
 }
 
 // gather + experts (fp32: FFMA; bf16: tcgen05 gate/up then down); leaves y
 // (per slot) in the workspace
-int run_experts(const Ctx& c, int R, const void* x, const moestep_layer* layer) {
+int run_experts(const Ctx& c, int R, const void* x, const moestep_layer* layer, bool gathered = false) {
     const moestep_dims* d = c.d;
     const Layout& L = c.L;
     const int* plan = at<int>(c.ws, L.hdr) + 32;
     const bool tc = d->dtype == MOESTEP_BF16;
-    MOESTEP_LAUNCH(2, launch_gather(d->dtype, x, d->H, at<int32_t>(c.ws, L.slot_tok), plan, L.max_slots,
+    if (!gathered) MOESTEP_LAUNCH(2, launch_gather(d->dtype, x, d->H, at<int32_t>(c.ws, L.slot_tok), plan, L.max_slots,
                                     at<void>(c.ws, L.xp), at<int4>(c.ws, L.chunks), tc ? layer->Wgu : nullptr,
                                     2ll * d->I * d->H * 2, kPrefetchChunks, tc ? at<int>(c.ws, L.done) : nullptr,
                                     L.max_chunks, c.s));
@@ -574,12 +614,28 @@ int block_decode_step(const moestep_dims* dims, int R, int n_layers, const moest
     void* x = at<void>(ws, L.x);
     MOESTEP_CK(cudaMemsetAsync(at<char>(ws, L.counters), 0, L.counters_bytes, c.s));
     float* hid_trace = trace ? trace->hidden : nullptr;
-    MOESTEP_LAUNCH(5, launch_combine(2, dims->dtype, T, dims->H, k, nullptr, nullptr, nullptr, nullptr, 0, h_in, hres,
-                                     x, n_layers == 0 ? hid_trace : nullptr, nullptr, c.s));
+    const bool one_block = g_route_plan && n_layers > 0 &&
+                           route_plan_eligible(R, dims->dtype, T, dims->H, dims->E, k);
+    if (!one_block)
+        MOESTEP_LAUNCH(5, launch_combine(2, dims->dtype, T, dims->H, k, nullptr, nullptr, nullptr, nullptr, 0, h_in,
+                                         hres, x, n_layers == 0 ? hid_trace : nullptr, nullptr, c.s));
     for (int l = 0; l < n_layers; ++l) {
         int32_t* idx = (trace && trace->idx) ? trace->idx + static_cast<size_t>(l) * T * k : at<int32_t>(ws, L.idx);
         int32_t* nsel = (trace && trace->n_sel) ? trace->n_sel + static_cast<size_t>(l) * R : at<int32_t>(ws, L.nsel);
         int32_t* sel = (trace && trace->sel) ? trace->sel + static_cast<size_t>(l) * R * dims->E : at<int32_t>(ws, L.sel);
+        const bool last = l == n_layers - 1;
+        if (one_block) {
+            // the combine of layer l-1 (or the input norm) runs inside the layer-l launch
+            MOESTEP_TRY(run_route_plan(c, l == 0 ? 2 : 1, h_in, layers[l].Wr, last ? nullptr : layers[l + 1].Wr, top_p,
+                                       idx, nsel, sel));
+            MOESTEP_TRY(run_experts(c, R, x, &layers[l], true));
+            if (last)
+                MOESTEP_LAUNCH(5, launch_combine(1, dims->dtype, T, dims->H, k, at<float>(ws, L.y),
+                                                 at<int32_t>(ws, L.slot_of), at<int32_t>(ws, L.slot_sh),
+                                                 at<float>(ws, L.gaterr), dims->Is > 0, nullptr, hres, x, hid_trace,
+                                                 nullptr, c.s));
+            continue;
+        }
         MOESTEP_TRY(run_route(c, T, x, layers[l].Wr, idx, at<float>(ws, L.mass), at<float>(ws, L.gate), nullptr));
         MOESTEP_TRY(run_coreset(c, R, top_p, idx, at<float>(ws, L.mass), nsel, sel,
                                 at<uint8_t>(ws, L.survive), at<float>(ws, L.gaterr)));
@@ -587,7 +643,7 @@ int block_decode_step(const moestep_dims* dims, int R, int n_layers, const moest
         MOESTEP_LAUNCH(5, launch_combine(1, dims->dtype, T, dims->H, k, at<float>(ws, L.y),
                                          at<int32_t>(ws, L.slot_of), at<int32_t>(ws, L.slot_sh),
                                          at<float>(ws, L.gaterr), dims->Is > 0, nullptr, hres, x,
-                                         l == n_layers - 1 ? hid_trace : nullptr, nullptr, c.s));
+                                         last ? hid_trace : nullptr, nullptr, c.s));
     }
     MOESTEP_TRY(run_lm_commit(c, R, x, Wlm, logit_scale, threshold, tokens, masked, choice, conf, accept, n_committed,
                               nullptr));
@@ -655,6 +711,11 @@ int moestep_prof_read(int kernel_id, int* launches, double* total_ms) {
 }
 
 // Test hook: limit of every bounded wait in the tensor-core kernels (ns).
+int moestep_set_route_fusion(int on) {
+    g_route_plan = on != 0;
+    return MOESTEP_OK;
+}
+
 int moestep_set_wait_timeout_ns(unsigned long long ns) {
     g_timeout_ns = ns;
     return MOESTEP_OK;

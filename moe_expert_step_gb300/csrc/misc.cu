@@ -1,6 +1,7 @@
 // Combine + residual + RMSNorm, block embedding, the fp32 FFMA path (router
 // aside) for fp32 weights, softmax partials of given logits, and the
 // LowConfidence commit.
+#include "combine.cuh"
 #include "common.cuh"
 #include "kernels.h"
 #include "launch.cuh"
@@ -8,46 +9,7 @@
 namespace moestep {
 namespace {
 
-constexpr float kRmsEps = 1e-6f;
-
-__device__ float block_sum_256(float v, float* red) {
-    v = warp_sum(v);
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    if (lane == 0) red[warp] = v;
-    __syncthreads();
-    float t = (threadIdx.x < 8) ? red[threadIdx.x] : 0.f;
-    if (warp == 0) t = warp_sum(t);
-    if (threadIdx.x == 0) red[8] = t;
-    __syncthreads();
-    return red[8];
-}
-
-template <typename T>
-__device__ __forceinline__ void store4(T* p, float4 v);
-template <>
-__device__ __forceinline__ void store4<float>(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
-template <>
-__device__ __forceinline__ void store4<bf16>(bf16* p, float4 v) {
-    __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y);
-    __nv_bfloat162 b = __floats2bfloat162_rn(v.z, v.w);
-    uint2 u;
-    u.x = *reinterpret_cast<uint32_t*>(&a);
-    u.y = *reinterpret_cast<uint32_t*>(&b);
-    *reinterpret_cast<uint2*>(p) = u;
-}
-template <typename T>
-__device__ __forceinline__ float4 roundtrip4(float4 v) {
-    return v;
-}
-template <>
-__device__ __forceinline__ float4 roundtrip4<bf16>(float4 v) {
-    return make_float4(__bfloat162float(__float2bfloat16_rn(v.x)), __bfloat162float(__float2bfloat16_rn(v.y)),
-                       __bfloat162float(__float2bfloat16_rn(v.z)), __bfloat162float(__float2bfloat16_rn(v.w)));
-}
-
-// One CTA per token.  MODE 0: out = sum_j gate_rr*y[slot_j] + y[shared slot].
-// MODE 1: h += that; x = RMSNorm(h).  MODE 2: h = h_in; x = RMSNorm(h).
-// The routed terms are added in candidate order j = 0..k-1, then the shared one.
+// One CTA (256 threads) per token: see combine_row.
 template <typename T, int MODE>
 __global__ void __launch_bounds__(256) combine_kernel(int H, int k, const float* __restrict__ y,
                                                       const int32_t* __restrict__ slot_of,
@@ -59,82 +21,10 @@ __global__ void __launch_bounds__(256) combine_kernel(int H, int k, const float*
     __shared__ int s_slot[33];
     __shared__ float s_g[33];
     __shared__ float red[9];
-    const int t = blockIdx.x;
     pdl_trigger();
     pdl_wait();
-    if (MODE != 2) {
-        if (threadIdx.x < k) {
-            s_slot[threadIdx.x] = slot_of[t * k + threadIdx.x];
-            s_g[threadIdx.x] = gate_rr[t * k + threadIdx.x];
-        }
-        if (threadIdx.x == 32) s_slot[32] = has_shared ? slot_sh[t] : -1;
-        __syncthreads();
-    }
-    float ss = 0.f;
-    const size_t row = static_cast<size_t>(t) * H;
-    constexpr int kKeep = 4;  // float4 columns per thread kept in registers (H <= 4096)
-    float4 hv[kKeep];
-    int i = 0;
-    for (int c = threadIdx.x * 4; c < H; c += 1024, ++i) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (MODE != 2) {
-            // slots in groups of 8 loaded together, added in candidate order
-            for (int j0 = 0; j0 < k; j0 += 8) {
-                float4 v[8];
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const int sl = (j0 + q < k) ? s_slot[j0 + q] : -1;
-                    v[q] = sl >= 0 ? __ldg(reinterpret_cast<const float4*>(y + static_cast<size_t>(sl) * H + c))
-                                   : make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    if (j0 + q < k && s_slot[j0 + q] >= 0) {
-                        const float g = s_g[j0 + q];
-                        acc.x += g * v[q].x;
-                        acc.y += g * v[q].y;
-                        acc.z += g * v[q].z;
-                        acc.w += g * v[q].w;
-                    }
-                }
-            }
-            if (s_slot[32] >= 0) {
-                const float4 v = *reinterpret_cast<const float4*>(y + static_cast<size_t>(s_slot[32]) * H + c);
-                acc.x += v.x;
-                acc.y += v.y;
-                acc.z += v.z;
-                acc.w += v.w;
-            }
-        }
-        if (MODE == 0) {
-            *reinterpret_cast<float4*>(out + row + c) = acc;
-        } else {
-            const float4 base = *reinterpret_cast<const float4*>((MODE == 1 ? h : h_in) + row + c);
-            const float4 v = make_float4(base.x + acc.x, base.y + acc.y, base.z + acc.z, base.w + acc.w);
-            *reinterpret_cast<float4*>(h + row + c) = v;
-            ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
-#pragma unroll
-            for (int q = 0; q < kKeep; ++q)
-                if (q == i) hv[q] = v;
-        }
-    }
-    if (MODE == 0) return;
-    const float tot = block_sum_256(ss, red);
-    const float inv = 1.0f / sqrtf(tot / static_cast<float>(H) + kRmsEps);
-    i = 0;
-    for (int c = threadIdx.x * 4; c < H; c += 1024, ++i) {
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (i < kKeep) {
-#pragma unroll
-            for (int q = 0; q < kKeep; ++q)
-                if (q == i) v = hv[q];
-        } else {
-            v = *reinterpret_cast<const float4*>(h + row + c);
-        }
-        const float4 n = make_float4(v.x * inv, v.y * inv, v.z * inv, v.w * inv);
-        store4<T>(x + row + c, n);
-        if (x_f32 != nullptr) *reinterpret_cast<float4*>(x_f32 + row + c) = roundtrip4<T>(n);
-    }
+    combine_row<T, MODE>(blockIdx.x, H, k, y, slot_of, slot_sh, gate_rr, has_shared, h_in, h, x, x_f32, out, s_slot,
+                         s_g, red);
 }
 
 template <typename T>
@@ -276,7 +166,7 @@ __global__ void __launch_bounds__(256) partials_kernel(const float* __restrict__
         }
     float s = 0.f;
     for (int v = v0 + threadIdx.x; v < v1; v += 256) s += __expf(row[v] - M);
-    s = block_sum_256(s, red);
+    s = group_sum_256(s, red);
     if (threadIdx.x == 0) {
         const size_t o = static_cast<size_t>(tile) * T + p;
         pmax[o] = M;

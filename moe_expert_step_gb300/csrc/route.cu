@@ -9,6 +9,9 @@
 // sum candidate masses per expert (exact 2^-54 fixed point), rank experts by
 // the sum, keep the shortest prefix that reaches top_p of the total, restrict
 // every token to its kept candidates and renormalise its gates.
+#include <cooperative_groups.h>
+
+#include "combine.cuh"
 #include "common.cuh"
 #include "kernels.h"
 #include "launch.cuh"
@@ -19,37 +22,92 @@ namespace {
 constexpr int kRouteTokens = kRouteTokensPerCta;
 constexpr int kRouteExperts = 8;  // experts per router CTA (one per warp)
 
-// Top-k of one token's logits by one warp.  `s` holds the E logits (shared memory).
-__device__ void topk_one_token(const float* s, int E, int k, int t, int32_t* idx, float* mass, float* gate) {
+// Order-preserving unsigned key of a float (a larger float has a larger key; -0
+// is taken as +0) and its inverse.
+__device__ __forceinline__ uint32_t fkey(float f) {
+    const uint32_t b = __float_as_uint(f + 0.0f);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float fkey_inv(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// Top-k of one token's logits by one warp.  `s` holds the E logits (shared
+// memory, E <= 1024); lane l keeps the keys of entries l, l+32, ... in
+// registers.  Each pick is an exact warp maximum of the keys (redux.sync) and,
+// among equal values, the lowest expert id.  mass_j = exp(z_j - max) / sum of
+// exp over all E (the sum per lane in entry order, then across lanes);
+// gate_j = mass_j / (mass_0 + ... + mass_{k-1}), summed in pick order.
+template <int kMaxPerLane>
+__device__ void topk_regs(const float* s, int E, int k, int t, int32_t* idx, float* mass, float* gate,
+                          int32_t* idx2, float* mass2) {
     const int lane = threadIdx.x & 31;
-    float m = -INFINITY;
-    for (int e = lane; e < E; e += 32) m = fmaxf(m, s[e]);
-    m = warp_max(m);
+    const int nv = (E - lane + 31) >> 5;  // entries of this lane
+    uint32_t key[kMaxPerLane];
+    uint32_t km = 0u;
+#pragma unroll
+    for (int q = 0; q < kMaxPerLane; ++q) {
+        key[q] = q < nv ? fkey(s[lane + 32 * q]) : 0u;
+        km = max(km, key[q]);
+    }
+    const float m = fkey_inv(__reduce_max_sync(0xffffffffu, km));
     float sum = 0.f;
-    for (int e = lane; e < E; e += 32) sum += expf(s[e] - m);
+#pragma unroll
+    for (int q = 0; q < kMaxPerLane; ++q)
+        if (q < nv) sum += expf(fkey_inv(key[q]) - m);
     sum = warp_sum(sum);
     uint32_t taken = 0;  // bit q: entry lane + 32q already chosen
-    float mine = 0.f, gsum = 0.f;
-    for (int j = 0; j < k; ++j) {
-        float bv = -INFINITY;
-        int bi = 0x7fffffff;
-        int q = 0;
-        for (int e = lane; e < E; e += 32, ++q)
-            if (!((taken >> q) & 1u) && (s[e] > bv || bi == 0x7fffffff)) {
-                bv = s[e];
-                bi = e;
+    uint32_t bk = 0u;    // best key of this lane among the entries not taken, and its slot
+    int bq = -1;
+    auto local_best = [&]() {
+        bk = 0u;
+        bq = -1;
+#pragma unroll
+        for (int q = 0; q < kMaxPerLane; ++q)
+            if (q < nv && !((taken >> q) & 1u) && (bq < 0 || key[q] > bk)) {
+                bk = key[q];
+                bq = q;
             }
-        warp_argmax(bv, bi);
-        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-        const float mj = expf(bv - m) / sum;
-        gsum += mj;
-        if (lane == j) mine = mj;
-        if (lane == 0) {
-            idx[t * k + j] = bi;
-            mass[t * k + j] = mj;
+    };
+    local_best();
+    uint32_t my_key = 0u;  // lane j: key and expert of pick j
+    int my_e = 0;
+    for (int j = 0; j < k; ++j) {
+        const uint32_t kb = __reduce_max_sync(0xffffffffu, bq >= 0 ? bk : 0u);
+        const int cand = (bq >= 0 && bk == kb) ? lane + 32 * bq : 0x7fffffff;
+        const int bi = __reduce_min_sync(0xffffffffu, cand);
+        if (lane == j) {
+            my_key = kb;
+            my_e = bi;
+        }
+        if ((bi & 31) == lane) {
+            taken |= 1u << (bi >> 5);
+            local_best();
         }
     }
-    if (lane < k) gate[t * k + lane] = mine / gsum;
+    const float mj = lane < k ? expf(fkey_inv(my_key) - m) / sum : 0.f;
+    float gsum = 0.f;
+    for (int j = 0; j < k; ++j) gsum += __shfl_sync(0xffffffffu, mj, j);
+    if (lane < k) {
+        idx[t * k + lane] = my_e;
+        mass[t * k + lane] = mj;
+        gate[t * k + lane] = mj / gsum;
+        if (idx2 != nullptr) {
+            idx2[t * k + lane] = my_e;
+            mass2[t * k + lane] = mj;
+        }
+    }
+}
+
+// idx2 / mass2 (may be NULL): a second copy of idx / mass
+__device__ void topk_one_token(const float* s, int E, int k, int t, int32_t* idx, float* mass, float* gate,
+                               int32_t* idx2 = nullptr, float* mass2 = nullptr) {
+    if (E <= 256)
+        topk_regs<8>(s, E, k, t, idx, mass, gate, idx2, mass2);
+    else if (E <= 512)
+        topk_regs<16>(s, E, k, t, idx, mass, gate, idx2, mass2);
+    else
+        topk_regs<32>(s, E, k, t, idx, mass, gate, idx2, mass2);
 }
 
 template <typename T>
@@ -244,39 +302,55 @@ __device__ V block_inclusive_scan(V v, V* warp_tot) {
 
 constexpr int kCandCache = 2048;  // candidates of one request kept in shared memory
 
-// grid R, 1024 threads.  Phase 1 (every CTA): the coreset of request blockIdx.x.
-// Phase 2 (the last CTA to finish, or the only one): the grouped-by-expert
-// work plan over the union of all requests' kept experts.
-__global__ void __launch_bounds__(kCoresetThreads) coreset_kernel(CoresetArgs a) {
-    __shared__ long long A[1024];
-    __shared__ long long cum[1024];
-    __shared__ int cnt[1024];
-    __shared__ int order[1024];
-    __shared__ int keep[1024];
-    __shared__ int cidx[kCandCache];
-    __shared__ float cmass[kCandCache];
-    __shared__ uint8_t csurv[kCandCache];
-    __shared__ long long wtot64[32];
-    __shared__ int wtot32[32];
-    __shared__ int s_last, s_nr, s_nrc;
-    extern __shared__ uint32_t masks[];  // phase 2: [E][ceil(T/32)]
+// The block coreset and work plan, executed by one 1024-thread CTA for request
+// r of nreq.  Phase 1: the coreset of request r.  Phase 2 (done by the last
+// request's CTA to finish, or directly when nreq == 1): the grouped-by-expert
+// work plan over the union of all requests' kept experts.  `masks` (E *
+// ceil(T/32) words) and `sc` are shared-memory scratch.  Used by the coreset kernel
+// (one CTA per request) and by the single-block router.
+struct CoresetScratch {  // shared memory of one coreset CTA
+    long long A[1024];
+    long long cum[1024];
+    int cnt[1024];
+    int order[1024];
+    int keep[1024];
+    int cidx[kCandCache];
+    float cmass[kCandCache];
+    uint32_t khi[1024 + 32];  // candidates' aggregates, compacted: high words (zero padded) ...
+    int ce[1024];             // ... and expert ids; the full aggregates go to cum
+    long long wtot64[32];
+    int s_last, s_nr, s_nrc, s_m;
+    uint8_t csurv[kCandCache];
+};
+
+__device__ void coreset_body(const CoresetArgs& a, int r, int nreq, uint32_t* masks, CoresetScratch& sc) {
+    long long* A = sc.A;
+    long long* cum = sc.cum;
+    int* cnt = sc.cnt;
+    int* order = sc.order;
+    int* keep = sc.keep;
+    int* cidx = sc.cidx;
+    float* cmass = sc.cmass;
+    uint8_t* csurv = sc.csurv;
+    long long* wtot64 = sc.wtot64;
+    int& s_last = sc.s_last;
+    int& s_nr = sc.s_nr;
+    int& s_nrc = sc.s_nrc;
 
     const int tid = threadIdx.x;
-    const int r = blockIdx.x;
     const int E = a.E, k = a.k, P = a.P;
     const int nc = P * k;                    // candidates of this request
     const bool cached = nc <= kCandCache;
     const int base = r * nc;                 // first candidate of this request in idx/mass
     // one request whose candidates all fit in shared memory: the plan reuses phase 1's counts
-    const bool local = gridDim.x == 1 && cached;
+    const bool local = nreq == 1 && cached;
     const int TWl = (P + 31) >> 5;
-    pdl_trigger();
-    pdl_wait();
     const float tp = a.top_p[r];
     // ---------------- phase 1
     if (tid < E) {
         A[tid] = 0;
         cnt[tid] = 0;
+        keep[tid] = -1;
     }
     if (local)
         for (int i = tid; i < E * TWl; i += blockDim.x) masks[i] = 0u;
@@ -301,104 +375,176 @@ __global__ void __launch_bounds__(kCoresetThreads) coreset_kernel(CoresetArgs a)
         }
     }
     __syncthreads();
-    // rank of every candidate expert, (aggregate desc, id asc): `parts` threads share one expert
-    int parts = 1;
-    while (parts < 32 && parts * 2 * E <= kCoresetThreads) parts *= 2;
-    {
-        const int e = tid / parts, part = tid % parts;
-        int rk = 0;
-        const bool mine_valid = e < E && cnt[e] > 0;
-        if (mine_valid) {
-            const long long mine = A[e];
-            const int per = (E + parts - 1) / parts;
-            const int lo = part * per, hi = min(E, lo + per);
-            for (int e2 = lo; e2 < hi; ++e2)
-                if (cnt[e2] > 0 && (A[e2] > mine || (A[e2] == mine && e2 < e))) ++rk;
-        }
-        for (int o = 1; o < parts; o <<= 1) rk += __shfl_xor_sync(0xffffffffu, rk, o);
-        if (mine_valid && part == 0) order[rk] = e;
-        if (part == 0 && e < E) keep[e] = mine_valid ? rk : -1;  // rank for now, flag below
+    // compact the candidate experts in id order: cum[p] = aggregate, khi[p] = its high
+    // word, ce[p] = expert id
+    const int flag = (tid < E && cnt[tid] > 0) ? 1 : 0;
+    const int incl = block_inclusive_scan<int>(flag, reinterpret_cast<int*>(wtot64));
+    const int nC = reinterpret_cast<int*>(wtot64)[31];
+    if (flag) {
+        cum[incl - 1] = A[tid];
+        sc.khi[incl - 1] = static_cast<uint32_t>(static_cast<unsigned long long>(A[tid]) >> 32);
+        sc.ce[incl - 1] = tid;
     }
-    int nC = 0;
-    {
-        const int e = tid;
-        nC = __syncthreads_count(e < E && cnt[e] > 0);
-    }
-    long long v = (tid < nC) ? A[order[tid]] : 0;
-    v = block_inclusive_scan<long long>(v, wtot64);
-    if (tid < nC) cum[tid] = v;
+    if (tid < 32) sc.khi[nC + tid] = 0u;  // padding of the last 4-key block
     __syncthreads();
-    const long long total = nC > 0 ? cum[nC - 1] : 0;
-    int m;
-    if (!(tp > 0.0f)) {  // NaN or non-positive fraction: keep everything and flag the input
-        if (tid == 0) record_error(a.err, kErrBadInput);
-        m = nC;
-    } else if (tp >= 1.0f || total == 0) {
-        m = nC;
-    } else {
-        long long target = static_cast<long long>(ceil(__dmul_rn(static_cast<double>(tp), __ll2double_rn(total))));
-        target = target < 1 ? 1 : (target > total ? total : target);
-        m = 1 + __syncthreads_count(tid < nC && cum[tid] < target);
-        m = m > nC ? nC : m;
+    // rank of every candidate, (aggregate desc, id asc): `parts` threads share one
+    // candidate and take every parts-th block of 4 rivals.  The high words settle
+    // every rival whose high word differs; a tie on the high word (rare) is settled
+    // on the full aggregate and the id.  All sums are >= 0.
+    {
+        int parts = 1;
+        while (parts < 32 && parts * 2 * nC <= kCoresetThreads) parts *= 2;
+        const int p = tid / parts, part = tid % parts;
+        const bool mine_ok = p < nC;
+        const uint32_t mh = mine_ok ? sc.khi[p] : 0u;
+        int gt = 0, eq = 0;
+        if (mine_ok) {
+            const int nblk = (nC + 3) >> 2;
+            for (int b = part; b < nblk; b += parts) {
+                const uint4 h = *reinterpret_cast<const uint4*>(&sc.khi[4 * b]);
+                gt += (h.x > mh) + (h.y > mh) + (h.z > mh) + (h.w > mh);
+                eq += (h.x == mh) + (h.y == mh) + (h.z == mh) + (h.w == mh);
+            }
+        }
+        const int lane = tid & 31;
+        const unsigned gmask = parts == 32 ? 0xffffffffu : (((1u << parts) - 1u) << (lane & ~(parts - 1)));
+        for (int o = 1; o < parts; o <<= 1) {
+            gt += __shfl_xor_sync(gmask, gt, o);
+            eq += __shfl_xor_sync(gmask, eq, o);
+        }
+        if (mine_ok && eq > 1) {  // uniform within the group of `parts` lanes
+            const long long mine = cum[p];
+            int add = 0;
+            for (int p2 = part; p2 < nC; p2 += parts)
+                if (p2 != p && sc.khi[p2] == mh) {
+                    const long long o = cum[p2];
+                    add += (o > mine || (o == mine && p2 < p)) ? 1 : 0;
+                }
+            for (int o = 1; o < parts; o <<= 1) add += __shfl_xor_sync(gmask, add, o);
+            gt += add;
+        }
+        if (mine_ok && part == 0) {
+            order[gt] = sc.ce[p];
+            keep[sc.ce[p]] = gt;  // rank for now, flag below
+        }
     }
+    __syncthreads();
+    // the cut, by one warp: m = smallest prefix of the ranked candidates whose
+    // aggregate reaches ceil(top_p * total) (exact integer sums, any order)
+    if (tid < 32) {
+        const int per = (nC + 31) >> 5;
+        const int lo = min(nC, tid * per), hi = min(nC, lo + per);
+        long long own = 0;
+        for (int i = lo; i < hi; ++i) own += A[order[i]];
+        long long incl64 = own;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const long long n = __shfl_up_sync(0xffffffffu, incl64, o);
+            if (tid >= o) incl64 += n;
+        }
+        const long long total = __shfl_sync(0xffffffffu, incl64, 31);
+        int m;
+        if (!(tp > 0.0f)) {  // NaN or non-positive fraction: keep everything and flag the input
+            if (tid == 0) record_error(a.err, kErrBadInput);
+            m = nC;
+        } else if (tp >= 1.0f || total == 0) {
+            m = nC;
+        } else {
+            long long target =
+                static_cast<long long>(ceil(__dmul_rn(static_cast<double>(tp), __ll2double_rn(total))));
+            target = target < 1 ? 1 : (target > total ? total : target);
+            long long run = incl64 - own;
+            int below = 0;  // ranked prefixes whose sum is still short of the target
+            for (int i = lo; i < hi; ++i) {
+                run += A[order[i]];
+                below += run < target ? 1 : 0;
+            }
+            m = 1 + __reduce_add_sync(0xffffffffu, below);
+            m = m > nC ? nC : m;
+        }
+        if (tid == 0) {
+            sc.s_m = m;
+            a.n_sel[r] = m;
+        }
+    }
+    __syncthreads();
+    const int m = sc.s_m;
     if (tid < E) keep[tid] = (keep[tid] >= 0 && keep[tid] < m);
     if (tid < m) a.sel[r * E + tid] = order[tid];
-    if (tid == 0) a.n_sel[r] = m;
     __syncthreads();
-    for (int tt = tid; tt < P; tt += blockDim.x) {
-        const int c0 = tt * k;
-        // candidates in groups of 8; the renormaliser is summed in candidate order
+    if (cached && nc <= static_cast<int>(blockDim.x) && (32 % k) == 0) {
+        // one thread per candidate; a token's k candidates are k adjacent lanes, and
+        // each lane sums the kept masses of its token in candidate order
+        const int c = tid;
+        const bool valid = c < nc;
+        const int e = valid ? cidx[c] : -1;
+        const float ms = valid ? cmass[c] : 0.f;
+        const bool sv = e >= 0 && e < E && keep[e];
+        const float mv = sv ? ms : 0.f;
+        const int g0 = (threadIdx.x & 31) / k * k;
         float denom = 0.f;
-        for (int j0 = 0; j0 < k; j0 += 8) {
-            int ev[8];
-            float mv[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const int c = c0 + j0 + q;
-                const bool in = j0 + q < k;
-                ev[q] = in ? (cached ? cidx[c] : a.idx[base + c]) : -1;
-                mv[q] = in ? (cached ? cmass[c] : a.mass[base + c]) : 0.f;
-            }
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-                if (ev[q] >= 0 && ev[q] < E && keep[ev[q]]) denom += mv[q];
+        for (int j = 0; j < k; ++j) denom += __shfl_sync(0xffffffffu, mv, g0 + j);
+        if (valid) {
+            a.survive[base + c] = sv ? 1 : 0;
+            a.gate_rr[base + c] = (sv && denom > 0.f) ? ms / denom : 0.f;
+            csurv[c] = sv ? 1 : 0;
         }
-        for (int j0 = 0; j0 < k; j0 += 8) {
-            int ev[8];
-            float mv[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const int c = c0 + j0 + q;
-                const bool in = j0 + q < k;
-                ev[q] = in ? (cached ? cidx[c] : a.idx[base + c]) : -1;
-                mv[q] = in ? (cached ? cmass[c] : a.mass[base + c]) : 0.f;
+    } else {
+        for (int tt = tid; tt < P; tt += blockDim.x) {
+            const int c0 = tt * k;
+            // candidates in groups of 8; the renormaliser is summed in candidate order
+            float denom = 0.f;
+            for (int j0 = 0; j0 < k; j0 += 8) {
+                int ev[8];
+                float mv[8];
+    #pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const int c = c0 + j0 + q;
+                    const bool in = j0 + q < k;
+                    ev[q] = in ? (cached ? cidx[c] : a.idx[base + c]) : -1;
+                    mv[q] = in ? (cached ? cmass[c] : a.mass[base + c]) : 0.f;
+                }
+    #pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    if (ev[q] >= 0 && ev[q] < E && keep[ev[q]]) denom += mv[q];
             }
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const int c = c0 + j0 + q;
-                if (j0 + q < k) {
-                    const bool sv = ev[q] >= 0 && ev[q] < E && keep[ev[q]];
-                    a.survive[base + c] = sv ? 1 : 0;
-                    a.gate_rr[base + c] = (sv && denom > 0.f) ? mv[q] / denom : 0.f;
-                    if (cached) csurv[c] = sv ? 1 : 0;
+            for (int j0 = 0; j0 < k; j0 += 8) {
+                int ev[8];
+                float mv[8];
+    #pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const int c = c0 + j0 + q;
+                    const bool in = j0 + q < k;
+                    ev[q] = in ? (cached ? cidx[c] : a.idx[base + c]) : -1;
+                    mv[q] = in ? (cached ? cmass[c] : a.mass[base + c]) : 0.f;
+                }
+    #pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const int c = c0 + j0 + q;
+                    if (j0 + q < k) {
+                        const bool sv = ev[q] >= 0 && ev[q] < E && keep[ev[q]];
+                        a.survive[base + c] = sv ? 1 : 0;
+                        a.gate_rr[base + c] = (sv && denom > 0.f) ? mv[q] / denom : 0.f;
+                        if (cached) csurv[c] = sv ? 1 : 0;
+                    }
                 }
             }
         }
     }
     // ---------------- phase 2 (one CTA)
-    if (gridDim.x > 1) {
+    if (nreq > 1) {
         __threadfence();
         __syncthreads();
         if (tid == 0) {
             const int prev = atomicAdd(a.counter, 1);
-            s_last = (prev == static_cast<int>(gridDim.x) - 1);
+            s_last = (prev == nreq - 1);
             if (s_last) *a.counter = 0;
         }
         __syncthreads();
         if (!s_last) return;
         __threadfence();
     } else {
-        __threadfence();
+        if (!local) __threadfence();
         __syncthreads();
     }
     const int T = a.T;
@@ -420,8 +566,11 @@ __global__ void __launch_bounds__(kCoresetThreads) coreset_kernel(CoresetArgs a)
     // one request: every candidate of a kept expert survives, so phase 1's counts and masks hold
     const int my_cnt = tid < E ? ((local && !keep[tid]) ? 0 : cnt[tid]) : 0;
     const int my_nch = (my_cnt + a.nch - 1) / a.nch;
-    const int slot_end = block_inclusive_scan<int>(my_cnt, wtot32);
-    const int chunk_end = block_inclusive_scan<int>(my_nch, wtot32);
+    // one scan of (chunks << 32 | slots)
+    const long long both = block_inclusive_scan<long long>(
+        (static_cast<long long>(my_nch) << 32) | static_cast<long long>(my_cnt), wtot64);
+    const int slot_end = static_cast<int>(both & 0xffffffffll);
+    const int chunk_end = static_cast<int>(both >> 32);
     const int slot_base = slot_end - my_cnt;
     const int chunk_base = chunk_end - my_nch;
     if (tid < E) {
@@ -466,6 +615,241 @@ __global__ void __launch_bounds__(kCoresetThreads) coreset_kernel(CoresetArgs a)
         a.plan[0] = nrc;
         a.plan[1] = nsc;
         a.plan[2] = NR + (a.has_shared ? T : 0);
+    }
+}
+
+// grid R, 1024 threads: one CTA per request (see coreset_body).
+__global__ void __launch_bounds__(kCoresetThreads) coreset_kernel(CoresetArgs a) {
+    extern __shared__ __align__(16) uint8_t coreset_smem[];  // scratch, then masks [E][ceil(T/32)]
+    pdl_trigger();
+    pdl_wait();
+    coreset_body(a, blockIdx.x, gridDim.x, reinterpret_cast<uint32_t*>(coreset_smem + sizeof(CoresetScratch)),
+                 *reinterpret_cast<CoresetScratch*>(coreset_smem));
+}
+
+// ---------------------------------------------------------------------------- single-block layer head
+// One request (T <= 32 tokens), everything between two expert launches in ONE
+// launch of a cluster of kPlanCluster CTAs with no global atomics:
+//  1. combine: the previous layer's expert outputs into the residual stream and
+//     RMSNorm -> x (or, first layer, the norm of the input), the same
+//     arithmetic as the combine kernel; CTA c takes tokens c, c+8, ...;
+//  2. every CTA stages the block's x rows in shared memory;
+//  3. router logits of the CTA's experts [c*E/8, (c+1)*E/8) for every token on
+//     tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate; a warp takes a
+//     16-expert tile over 1/kq of H, the kq partial sums added in a fixed order)
+//     and each logit stored in the shared memory of the CTA that takes the
+//     token's top-k (distributed shared memory);
+//  4. top-k per token (one warp each), copies to CTA 0;
+//  5. coreset and work plan in CTA 0 (the coreset kernel's code);
+//  6. every CTA copies its share of token rows into the gathered activations.
+// L2 hints bring this CTA's router rows in before the previous kernel ends and
+// the next layer's router rows in for the next launch.
+namespace cg = cooperative_groups;
+constexpr int kPlanCluster = 8;
+constexpr int kPlanThreads = 1024;
+
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// word i (0..7) of a pair of 16-byte vectors holding 16 bf16
+__device__ __forceinline__ uint32_t word8(const uint4& lo, const uint4& hi, int i) {
+    const uint4& v = i < 4 ? lo : hi;
+    const int j = i & 3;
+    return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
+}
+
+struct PlanLayout {
+    int LD;             // staged row length (elements): H + 8, so the 8 rows of an MMA tile hit distinct banks
+    size_t region;      // staged rows / K-split partial sums / coreset scratch (aliased in turn)
+    size_t zs, sidx, smass, masks, cslot, cg, cred, total;
+};
+
+__host__ __device__ inline PlanLayout plan_layout(int T, int H, int E, int k) {
+    PlanLayout L;
+    const int ntt = (T + 7) / 8;
+    const int tpc = (T + kPlanCluster - 1) / kPlanCluster;
+    L.LD = H + 8;
+    size_t region = static_cast<size_t>(ntt) * 8 * L.LD * 2;
+    const size_t part = static_cast<size_t>(32) * 4 * 32 * 4 * sizeof(float);
+    if (part > region) region = part;
+    if (sizeof(CoresetScratch) > region) region = sizeof(CoresetScratch);
+    L.region = (region + 15) / 16 * 16;
+    L.zs = L.region;
+    L.sidx = L.zs + sizeof(float) * tpc * E;
+    L.smass = L.sidx + sizeof(int32_t) * T * k;
+    L.masks = L.smass + sizeof(float) * T * k;
+    L.cslot = L.masks + sizeof(uint32_t) * E * ((T + 31) / 32);
+    L.cg = L.cslot + sizeof(int) * 4 * 33;
+    L.cred = L.cg + sizeof(float) * 4 * 33;
+    L.total = L.cred + sizeof(float) * 4 * 9;
+    return L;
+}
+
+__global__ void __launch_bounds__(kPlanThreads, 1) route_plan_kernel(RoutePlanArgs a) {
+    extern __shared__ __align__(16) uint8_t rp_smem[];
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rank = static_cast<int>(cluster.block_rank());
+    const int CL = kPlanCluster;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, tig = lane & 3;
+    const int T = a.T, H = a.H, E = a.E, k = a.cs.k;
+    const int EPC = E / CL;                        // experts of this CTA
+    const int ett = EPC / 16, kq = 32 / ett;       // expert tiles, K splits (host: ett divides 32)
+    const int kspan = H / kq;                      // multiple of 128 (host)
+    const int ntt = (T + 7) / 8, TPC = (T + CL - 1) / CL;
+    const PlanLayout L = plan_layout(T, H, E, k);
+    bf16* xs = reinterpret_cast<bf16*>(rp_smem);
+    float* part = reinterpret_cast<float*>(rp_smem);
+    float* zs = reinterpret_cast<float*>(rp_smem + L.zs);
+    int32_t* sidx = reinterpret_cast<int32_t*>(rp_smem + L.sidx);
+    float* smass = reinterpret_cast<float*>(rp_smem + L.smass);
+    uint32_t* masks = reinterpret_cast<uint32_t*>(rp_smem + L.masks);
+    const int grp = threadIdx.x >> 8;  // combine: 4 groups of 256 threads, one token each
+    int* c_slot = reinterpret_cast<int*>(rp_smem + L.cslot) + 33 * grp;
+    float* c_g = reinterpret_cast<float*>(rp_smem + L.cg) + 33 * grp;
+    float* c_red = reinterpret_cast<float*>(rp_smem + L.cred) + 9 * grp;
+    {  // router weights are never written: hint this CTA's rows before waiting
+        const char* w = reinterpret_cast<const char*>(a.Wr + static_cast<size_t>(rank) * EPC * H);
+        const int lines = EPC * H * 2 / 128;
+        for (int l = threadIdx.x; l < lines; l += kPlanThreads) asm volatile("prefetch.global.L2 [%0];" ::"l"(w + 128ll * l));
+    }
+    pdl_trigger();
+    pdl_wait();
+    // 1. combine
+    {
+        const int t = rank + CL * grp;
+        const int tt = (grp < TPC && t < T) ? t : -1;
+        if (a.mode == 1)
+            combine_row<bf16, 1>(tt, H, k, a.y, a.slot_of, a.slot_sh, a.gate_rr_prev, a.has_shared, nullptr, a.hres,
+                                 a.x, nullptr, nullptr, c_slot, c_g, c_red);
+        else
+            combine_row<bf16, 2>(tt, H, k, nullptr, nullptr, nullptr, nullptr, 0, a.h_in, a.hres, a.x, nullptr,
+                                 nullptr, c_slot, c_g, c_red);
+    }
+    cluster.sync();  // every token's x row is in global memory (and every CTA has started)
+    // 2. stage x: row t at t*LD, rows T .. 8*ntt-1 zero
+    {
+        const int vpr = H / 8;
+        const int nvec = ntt * 8 * vpr;
+        const uint4* xg = reinterpret_cast<const uint4*>(a.x);
+        for (int i0 = threadIdx.x; i0 < nvec; i0 += 8 * kPlanThreads) {
+            uint4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int i = i0 + u * kPlanThreads;
+                const int row = i / vpr;
+                v[u] = (i < nvec && row < T) ? __ldcg(xg + i) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int i = i0 + u * kPlanThreads;
+                if (i < nvec) {
+                    const int row = i / vpr, c = i - row * vpr;
+                    *reinterpret_cast<uint4*>(xs + static_cast<size_t>(row) * L.LD + c * 8) = v[u];
+                }
+            }
+        }
+    }
+    __syncthreads();
+    // 3. logits.  Thread (g, tig)'s 4 K positions of MMA j in a 64-wide chunk are
+    // elements 16*tig + 4j .. +3 (one permutation of K for A and B, so the sums are
+    // unchanged) and its fragments are plain 16-byte loads.
+    {
+        const int et = warp / kq, q = warp % kq;
+        float d[4][4];
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) d[nt][r] = 0.f;
+        const bf16* w0 = a.Wr + static_cast<size_t>(rank * EPC + et * 16 + g) * H;
+        const bf16* w1 = w0 + static_cast<size_t>(8) * H;
+        for (int h0 = q * kspan; h0 < (q + 1) * kspan; h0 += 64) {
+            const int hb = h0 + 16 * tig;
+            const uint4 a00 = __ldg(reinterpret_cast<const uint4*>(w0 + hb));
+            const uint4 a01 = __ldg(reinterpret_cast<const uint4*>(w0 + hb + 8));
+            const uint4 a10 = __ldg(reinterpret_cast<const uint4*>(w1 + hb));
+            const uint4 a11 = __ldg(reinterpret_cast<const uint4*>(w1 + hb + 8));
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) {
+                if (nt < ntt) {
+                    const bf16* xr = xs + static_cast<size_t>(nt * 8 + g) * L.LD + hb;
+                    const uint4 b0 = *reinterpret_cast<const uint4*>(xr);
+                    const uint4 b1 = *reinterpret_cast<const uint4*>(xr + 8);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        mma_16816(d[nt], word8(a00, a01, 2 * j), word8(a10, a11, 2 * j), word8(a00, a01, 2 * j + 1),
+                                  word8(a10, a11, 2 * j + 1), word8(b0, b1, 2 * j), word8(b0, b1, 2 * j + 1));
+                }
+            }
+        }
+        __syncthreads();  // the staged rows are dead: the partial sums take their place
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+            if (nt < ntt)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) part[((warp * 4 + nt) * 32 + lane) * 4 + r] = d[nt][r];
+    }
+    __syncthreads();
+    // 4. add the K splits in split order (element r of lane ln is expert g + 8*(r>=2)
+    // and token 2*tig + (r&1) of the tile) and store the logit with the CTA that
+    // takes the token's top-k
+    for (int i = threadIdx.x; i < ett * ntt * 128; i += kPlanThreads) {
+        const int tile = i >> 7, ln = (i >> 2) & 31, r = i & 3;
+        const int et = tile / ntt, nt = tile % ntt;
+        float v = 0.f;
+        for (int q = 0; q < kq; ++q) v += part[(((et * kq + q) * 4 + nt) * 32 + ln) * 4 + r];
+        const int el = et * 16 + (ln >> 2) + (r >= 2 ? 8 : 0);
+        const int t = nt * 8 + 2 * (ln & 3) + (r & 1);
+        if (t < T) cluster.map_shared_rank(zs, t % CL)[(t / CL) * E + rank * EPC + el] = v;
+    }
+    if (a.wr_next != nullptr) {  // the next layer's router rows, for the next launch
+        const char* w = reinterpret_cast<const char*>(a.wr_next + static_cast<size_t>(rank) * EPC * H);
+        const int lines = EPC * H * 2 / 128;
+        for (int l = threadIdx.x; l < lines; l += kPlanThreads) asm volatile("prefetch.global.L2 [%0];" ::"l"(w + 128ll * l));
+    }
+    cluster.sync();  // every token's logits are with the CTA that takes its top-k
+    {
+        const int t = rank + CL * warp;
+        if (warp < TPC && t < T)
+            topk_one_token(zs + warp * E, E, k, t, a.idx, a.mass, a.gate, cluster.map_shared_rank(sidx, 0),
+                           cluster.map_shared_rank(smass, 0));
+    }
+    cluster.sync();  // CTA 0 holds every token's experts and routing mass
+    if (rank == 0) {
+        CoresetArgs cs = a.cs;
+        cs.idx = sidx;
+        cs.mass = smass;
+        coreset_body(cs, 0, 1, masks, *reinterpret_cast<CoresetScratch*>(rp_smem));
+        for (int i = threadIdx.x; i < a.n_done; i += kPlanThreads) a.done[i] = 0;
+        __threadfence();
+    }
+    cluster.sync();  // the plan is written
+    // 6. gathered rows: one warp per slot row, 8 16-byte vectors in flight per lane
+    const int n_slots = __ldcg(&a.cs.plan[2]);
+    const uint4* xg = reinterpret_cast<const uint4*>(a.x);
+    for (int sl = rank * (kPlanThreads / 32) + warp; sl < n_slots; sl += CL * (kPlanThreads / 32)) {
+        const int t = __ldcg(&a.cs.slot_tok[sl]);
+        const uint4* src = xg + static_cast<size_t>(t) * a.row_vec;
+        uint4* dst = a.xp + static_cast<size_t>(sl) * a.row_vec;
+        for (int c0 = 0; c0 < a.row_vec; c0 += 256) {
+            uint4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int c = c0 + u * 32 + lane;
+                if (c < a.row_vec) v[u] = __ldcg(src + c);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int c = c0 + u * 32 + lane;
+                if (c < a.row_vec) dst[c] = v[u];
+            }
+        }
     }
 }
 
@@ -535,7 +919,7 @@ cudaError_t launch_topk_from_logits(const float* logits, int T, int E, int k, in
                       gate);
 }
 
-int coreset_smem_bytes(int E, int T) { return E * ((T + 31) / 32) * 4; }
+int coreset_smem_bytes(int E, int T) { return static_cast<int>(sizeof(CoresetScratch)) + E * ((T + 31) / 32) * 4; }
 
 cudaError_t launch_coreset(const CoresetArgs& a, cudaStream_t s) {
     const size_t smem = coreset_smem_bytes(a.E, a.T);
@@ -552,6 +936,39 @@ cudaError_t launch_gather(int dtype, const void* x, int H, const int32_t* slot_t
     return launch_pdl(gather_kernel, dim3(max_slots), dim3(256), 0, s, static_cast<const uint4*>(x), row_vec,
                       slot_tok, plan, static_cast<uint4*>(xp), chunks, static_cast<const char*>(pf_wgu), pf_stride,
                       pf_chunks, done, n_done);
+}
+
+int route_plan_eligible(int R, int dtype, int T, int H, int E, int k) {
+    if (R != 1 || dtype != MOESTEP_BF16 || T < 1 || T > 32 || k > 32 || H > 4096) return 0;
+    if (E % (16 * kPlanCluster) != 0 || E > 512) return 0;
+    const int ett = E / kPlanCluster / 16;
+    if (32 % ett != 0) return 0;
+    if (H % (64 * (32 / ett)) != 0) return 0;
+    return plan_layout(T, H, E, k).total <= 227 * 1024 ? 1 : 0;
+}
+
+size_t route_plan_smem_bytes(int T, int H, int E, int k) { return plan_layout(T, H, E, k).total; }
+
+cudaError_t launch_route_plan(const RoutePlanArgs& a, cudaStream_t s) {
+    const size_t smem = route_plan_smem_bytes(a.T, a.H, a.E, a.cs.k);
+    static int done[64] = {};
+    cudaError_t e = ensure_smem(route_plan_kernel, smem, done);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(kPlanCluster);
+    cfg.blockDim = dim3(kPlanThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kPlanCluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, route_plan_kernel, a);
 }
 
 }  // namespace moestep

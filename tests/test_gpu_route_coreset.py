@@ -134,6 +134,21 @@ def test_coreset_edge_cases():
         np.testing.assert_array_equal(gate_rr, cs.gate_rr)
 
 
+def test_coreset_near_ties_rank_exactly():
+    """Aggregates that differ only far below 2^-22 (the same high word of the 2^-54
+    fixed point) and exact ties: the ranking still follows the exact sums, then ids."""
+    d = ms.ModelDims(H=2048, E=32, k=4, I=512, Is=512, V=1024, P=2, dtype=ms.BF16)
+    q = 2.0 ** -25                                   # one ulp of 0.25 in fp32
+    idx = np.array([[3, 7, 1, 2], [9, 4, 11, 12]], np.int32)
+    mass = np.array([[0.25, 0.25 + q, 0.2, 0.1], [0.1, 0.1, 0.2 + 2 * q, 0.2]], np.float32)
+    for tp in [0.2, 0.5, 1.0]:
+        n_sel, sel, survive, gate_rr, err = coreset_gpu(d, 1, [tp], idx, mass)
+        cs = oracle.coreset_select(idx, mass, tp, 2)
+        assert err == ms.OK and list(sel[0, :n_sel[0]]) == cs.sel[0]
+        np.testing.assert_array_equal(survive, cs.survive)
+    assert cs.sel[0][:4] == [7, 3, 11, 1]           # exact order, not id order
+
+
 def test_coreset_flags_bad_input():
     d = ms.ModelDims(H=2048, E=32, k=4, I=512, Is=512, V=1024, P=4, dtype=ms.BF16)
     idx = np.tile(np.array([5, 3, 99, 1], np.int32), (4, 1))   # 99 >= E
