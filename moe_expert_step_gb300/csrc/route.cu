@@ -15,6 +15,7 @@
 #include "common.cuh"
 #include "kernels.h"
 #include "launch.cuh"
+#include "target.h"
 
 namespace moestep {
 namespace {
@@ -319,7 +320,8 @@ struct CoresetScratch {  // shared memory of one coreset CTA
     uint32_t khi[1024 + 32];  // candidates' aggregates, compacted: high words (zero padded) ...
     int ce[1024];             // ... and expert ids; the full aggregates go to cum
     long long wtot64[32];
-    int s_last, s_nr, s_nrc, s_m;
+    long long s_target;
+    int s_last, s_nr, s_nrc;
     uint8_t csurv[kCandCache];
 };
 
@@ -332,7 +334,6 @@ __device__ void coreset_body(const CoresetArgs& a, int r, int nreq, uint32_t* ma
     int* cidx = sc.cidx;
     float* cmass = sc.cmass;
     uint8_t* csurv = sc.csurv;
-    long long* wtot64 = sc.wtot64;
     int& s_last = sc.s_last;
     int& s_nr = sc.s_nr;
     int& s_nrc = sc.s_nrc;
@@ -378,8 +379,8 @@ __device__ void coreset_body(const CoresetArgs& a, int r, int nreq, uint32_t* ma
     // compact the candidate experts in id order: cum[p] = aggregate, khi[p] = its high
     // word, ce[p] = expert id
     const int flag = (tid < E && cnt[tid] > 0) ? 1 : 0;
-    const int incl = block_inclusive_scan<int>(flag, reinterpret_cast<int*>(wtot64));
-    const int nC = reinterpret_cast<int*>(wtot64)[31];
+    const int incl = block_inclusive_scan<int>(flag, reinterpret_cast<int*>(sc.wtot64));
+    const int nC = reinterpret_cast<int*>(sc.wtot64)[31];
     if (flag) {
         cum[incl - 1] = A[tid];
         sc.khi[incl - 1] = static_cast<uint32_t>(static_cast<unsigned long long>(A[tid]) >> 32);
@@ -429,46 +430,21 @@ __device__ void coreset_body(const CoresetArgs& a, int r, int nreq, uint32_t* ma
         }
     }
     __syncthreads();
-    // the cut, by one warp: m = smallest prefix of the ranked candidates whose
-    // aggregate reaches ceil(top_p * total) (exact integer sums, any order)
-    if (tid < 32) {
-        const int per = (nC + 31) >> 5;
-        const int lo = min(nC, tid * per), hi = min(nC, lo + per);
-        long long own = 0;
-        for (int i = lo; i < hi; ++i) own += A[order[i]];
-        long long incl64 = own;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const long long n = __shfl_up_sync(0xffffffffu, incl64, o);
-            if (tid >= o) incl64 += n;
-        }
-        const long long total = __shfl_sync(0xffffffffu, incl64, 31);
-        int m;
-        if (!(tp > 0.0f)) {  // NaN or non-positive fraction: keep everything and flag the input
-            if (tid == 0) record_error(a.err, kErrBadInput);
-            m = nC;
-        } else if (tp >= 1.0f || total == 0) {
-            m = nC;
-        } else {
-            long long target =
-                static_cast<long long>(ceil(__dmul_rn(static_cast<double>(tp), __ll2double_rn(total))));
-            target = target < 1 ? 1 : (target > total ? total : target);
-            long long run = incl64 - own;
-            int below = 0;  // ranked prefixes whose sum is still short of the target
-            for (int i = lo; i < hi; ++i) {
-                run += A[order[i]];
-                below += run < target ? 1 : 0;
-            }
-            m = 1 + __reduce_add_sync(0xffffffffu, below);
-            m = m > nC ? nC : m;
-        }
-        if (tid == 0) {
-            sc.s_m = m;
-            a.n_sel[r] = m;
-        }
+    // the cut: m = smallest prefix of the ranked candidates whose aggregate reaches
+    // ceil(top_p * total) (exact integer sums; one thread takes the target)
+    long long v = (tid < nC) ? A[order[tid]] : 0;
+    v = block_inclusive_scan<long long>(v, sc.wtot64);
+    const long long total = sc.wtot64[31];
+    int m = nC;
+    if (!(tp > 0.0f)) {  // NaN or non-positive fraction: keep everything and flag the input
+        if (tid == 0) record_error(a.err, kErrBadInput);
+    } else if (tp < 1.0f && total != 0) {
+        if (tid == 0) sc.s_target = coreset_target(tp, total);
+        __syncthreads();
+        m = 1 + __syncthreads_count(tid < nC && v < sc.s_target);
+        m = m > nC ? nC : m;
     }
-    __syncthreads();
-    const int m = sc.s_m;
+    if (tid == 0) a.n_sel[r] = m;
     if (tid < E) keep[tid] = (keep[tid] >= 0 && keep[tid] < m);
     if (tid < m) a.sel[r * E + tid] = order[tid];
     __syncthreads();
@@ -568,7 +544,7 @@ __device__ void coreset_body(const CoresetArgs& a, int r, int nreq, uint32_t* ma
     const int my_nch = (my_cnt + a.nch - 1) / a.nch;
     // one scan of (chunks << 32 | slots)
     const long long both = block_inclusive_scan<long long>(
-        (static_cast<long long>(my_nch) << 32) | static_cast<long long>(my_cnt), wtot64);
+        (static_cast<long long>(my_nch) << 32) | static_cast<long long>(my_cnt), sc.wtot64);
     const int slot_end = static_cast<int>(both & 0xffffffffll);
     const int chunk_end = static_cast<int>(both >> 32);
     const int slot_base = slot_end - my_cnt;
