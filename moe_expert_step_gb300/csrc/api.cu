@@ -272,9 +272,16 @@ CoresetArgs coreset_args(const Ctx& c, int R, const float* top_p, const int32_t*
     return a;
 }
 
+// Wgu (may be NULL): the layer's gate/up weights, hinted into L2 for the first candidates
 int run_coreset(const Ctx& c, int R, const float* top_p, const int32_t* idx, const float* mass, int32_t* n_sel,
-                int32_t* sel, uint8_t* survive, float* gate_rr) {
-    const CoresetArgs a = coreset_args(c, R, top_p, idx, mass, n_sel, sel, survive, gate_rr);
+                int32_t* sel, uint8_t* survive, float* gate_rr, const void* Wgu = nullptr) {
+    CoresetArgs a = coreset_args(c, R, top_p, idx, mass, n_sel, sel, survive, gate_rr);
+    if (Wgu != nullptr && c.d->dtype == MOESTEP_BF16 && c.sms > R) {
+        a.pf_base = static_cast<const char*>(Wgu);
+        a.pf_stride = 2ll * c.d->I * c.d->H * 2;
+        a.pf_experts = kCoresetPrefetchExperts;
+        a.pf_ctas = c.sms - R;
+    }
     MOESTEP_LAUNCH(1, launch_coreset(a, c.s));
     return MOESTEP_OK;
 }
@@ -319,10 +326,10 @@ int run_experts(const Ctx& c, int R, const void* x, const moestep_layer* layer, 
     const Layout& L = c.L;
     const int* plan = at<int>(c.ws, L.hdr) + 32;
     const bool tc = d->dtype == MOESTEP_BF16;
-    if (!gathered) MOESTEP_LAUNCH(2, launch_gather(d->dtype, x, d->H, at<int32_t>(c.ws, L.slot_tok), plan, L.max_slots,
-                                    at<void>(c.ws, L.xp), at<int4>(c.ws, L.chunks), tc ? layer->Wgu : nullptr,
-                                    2ll * d->I * d->H * 2, kPrefetchChunks, tc ? at<int>(c.ws, L.done) : nullptr,
-                                    L.max_chunks, c.s));
+    if (!gathered)
+        MOESTEP_LAUNCH(2, launch_gather(d->dtype, x, d->H, at<int32_t>(c.ws, L.slot_tok), plan, L.max_slots,
+                                        at<void>(c.ws, L.xp), tc ? at<int>(c.ws, L.done) : nullptr, L.max_chunks,
+                                        c.s));
     if (d->dtype == MOESTEP_F32) {
         MOESTEP_LAUNCH(3, launch_f32_gateup(d->H, d->E, d->I, d->Is, L.max_slots, at<float>(c.ws, L.xp),
                                             at<int32_t>(c.ws, L.slot_exp), plan, static_cast<const float*>(layer->Wgu),
@@ -638,7 +645,7 @@ int block_decode_step(const moestep_dims* dims, int R, int n_layers, const moest
         }
         MOESTEP_TRY(run_route(c, T, x, layers[l].Wr, idx, at<float>(ws, L.mass), at<float>(ws, L.gate), nullptr));
         MOESTEP_TRY(run_coreset(c, R, top_p, idx, at<float>(ws, L.mass), nsel, sel,
-                                at<uint8_t>(ws, L.survive), at<float>(ws, L.gaterr)));
+                                at<uint8_t>(ws, L.survive), at<float>(ws, L.gaterr), layers[l].Wgu));
         MOESTEP_TRY(run_experts(c, R, x, &layers[l]));
         MOESTEP_LAUNCH(5, launch_combine(1, dims->dtype, T, dims->H, k, at<float>(ws, L.y),
                                          at<int32_t>(ws, L.slot_of), at<int32_t>(ws, L.slot_sh),

@@ -79,12 +79,21 @@ struct CoresetArgs {
     int nch;
     int has_shared;
     int* err;
+    // optional L2 hints: CTAs R .. R+pf_ctas-1 of the coreset launch hint the
+    // weights (pf_stride bytes from pf_base + e * pf_stride) of the pf_experts
+    // lowest-id experts that any token picked, while CTAs 0 .. R-1 run the coreset
+    const char* pf_base;
+    long long pf_stride;
+    int pf_experts;
+    int pf_ctas;
 };
 
 cudaError_t launch_route(int dtype, const void* x, const void* Wr, int T, int H, int E, int k, float* logits,
                          int32_t* idx, float* mass, float* gate, int* counters, int* err, cudaStream_t s);
 cudaError_t launch_topk_from_logits(const float* logits, int T, int E, int k, int32_t* idx, float* mass,
                                     float* gate, cudaStream_t s);
+// experts whose gate/up weights the coreset launch hints into L2 in the block step
+constexpr int kCoresetPrefetchExperts = 32;
 cudaError_t launch_coreset(const CoresetArgs& a, cudaStream_t s);
 int coreset_smem_bytes(int E, int T);
 // One request (T <= 32, bf16): the previous layer's combine + RMSNorm, router,
@@ -115,12 +124,10 @@ int route_plan_eligible(int R, int dtype, int T, int H, int E, int k);
 size_t route_plan_smem_bytes(int T, int H, int E, int k);
 cudaError_t launch_route_plan(const RoutePlanArgs& a, cudaStream_t s);
 
-// xp[slot] = x[slot_tok[slot]]; zeroes done[0..n_done) (fused expert kernel counters); optionally hints into L2 the gate/up weights (pf_wgu, pf_stride bytes per
-// expert) of the plan's first pf_chunks chunks
+// xp[slot] = x[slot_tok[slot]] for the plan's slots; zeroes done[0..n_done)
+// (the fused expert launch's counters; NULL: none)
 cudaError_t launch_gather(int dtype, const void* x, int H, const int32_t* slot_tok, const int* plan,
-                          int max_slots, void* xp, const int4* chunks, const void* pf_wgu, long long pf_stride,
-                          int pf_chunks, int* done, int n_done, cudaStream_t s);
-constexpr int kPrefetchChunks = 10;  // ~40 MiB of gate/up weights at the Clover layer shape
+                          int max_slots, void* xp, int* done, int n_done, cudaStream_t s);
 
 // ------------------------------------------------------------------ combine / norm / embed
 // mode 0: out = routed + shared; mode 1: h += routed + shared, x = RMSNorm(h); mode 2: h = h_in, x = RMSNorm(h)

@@ -594,12 +594,65 @@ __device__ void coreset_body(const CoresetArgs& a, int r, int nreq, uint32_t* ma
     }
 }
 
-// grid R, 1024 threads: one CTA per request (see coreset_body).
+// L2 hints by the extra CTAs of the coreset launch: the union of the experts the
+// router picked, then the gate/up weights of its pf_experts lowest ids (the
+// expert launch takes the kept experts in id order, so these are the first it
+// streams; most candidates are kept).  Hints only: nothing is written.
+constexpr int kMaxPrefetchExperts = 64;
+__device__ void coreset_prefetch(const CoresetArgs& a, uint32_t* bits) {
+    __shared__ int s_pe[kMaxPrefetchExperts];
+    __shared__ int s_npe;
+    const int tid = threadIdx.x;
+    const int E = a.E, nw = (E + 31) >> 5;
+    const int npf = min(a.pf_experts, kMaxPrefetchExperts);
+    for (int i = tid; i < nw; i += blockDim.x) bits[i] = 0u;
+    __syncthreads();
+    for (int c = tid; c < a.T * a.k; c += blockDim.x) {
+        const int e = __ldg(&a.idx[c]);
+        if (e >= 0 && e < E) atomicOr(&bits[e >> 5], 1u << (e & 31));
+    }
+    __syncthreads();
+    if (tid < 32) {  // the first npf set bits in id order
+        int found = 0;
+        for (int w0 = 0; w0 < nw && found < npf; w0 += 32) {
+            uint32_t word = w0 + tid < nw ? bits[w0 + tid] : 0u;
+            int incl = __popc(word);
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int n = __shfl_up_sync(0xffffffffu, incl, o);
+                if (tid >= o) incl += n;
+            }
+            int pos = found + incl - __popc(word);
+            while (word != 0u && pos < npf) {
+                const int b = __ffs(word) - 1;
+                s_pe[pos++] = (w0 + tid) * 32 + b;
+                word &= word - 1u;
+            }
+            found = min(npf, found + __shfl_sync(0xffffffffu, incl, 31));
+        }
+        if (tid == 0) s_npe = found;
+    }
+    __syncthreads();
+    const long long lines_per = a.pf_stride >> 7;
+    const long long total = lines_per * s_npe;
+    const long long stride = static_cast<long long>(gridDim.x - a.R) * blockDim.x;
+    for (long long l = static_cast<long long>(blockIdx.x - a.R) * blockDim.x + tid; l < total; l += stride) {
+        const int j = static_cast<int>(l / lines_per);
+        const char* p = a.pf_base + static_cast<long long>(s_pe[j]) * a.pf_stride + ((l - j * lines_per) << 7);
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+    }
+}
+
+// grid R (+ pf_ctas hint CTAs), 1024 threads: one CTA per request (see coreset_body).
 __global__ void __launch_bounds__(kCoresetThreads) coreset_kernel(CoresetArgs a) {
     extern __shared__ __align__(16) uint8_t coreset_smem[];  // scratch, then masks [E][ceil(T/32)]
     pdl_trigger();
     pdl_wait();
-    coreset_body(a, blockIdx.x, gridDim.x, reinterpret_cast<uint32_t*>(coreset_smem + sizeof(CoresetScratch)),
+    if (static_cast<int>(blockIdx.x) >= a.R) {
+        coreset_prefetch(a, reinterpret_cast<uint32_t*>(coreset_smem));
+        return;
+    }
+    coreset_body(a, blockIdx.x, a.R, reinterpret_cast<uint32_t*>(coreset_smem + sizeof(CoresetScratch)),
                  *reinterpret_cast<CoresetScratch*>(coreset_smem));
 }
 
@@ -829,16 +882,11 @@ __global__ void __launch_bounds__(kPlanThreads, 1) route_plan_kernel(RoutePlanAr
     }
 }
 
-// One CTA per slot: xp[slot] = x[slot_tok[slot]].  Then, while HBM would
-// otherwise idle until the expert GEMM starts streaming, every thread hints a
-// few 128-byte lines of the gate/up weights of the first chunks in the plan
-// (the experts the GEMM processes first) into L2.  The hints are
-// fire-and-forget: nothing waits for them.
+// One CTA per slot: xp[slot] = x[slot_tok[slot]]; CTA 0 also zeroes the
+// expert launch's chunk counters.
 __global__ void __launch_bounds__(256) gather_kernel(const uint4* __restrict__ x, int row_vec,
                                                      const int32_t* __restrict__ slot_tok, const int* __restrict__ plan,
-                                                     uint4* __restrict__ xp, const int4* __restrict__ chunks,
-                                                     const char* __restrict__ pf_base, long long pf_stride,
-                                                     int pf_chunks, int* __restrict__ done, int n_done) {
+                                                     uint4* __restrict__ xp, int* __restrict__ done, int n_done) {
     const int slot = blockIdx.x;
     pdl_trigger();
     pdl_wait();
@@ -848,18 +896,6 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint4* __restrict__ x
         const int t = slot_tok[slot];
         for (int i = threadIdx.x; i < row_vec; i += blockDim.x)
             xp[static_cast<size_t>(slot) * row_vec + i] = x[static_cast<size_t>(t) * row_vec + i];
-    }
-    if (pf_base != nullptr) {
-        const int nc = min(pf_chunks, plan[0]);
-        const long long lines_per = pf_stride >> 7;
-        const long long total = lines_per * nc;
-        const long long nthreads = static_cast<long long>(gridDim.x) * blockDim.x;
-        for (long long l = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; l < total; l += nthreads) {
-            const int c = static_cast<int>(l / lines_per);
-            const long long off = (l - c * lines_per) << 7;
-            const char* p = pf_base + static_cast<long long>(chunks[c].x) * pf_stride + off;
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-        }
     }
 }
 
@@ -902,16 +938,15 @@ cudaError_t launch_coreset(const CoresetArgs& a, cudaStream_t s) {
     static int done[64] = {};
     cudaError_t e = ensure_smem(coreset_kernel, smem, done);
     if (e != cudaSuccess) return e;
-    return launch_pdl(coreset_kernel, dim3(a.R), dim3(kCoresetThreads), smem, s, a);
+    const int helpers = (a.pf_base != nullptr && a.pf_experts > 0) ? a.pf_ctas : 0;
+    return launch_pdl(coreset_kernel, dim3(a.R + helpers), dim3(kCoresetThreads), smem, s, a);
 }
 
 cudaError_t launch_gather(int dtype, const void* x, int H, const int32_t* slot_tok, const int* plan, int max_slots,
-                          void* xp, const int4* chunks, const void* pf_wgu, long long pf_stride, int pf_chunks,
-                          int* done, int n_done, cudaStream_t s) {
+                          void* xp, int* done, int n_done, cudaStream_t s) {
     const int row_vec = H * (dtype == MOESTEP_BF16 ? 2 : 4) / 16;
     return launch_pdl(gather_kernel, dim3(max_slots), dim3(256), 0, s, static_cast<const uint4*>(x), row_vec,
-                      slot_tok, plan, static_cast<uint4*>(xp), chunks, static_cast<const char*>(pf_wgu), pf_stride,
-                      pf_chunks, done, n_done);
+                      slot_tok, plan, static_cast<uint4*>(xp), done, n_done);
 }
 
 int route_plan_eligible(int R, int dtype, int T, int H, int E, int k) {
