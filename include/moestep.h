@@ -210,6 +210,25 @@ int block_decode_step(const moestep_dims* dims, int R, int n_layers, const moest
                       float* conf, uint8_t* accept, int32_t* n_committed, const moestep_trace* trace,
                       void* ws, size_t ws_bytes, void* stream);
 
+/* The whole LowConfidence loop of one block on the device ([AIT 三] block
+ * decoding loop; [GRM] "How does confidence-threshold block decoding
+ * work?"): while any position of the R requests is masked and fewer than
+ * max_rounds rounds have run, h = block_embed(tokens, masked) and one
+ * block_decode_step (no h_out, no trace).  The rounds run as the body of a
+ * CUDA-graph while node whose condition a device kernel sets after each
+ * commit, so no round returns to the host.
+ *   emb, pos, mask_id as in block_embed; the model and top_p, logit_scale,
+ *   threshold as in block_decode_step; tokens/masked [R*P] in/out;
+ *   rounds [1] int32 (device, output): the rounds that ran.
+ * The executable graph is cached and reused while every argument (pointers,
+ * sizes, scalars, the layer array's contents) is unchanged, and rebuilt
+ * otherwise.  Kernel timing (moestep_prof_enable) does not apply inside the
+ * loop.  max_rounds >= 0; 0 runs nothing.  Not thread-safe. */
+int block_decode_loop(const moestep_dims* dims, int R, int n_layers, const moestep_layer* layers, const void* Wlm,
+                      const void* emb, const void* pos, int mask_id, const float* top_p, float logit_scale,
+                      float threshold, int max_rounds, int32_t* tokens, uint8_t* masked, int32_t* rounds,
+                      void* ws, size_t ws_bytes, void* stream);
+
 /* Synchronously reads and clears the workspace's device error word (host *word:
  * 0 or a MOESTEP_E* code).  Waits for `stream`. */
 int moestep_read_device_error(void* ws, size_t ws_bytes, void* stream, int* word);

@@ -30,7 +30,8 @@ PROF_KERNELS = ["route", "coreset", "gather", "expert_ffn", "expert_down", "comb
 
 EXPORTS = [
     "moestep_workspace_size", "moestep_workspace_init", "moe_block_route", "moe_route_from_logits", "coreset_select", "moe_block_ffn",
-    "lm_head_commit", "lm_commit_from_logits", "block_embed", "block_decode_step", "moestep_read_device_error",
+    "lm_head_commit", "lm_commit_from_logits", "block_embed", "block_decode_step", "block_decode_loop",
+    "moestep_read_device_error",
     "moestep_error_string", "moestep_last_cuda_error", "moestep_prof_enable", "moestep_prof_read",
     "moestep_set_wait_timeout_ns", "moestep_set_route_fusion", "moestep_launch_count", "moe_block_route_noalloc",
 ]
@@ -84,6 +85,7 @@ def lib():
             "block_embed": [D, i, vp, vp, vp, vp, i, vp, vp],
             "block_decode_step": [D, i, i, ctypes.POINTER(Layer), vp, vp, f, f, vp, vp, vp, vp, vp, vp, vp, vp,
                                   ctypes.POINTER(Trace), vp, sz, vp],
+            "block_decode_loop": [D, i, i, ctypes.POINTER(Layer), vp, vp, vp, i, vp, f, f, i, vp, vp, vp, vp, sz, vp],
             "moestep_read_device_error": [vp, sz, vp, ctypes.POINTER(i)],
             "moestep_error_string": [i],
             "moestep_last_cuda_error": [],
@@ -222,6 +224,16 @@ def block_decode_step(d: ModelDims, R: int, layers, Wlm, top_p, threshold, h_in,
                                    float(threshold), _p(h_in), _p(h_out), _p(tokens), _p(masked), _p(choice),
                                    _p(conf), _p(accept), _p(n_committed), ctypes.byref(tr), _p(ws), ws.numel(),
                                    _s(stream)), "block_decode_step")
+
+
+def block_decode_loop(d: ModelDims, R: int, layers, Wlm, emb, pos, mask_id: int, top_p, threshold, tokens, masked,
+                      rounds, ws, max_rounds=None, logit_scale=1.0, stream=None) -> None:
+    """Every LowConfidence round of the block on the device (CUDA-graph while loop); rounds[0] = rounds run."""
+    arr = (Layer * max(1, len(layers)))(*layers)
+    mr = d.P if max_rounds is None else int(max_rounds)
+    _check(lib().block_decode_loop(ctypes.byref(d.c()), R, len(layers), arr, _p(Wlm), _p(emb), _p(pos), int(mask_id),
+                                   _p(top_p), float(logit_scale), float(threshold), mr, _p(tokens), _p(masked),
+                                   _p(rounds), _p(ws), ws.numel(), _s(stream)), "block_decode_loop")
 
 
 def read_device_error(ws, stream=None) -> int:

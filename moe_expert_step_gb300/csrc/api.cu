@@ -16,6 +16,9 @@
 #include "moestep.h"
 
 namespace moestep {
+
+bool g_launch_pdl = true;
+
 namespace {
 
 thread_local int g_last_cuda = 0;
@@ -46,7 +49,8 @@ int lm_nch_for(int T) { return T <= 32 ? 32 : T <= 64 ? 64 : T <= 128 ? 128 : 25
 struct Layout {
     int T, max_slots, max_chunks, act_ld, n_ptiles, nch, lm_nch, route_groups;
     size_t hdr, counters, counters_bytes, logits, idx, mass, gate, nsel, sel, survive, gaterr, slot_of, slot_sh,
-        slot_tok, slot_exp, chunks, done, xp, act, y, hres, x, pmax, parg, psum, lmlogits, total;
+        slot_tok, slot_exp, chunks, done, xp, act, y, hres, x, pmax, parg, psum, lmlogits, loop_h, loop_choice,
+        loop_conf, loop_accept, loop_ncomm, total;
 };
 
 Layout make_layout(const moestep_dims& d, int R) {
@@ -95,6 +99,12 @@ Layout make_layout(const moestep_dims& d, int R) {
     L.parg = take(sizeof(int) * L.n_ptiles * T);
     L.psum = take(sizeof(float) * L.n_ptiles * T);
     L.lmlogits = take(d.dtype == MOESTEP_F32 ? sizeof(float) * T * static_cast<size_t>(d.V) : 0);
+    // device-resident round loop: embedded block and the per-round commit outputs
+    L.loop_h = take(sizeof(float) * T * d.H);
+    L.loop_choice = take(sizeof(int32_t) * T);
+    L.loop_conf = take(sizeof(float) * T);
+    L.loop_accept = take(static_cast<size_t>(T));
+    L.loop_ncomm = take(sizeof(int32_t) * R);
     L.total = o;
     return L;
 }
@@ -273,14 +283,18 @@ CoresetArgs coreset_args(const Ctx& c, int R, const float* top_p, const int32_t*
 }
 
 // Wgu (may be NULL): the layer's gate/up weights, hinted into L2 for the first candidates
+// Wr_next (may be NULL): the next layer's router weights, hinted too
 int run_coreset(const Ctx& c, int R, const float* top_p, const int32_t* idx, const float* mass, int32_t* n_sel,
-                int32_t* sel, uint8_t* survive, float* gate_rr, const void* Wgu = nullptr) {
+                int32_t* sel, uint8_t* survive, float* gate_rr, const void* Wgu = nullptr,
+                const void* Wr_next = nullptr) {
     CoresetArgs a = coreset_args(c, R, top_p, idx, mass, n_sel, sel, survive, gate_rr);
     if (Wgu != nullptr && c.d->dtype == MOESTEP_BF16 && c.sms > R) {
         a.pf_base = static_cast<const char*>(Wgu);
         a.pf_stride = 2ll * c.d->I * c.d->H * 2;
         a.pf_experts = kCoresetPrefetchExperts;
         a.pf_ctas = c.sms - R;
+        a.pf_next = static_cast<const char*>(Wr_next);
+        a.pf_next_bytes = 2ll * c.d->E * c.d->H;
     }
     MOESTEP_LAUNCH(1, launch_coreset(a, c.s));
     return MOESTEP_OK;
@@ -464,6 +478,98 @@ using namespace moestep;
         if (rc_ != MOESTEP_OK) return rc_; \
     } while (0)
 
+namespace {
+
+// ---------------------------------------------------------------------------- device-resident round loop
+// One cached executable graph: [condition kernel (rounds = 0)] -> while node
+// { block_embed, block_decode_step, condition kernel (rounds += 1) }.
+struct LoopGraph {
+    std::vector<unsigned char> key;
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t exec = nullptr;
+};
+std::mutex g_loop_mu;
+LoopGraph g_loop;
+cudaStream_t g_capture_stream[64] = {};
+
+template <typename V>
+void key_add(std::vector<unsigned char>& k, const V& v) {
+    const unsigned char* p = reinterpret_cast<const unsigned char*>(&v);
+    k.insert(k.end(), p, p + sizeof(V));
+}
+
+void loop_release() {
+    if (g_loop.exec) cudaGraphExecDestroy(g_loop.exec);
+    if (g_loop.graph) cudaGraphDestroy(g_loop.graph);
+    g_loop = LoopGraph{};
+}
+
+}  // namespace
+
+namespace {
+
+// Builds [condition (rounds = 0)] -> while { embed, step, condition (rounds += 1) } by
+// capture on `cs`.  Returns a MOESTEP_E* code for invalid arguments, else OK with the
+// CUDA status in *err (graph and exec set on success; nothing kept on failure).
+int build_loop_graph(const moestep_dims* dims, int R, int n_layers, const moestep_layer* layers, const void* Wlm,
+                     const void* emb, const void* pos, int mask_id, const float* top_p, float logit_scale,
+                     float threshold, int max_rounds, int32_t* tokens, uint8_t* masked, int32_t* rounds, void* ws,
+                     size_t ws_bytes, const Layout& L, cudaStream_t cs, cudaGraph_t* g_out, cudaGraphExec_t* ex_out,
+                     cudaError_t* err) {
+    cudaGraph_t g = nullptr;
+    cudaGraphConditionalHandle h = 0;
+    int rc = MOESTEP_OK;
+    cudaError_t e = cudaGraphCreate(&g, 0);
+    if (e == cudaSuccess) e = cudaGraphConditionalHandleCreate(&h, g, 0, 0);
+    if (e == cudaSuccess) e = cudaStreamBeginCaptureToGraph(cs, g, nullptr, nullptr, 0, cudaStreamCaptureModeRelaxed);
+    if (e == cudaSuccess) {
+        const cudaError_t le = launch_loop_cond(h, masked, L.T, rounds, max_rounds, 0, cs);
+        cudaGraph_t got = nullptr;
+        e = cudaStreamEndCapture(cs, &got);
+        if (e == cudaSuccess) e = le;
+    }
+    cudaGraphNode_t first = nullptr;
+    size_t n_nodes = 1;
+    if (e == cudaSuccess) e = cudaGraphGetNodes(g, &first, &n_nodes);
+    cudaGraphNodeParams cp{};
+    cp.type = cudaGraphNodeTypeConditional;
+    cp.conditional.handle = h;
+    cp.conditional.type = cudaGraphCondTypeWhile;
+    cp.conditional.size = 1;
+    cudaGraphNode_t wnode = nullptr;
+    if (e == cudaSuccess) e = cudaGraphAddNode(&wnode, g, &first, nullptr, 1, &cp);
+    if (e == cudaSuccess)
+        e = cudaStreamBeginCaptureToGraph(cs, cp.conditional.phGraph_out[0], nullptr, nullptr, 0,
+                                          cudaStreamCaptureModeRelaxed);
+    if (e == cudaSuccess) {
+        float* hb = at<float>(ws, L.loop_h);
+        rc = block_embed(dims, R, tokens, masked, emb, pos, mask_id, hb, cs);
+        if (rc == MOESTEP_OK)
+            rc = block_decode_step(dims, R, n_layers, layers, Wlm, top_p, logit_scale, threshold, hb, nullptr,
+                                        tokens, masked, at<int32_t>(ws, L.loop_choice), at<float>(ws, L.loop_conf),
+                                        at<uint8_t>(ws, L.loop_accept), at<int32_t>(ws, L.loop_ncomm), nullptr, ws,
+                                        ws_bytes, cs);
+        cudaError_t le = cudaSuccess;
+        if (rc == MOESTEP_OK) le = launch_loop_cond(h, masked, L.T, rounds, max_rounds, 1, cs);
+        cudaGraph_t got = nullptr;
+        e = cudaStreamEndCapture(cs, &got);
+        if (e == cudaSuccess) e = le;
+    }
+    cudaGraphExec_t ex = nullptr;
+    if (e == cudaSuccess && rc == MOESTEP_OK) e = cudaGraphInstantiate(&ex, g, 0);
+    if (e != cudaSuccess || rc != MOESTEP_OK) {
+        if (g) cudaGraphDestroy(g);
+        *err = e;
+        return rc;
+    }
+    *g_out = g;
+    *ex_out = ex;
+    *err = cudaSuccess;
+    return MOESTEP_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 int moestep_workspace_size(const moestep_dims* dims, int R, size_t* bytes) {
@@ -645,7 +751,8 @@ int block_decode_step(const moestep_dims* dims, int R, int n_layers, const moest
         }
         MOESTEP_TRY(run_route(c, T, x, layers[l].Wr, idx, at<float>(ws, L.mass), at<float>(ws, L.gate), nullptr));
         MOESTEP_TRY(run_coreset(c, R, top_p, idx, at<float>(ws, L.mass), nsel, sel,
-                                at<uint8_t>(ws, L.survive), at<float>(ws, L.gaterr), layers[l].Wgu));
+                                at<uint8_t>(ws, L.survive), at<float>(ws, L.gaterr), layers[l].Wgu,
+                                last ? nullptr : layers[l + 1].Wr));
         MOESTEP_TRY(run_experts(c, R, x, &layers[l]));
         MOESTEP_LAUNCH(5, launch_combine(1, dims->dtype, T, dims->H, k, at<float>(ws, L.y),
                                          at<int32_t>(ws, L.slot_of), at<int32_t>(ws, L.slot_sh),
@@ -655,6 +762,70 @@ int block_decode_step(const moestep_dims* dims, int R, int n_layers, const moest
     MOESTEP_TRY(run_lm_commit(c, R, x, Wlm, logit_scale, threshold, tokens, masked, choice, conf, accept, n_committed,
                               nullptr));
     if (h_out) MOESTEP_CK(cudaMemcpyAsync(h_out, hres, sizeof(float) * T * dims->H, cudaMemcpyDeviceToDevice, c.s));
+    return MOESTEP_OK;
+}
+
+int block_decode_loop(const moestep_dims* dims, int R, int n_layers, const moestep_layer* layers, const void* Wlm,
+                      const void* emb, const void* pos, int mask_id, const float* top_p, float logit_scale,
+                      float threshold, int max_rounds, int32_t* tokens, uint8_t* masked, int32_t* rounds,
+                      void* ws, size_t ws_bytes, void* stream) {
+    MOESTEP_TRY(check_dims(dims));
+    MOESTEP_TRY(check_R(dims, R));
+    if (max_rounds < 0 || !rounds || !emb || !pos || !tokens || !masked) return MOESTEP_EINVAL;
+    if (n_layers < 0 || (n_layers > 0 && !layers)) return MOESTEP_EINVAL;
+    MOESTEP_TRY(check_ws(dims, R, ws, ws_bytes));
+    MOESTEP_TRY(device_check(nullptr));
+    int dev = 0;
+    MOESTEP_CK(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= 64) return MOESTEP_EDEVICE;
+    const Layout L = make_layout(*dims, R);
+    std::vector<unsigned char> key;
+    key_add(key, dev);
+    key_add(key, *dims);
+    key_add(key, R);
+    key_add(key, n_layers);
+    for (int l = 0; l < n_layers; ++l) key_add(key, layers[l]);
+    const void* ptrs[] = {Wlm, emb, pos, top_p, tokens, masked, rounds, ws};
+    for (const void* q : ptrs) key_add(key, q);
+    key_add(key, ws_bytes);
+    key_add(key, mask_id);
+    key_add(key, logit_scale);
+    key_add(key, threshold);
+    key_add(key, max_rounds);
+    key_add(key, g_route_plan);
+    key_add(key, g_timeout_ns);
+    std::lock_guard<std::mutex> lock(g_loop_mu);
+    if (g_loop.exec == nullptr || g_loop.key != key) {
+        loop_release();
+        if (g_capture_stream[dev] == nullptr)
+            MOESTEP_CK(cudaStreamCreateWithFlags(&g_capture_stream[dev], cudaStreamNonBlocking));
+        cudaStream_t cs = g_capture_stream[dev];
+        const int prof_mask = g_prof.mask;  // event records are not allowed in a loop body
+        g_prof.mask = 0;
+        cudaGraph_t g = nullptr;
+        cudaGraphExec_t ex = nullptr;
+        int rc = MOESTEP_OK;
+        cudaError_t e = cudaSuccess;
+        // with programmatic edges between the round's kernels; without, if the graph refuses them
+        for (int attempt = 0; attempt < 2; ++attempt) {
+            g_launch_pdl = attempt == 0;
+            rc = build_loop_graph(dims, R, n_layers, layers, Wlm, emb, pos, mask_id, top_p, logit_scale, threshold,
+                                  max_rounds, tokens, masked, rounds, ws, ws_bytes, L, cs, &g, &ex, &e);
+            if (rc != MOESTEP_OK || e == cudaSuccess) break;
+            cudaGetLastError();
+        }
+        g_launch_pdl = true;
+        g_prof.mask = prof_mask;
+        if (rc != MOESTEP_OK) return rc;
+        if (e != cudaSuccess) {
+            g_last_cuda = static_cast<int>(e);
+            return MOESTEP_ECUDA;
+        }
+        g_loop.key = std::move(key);
+        g_loop.graph = g;
+        g_loop.exec = ex;
+    }
+    MOESTEP_CK(cudaGraphLaunch(g_loop.exec, static_cast<cudaStream_t>(stream)));
     return MOESTEP_OK;
 }
 

@@ -86,6 +86,8 @@ struct CoresetArgs {
     long long pf_stride;
     int pf_experts;
     int pf_ctas;
+    const char* pf_next;      // also hinted by those CTAs: pf_next_bytes from here (the next layer's router)
+    long long pf_next_bytes;
 };
 
 cudaError_t launch_route(int dtype, const void* x, const void* Wr, int T, int H, int E, int k, float* logits,
@@ -164,5 +166,10 @@ int device_ok(int* sms);                   // current device is sm_103; *sms = i
 // ------------------------------------------------------------------ profiling hooks (api.cu)
 void prof_begin(int kid, cudaStream_t s);
 void prof_end(int kid, cudaStream_t s);
+
+// Round loop: sets the while-node condition h to (any masked && rounds < max_rounds);
+// add = 1 increments *rounds first, add = 0 sets it to 0.
+cudaError_t launch_loop_cond(cudaGraphConditionalHandle h, const uint8_t* masked, int T, int32_t* rounds,
+                             int max_rounds, int add, cudaStream_t s);
 
 }  // namespace moestep

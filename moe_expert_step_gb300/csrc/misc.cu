@@ -283,6 +283,21 @@ int grid_1d(long long work, int per_block = 256) {
     return static_cast<int>(g);
 }
 
+// Round-loop condition (one CTA): continue while any position of the block is
+// masked and fewer than max_rounds rounds have run.  add = 1 counts the round
+// that just ended (inside the loop body); add = 0 starts the count (before it).
+__global__ void __launch_bounds__(256) loop_cond_kernel(cudaGraphConditionalHandle h, const uint8_t* __restrict__ masked,
+                                                        int T, int32_t* __restrict__ rounds, int max_rounds, int add) {
+    int any = 0;
+    for (int t = threadIdx.x; t < T; t += blockDim.x) any |= masked[t] != 0;
+    any = __syncthreads_or(any);
+    if (threadIdx.x == 0) {
+        const int r = add ? *rounds + 1 : 0;
+        *rounds = r;
+        cudaGraphSetConditional(h, (any && r < max_rounds) ? 1u : 0u);
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_combine(int mode, int dtype, int T, int H, int k, const float* y, const int32_t* slot_of,
@@ -343,6 +358,12 @@ cudaError_t launch_commit(int R, int P, int n_tiles, const float* pmax, const in
                           uint8_t* accept, int32_t* n_committed, int* counters, cudaStream_t s) {
     return launch_pdl(commit_kernel, dim3(R * P), dim3(256), 0, s, P, R * P, n_tiles, pmax, parg, psum, threshold,
                       tokens, masked, choice, conf, accept, n_committed, counters);
+}
+
+cudaError_t launch_loop_cond(cudaGraphConditionalHandle h, const uint8_t* masked, int T, int32_t* rounds,
+                             int max_rounds, int add, cudaStream_t s) {
+    loop_cond_kernel<<<1, 256, 0, s>>>(h, masked, T, rounds, max_rounds, add);
+    return cudaGetLastError();
 }
 
 }  // namespace moestep

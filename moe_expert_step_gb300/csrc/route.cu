@@ -401,6 +401,7 @@ __device__ void coreset_body(const CoresetArgs& a, int r, int nreq, uint32_t* ma
         int gt = 0, eq = 0;
         if (mine_ok) {
             const int nblk = (nC + 3) >> 2;
+#pragma unroll 4
             for (int b = part; b < nblk; b += parts) {
                 const uint4 h = *reinterpret_cast<const uint4*>(&sc.khi[4 * b]);
                 gt += (h.x > mh) + (h.y > mh) + (h.z > mh) + (h.w > mh);
@@ -636,11 +637,15 @@ __device__ void coreset_prefetch(const CoresetArgs& a, uint32_t* bits) {
     const long long lines_per = a.pf_stride >> 7;
     const long long total = lines_per * s_npe;
     const long long stride = static_cast<long long>(gridDim.x - a.R) * blockDim.x;
-    for (long long l = static_cast<long long>(blockIdx.x - a.R) * blockDim.x + tid; l < total; l += stride) {
+    const long long g = static_cast<long long>(blockIdx.x - a.R) * blockDim.x + tid;
+    for (long long l = g; l < total; l += stride) {
         const int j = static_cast<int>(l / lines_per);
         const char* p = a.pf_base + static_cast<long long>(s_pe[j]) * a.pf_stride + ((l - j * lines_per) << 7);
         asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
     }
+    if (a.pf_next != nullptr)
+        for (long long l = g; l < (a.pf_next_bytes >> 7); l += stride)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(a.pf_next + (l << 7)));
 }
 
 // grid R (+ pf_ctas hint CTAs), 1024 threads: one CTA per request (see coreset_body).
@@ -978,7 +983,7 @@ cudaError_t launch_route_plan(const RoutePlanArgs& a, cudaStream_t s) {
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 2;
+    cfg.numAttrs = g_launch_pdl ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, route_plan_kernel, a);
 }
 
