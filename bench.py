@@ -42,6 +42,9 @@ def parse():
     ap.add_argument("--requests", type=int, default=1, help="concurrent requests (blocks) per GPU")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-loop", action="store_true", help="skip the whole-block round-loop measurement")
+    ap.add_argument("--loop-scale", type=float, default=16.0,
+                    help="logit scale of the round-loop measurement (1 = every round is a fallback)")
     ap.add_argument("--prof-all", action="store_true", help="time every kernel in the roofline pass")
     ap.add_argument("--no-graph", action="store_true", help="time direct launches instead of CUDA-graph replays")
     ap.add_argument("--route-fusion", action="store_true",
@@ -305,6 +308,10 @@ def run_gpu(args, dist: Dist):
                "d2h_bytes_per_step": d2h,
                "how": "wall clock over K public-API calls (Python binding -> C ABI), each with pinned H2D inputs, "
                       "the step, D2H of tokens/masked/n_committed and a stream synchronize"}
+    # ---------------- the whole block: device-resident round loop vs rounds driven from the host
+    round_loop = None
+    if not args.no_loop:
+        round_loop = measure_round_loop(ms, W, cfg, d, R, layers, Wlm, top_p, ws, args.loop_scale, dist)
     if ms.read_device_error(ws) != ms.OK:
         raise RuntimeError("device error word set during the benchmark")
 
@@ -357,10 +364,77 @@ def run_gpu(args, dist: Dist):
         "roofline": roofline,
         "kernel_ms_per_step": {k: round(v[1] / steps_prof, 4) for k, v in prof.items() if v[0]},
         "clocks": clk, "gpu_launches": launches, "e2e": e2e,
+        "round_loop": round_loop,
         "graph": not args.no_graph,
         "setup_s": round(t_setup, 1),
     }
     return line, cfg
+
+
+def measure_round_loop(ms, W, cfg, d, R, layers, Wlm, top_p, ws, scale, dist, blocks=3):
+    """Decode whole blocks (every position masked at the start) with block_decode_loop, the
+    rounds as one CUDA-graph while loop, and with the same rounds driven from the host
+    (block_embed + block_decode_step, reading `masked` back after each round)."""
+    import numpy as np
+    import torch
+
+    T = R * cfg.P
+    emb = W.to_device(W.host_activations(cfg, "emb", cfg.V), "bf16")
+    pos = W.to_device(W.host_activations(cfg, "pos", cfg.P), "bf16")
+    tokens = torch.zeros(T, dtype=torch.int32, device="cuda")
+    masked = torch.ones(T, dtype=torch.uint8, device="cuda")
+    rounds = torch.zeros(1, dtype=torch.int32, device="cuda")
+    h = torch.empty((T, cfg.H), dtype=torch.float32, device="cuda")
+    choice = torch.empty(T, dtype=torch.int32, device="cuda")
+    conf = torch.empty(T, dtype=torch.float32, device="cuda")
+    accept = torch.empty(T, dtype=torch.uint8, device="cuda")
+    ncomm = torch.empty(R, dtype=torch.int32, device="cuda")
+
+    def device_block():
+        tokens.zero_()
+        masked.fill_(1)
+        ms.block_decode_loop(d, R, layers, Wlm, emb, pos, cfg.V - 1, top_p, THRESHOLD, tokens, masked, rounds, ws,
+                             logit_scale=scale)
+
+    def host_block():
+        tokens.zero_()
+        masked.fill_(1)
+        n = 0
+        while bool(masked.any().item()) and n < cfg.P:
+            ms.block_embed(d, R, tokens, masked, emb, pos, cfg.V - 1, h)
+            ms.block_decode_step(d, R, layers, Wlm, top_p, THRESHOLD, h, tokens, masked, choice, conf, accept,
+                                 ncomm, ws, logit_scale=scale)
+            n += 1
+        return n
+
+    device_block()
+    torch.cuda.synchronize()
+    dev_tokens, n_rounds = tokens.clone(), int(rounds.item())
+    n_host = host_block()
+    torch.cuda.synchronize()
+    if n_host != n_rounds or not torch.equal(tokens, dev_tokens):
+        raise RuntimeError("device round loop differs from the host-driven rounds")
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist.barrier()
+    e0.record(stream)
+    for _ in range(blocks):
+        device_block()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_dev = dist.max(e0.elapsed_time(e1)) / blocks
+    t0 = time.perf_counter()
+    for _ in range(blocks):
+        host_block()
+    torch.cuda.synchronize()
+    ms_host = dist.max(time.perf_counter() - t0) * 1e3 / blocks
+    del emb, pos
+    return {"what": "whole blocks: all positions masked, rounds until none is (LowConfidence, threshold "
+                    f"{THRESHOLD}), R={R}; synthetic N(0,1) bf16 embedding and positional tables",
+            "logit_scale": scale, "rounds_per_block": n_rounds, "positions_per_round": round(T / n_rounds / R, 3),
+            "ms_per_block_device_loop": round(ms_dev, 3), "ms_per_block_host_loop": round(ms_host, 3),
+            "committed_tokens_per_s_device_loop": round(dist.world * T / (ms_dev / 1e3), 1),
+            "blocks_timed": blocks, "identical_to_host_loop": True}
 
 
 def load_peaks() -> dict:
