@@ -38,7 +38,8 @@ def parse():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gpu", "reference"], default="gpu")
-    ap.add_argument("--config", choices=["clover_stack40", "clover_layer"], default="clover_stack40")
+    ap.add_argument("--config", choices=["clover_stack40", "clover_layer", "clover_stack40_fp8", "clover_layer_fp8"],
+                    default="clover_stack40")
     ap.add_argument("--requests", type=int, default=1, help="concurrent requests (blocks) per GPU")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
     ap.add_argument("--no-e2e", action="store_true")
@@ -141,7 +142,9 @@ def workload(name: str):
 
 def workload_desc(cfg, R: int) -> dict:
     return {"workload": f"{cfg.name}: {cfg.n_layers}-layer MoE FFN stack (H={cfg.H}, {cfg.E} routed experts top-{cfg.k}, "
-                        f"expert/shared SwiGLU I={cfg.I}, 1 shared expert, bf16 weights, fp32 accumulate), "
+                        f"expert/shared SwiGLU I={cfg.I}, 1 shared expert, "
+                        f"{'FP8 E4M3 expert weights with per-row fp32 scales, bf16 router and LM head' if cfg.dtype == 'fp8' else 'bf16 weights'}"
+                        f", fp32 accumulate), "
                         f"block of {cfg.P} tokens x {R} request(s), coreset top_p {TOP_P}, RMSNorm eps 1e-6 "
                         f"between layers, LM head V={cfg.V}, LowConfidence commit threshold {THRESHOLD}",
             "layers": cfg.n_layers, "block_tokens": cfg.P, "requests": R, "top_p": TOP_P,
@@ -155,8 +158,12 @@ def workload_desc(cfg, R: int) -> dict:
 def expert_bytes(cfg, unions) -> dict:
     """Algorithmic HBM bytes of one step: each selected expert's weights once, shared experts,
     routers and the LM head."""
-    per_expert = 3 * cfg.I * cfg.H * 2
-    shared = 3 * cfg.Is * cfg.H * 2
+    if cfg.dtype == "fp8":   # one byte per weight plus one fp32 scale per weight row
+        per_expert = 3 * cfg.I * cfg.H + (2 * cfg.I + cfg.H) * 4
+        shared = 3 * cfg.Is * cfg.H + (2 * cfg.Is + cfg.H) * 4
+    else:
+        per_expert = 3 * cfg.I * cfg.H * 2
+        shared = 3 * cfg.Is * cfg.H * 2
     experts = sum(unions) * per_expert + cfg.n_layers * shared
     return {"expert_weights": experts, "router": cfg.n_layers * cfg.E * cfg.H * 2, "lm_head": cfg.V * cfg.H * 2,
             "per_expert": per_expert, "shared_per_layer": shared}
@@ -174,10 +181,12 @@ def run_gpu(args, dist: Dist):
     cfg = workload(args.config)
     R = args.requests
     T = R * cfg.P
-    d = ms.ModelDims(H=cfg.H, E=cfg.E, k=cfg.k, I=cfg.I, Is=cfg.Is, V=cfg.V, P=cfg.P, dtype=ms.BF16)
+    d = ms.ModelDims(H=cfg.H, E=cfg.E, k=cfg.k, I=cfg.I, Is=cfg.Is, V=cfg.V, P=cfg.P,
+                     dtype=ms.FP8 if cfg.dtype == "fp8" else ms.BF16)
     t_setup = time.time()
     layers_t = [W.device_layer(cfg, l) for l in range(cfg.n_layers)]
-    layers = [ms.layer(l["Wr"], l["Wgu"], l["Wd"], l["Wsgu"], l["Wsd"]) for l in layers_t]
+    layers = [ms.layer(l["Wr"], l["Wgu"], l["Wd"], l["Wsgu"], l["Wsd"], l.get("Sgu"), l.get("Sd"), l.get("Ssgu"),
+                       l.get("Ssd")) for l in layers_t]
     Wlm = W.device_lm_head(cfg)
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
     h0_host = W.host_h0(cfg, R)
@@ -335,7 +344,7 @@ def run_gpu(args, dist: Dist):
     roofline = {"kernel": "tc_gemm_kernel<experts> (routed + shared expert gate/up, SwiGLU and down in one launch)",
                 "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                 "frac": round(achieved / hbm_peak, 4) if hbm_peak else None,
-                "traffic": load_traffic(statistics.mean(unions) + 1),
+                "traffic": load_traffic(statistics.mean(unions) + 1) if cfg.dtype != "fp8" else None,
                 "peak_source": peaks.get("source"),
                 "bytes_per_launch": int(ff_bytes_launch), "avg_launch_ms": round(ff_avg_ms, 5),
                 "launches_timed": ff_n}
@@ -344,7 +353,8 @@ def run_gpu(args, dist: Dist):
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": dist.world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": round(ms_step, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 experts, bf16 rest" if cfg.dtype == "fp8" else "bf16",
+        "data": "synthetic",
         "config": {**workload_desc(cfg, R), "route_fusion": R == 1 and args.route_fusion},
         "expert_weight_hbm": {
             "bytes_per_step": step_bytes, "expert_bytes_per_step": eb["expert_weights"],

@@ -58,9 +58,14 @@ extern "C" {
 /* Element type of weights and MoE activations. */
 #define MOESTEP_BF16 0 /* bf16 storage, fp32 accumulation on tcgen05 tensor cores */
 #define MOESTEP_F32 1  /* fp32 storage and fp32 FFMA arithmetic (accuracy path) */
+/* FP8 E4M3 expert weights (routed and shared; one fp32 scale per weight row),
+ * everything else as MOESTEP_BF16: the expert launch converts each weight tile
+ * to f16 in shared memory (exact), multiplies by f16 token rows on tcgen05
+ * with fp32 accumulation and applies the row scales in its epilogue. */
+#define MOESTEP_FP8 2
 
 /* Model dimensions.  Supported: 1 <= k <= min(E, 32), E <= 1024, P <= 1024.
- * bf16 path additionally: H % 128 == 0, I % 64 == 0, Is % 64 == 0.
+ * bf16 and fp8 paths additionally: H % 128 == 0, I % 64 == 0, Is % 64 == 0.
  * Is == 0 means no shared expert. */
 typedef struct {
     int H;     /* hidden size */
@@ -70,16 +75,20 @@ typedef struct {
     int Is;    /* shared-expert intermediate size (0 = none) */
     int V;     /* vocabulary size of the LM head */
     int P;     /* block size: positions per request (32 by default in [AIT 三]) */
-    int dtype; /* MOESTEP_BF16 or MOESTEP_F32 */
+    int dtype; /* MOESTEP_BF16, MOESTEP_F32 or MOESTEP_FP8 */
 } moestep_dims;
 
-/* Device weights of one MoE layer (element type = dims.dtype).
+/* Device weights of one MoE layer (element type = dims.dtype; with
+ * MOESTEP_FP8 the router is bf16 and the four expert tensors are E4M3 bytes).
  *   Wr   [E][H]        router
  *   Wgu  [E][I][2][H]  per expert, gate and up projections interleaved by row:
  *                      row 2i is gate row i, row 2i+1 is up row i
  *   Wd   [E][H][I]     per expert down projection
  *   Wsgu [Is][2][H]    shared expert gate/up, same interleaving (NULL iff Is == 0)
  *   Wsd  [H][Is]       shared expert down (NULL iff Is == 0)
+ *   Sgu  [E][2I], Sd [E][H], Ssgu [2Is], Ssd [H]: fp32 scale of each weight
+ *                      row (MOESTEP_FP8 only, NULL otherwise): a weight is
+ *                      its E4M3 value times its row's scale
  * The interleaving puts the two halves of each SwiGLU pair into neighbouring
  * accumulator rows, so the tensor-core epilogue combines them with one shuffle. */
 typedef struct {
@@ -88,6 +97,10 @@ typedef struct {
     const void* Wd;
     const void* Wsgu;
     const void* Wsd;
+    const float* Sgu;
+    const float* Sd;
+    const float* Ssgu;
+    const float* Ssd;
 } moestep_layer;
 
 /* Optional per-layer records written by block_decode_step (any field may be NULL). */

@@ -15,6 +15,7 @@ from . import _build
 
 BF16 = 0
 F32 = 1
+FP8 = 2
 
 OK = 0
 EINVAL = -1
@@ -48,7 +49,7 @@ class Dims(ctypes.Structure):
 
 
 class Layer(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_void_p) for n in ("Wr", "Wgu", "Wd", "Wsgu", "Wsd")]
+    _fields_ = [(n, ctypes.c_void_p) for n in ("Wr", "Wgu", "Wd", "Wsgu", "Wsd", "Sgu", "Sd", "Ssgu", "Ssd")]
 
 
 class Trace(ctypes.Structure):
@@ -147,8 +148,9 @@ class ModelDims:
         return Dims(self.H, self.E, self.k, self.I, self.Is, self.V, self.P, self.dtype)
 
 
-def layer(Wr, Wgu, Wd, Wsgu=None, Wsd=None) -> Layer:
-    return Layer(_p(Wr), _p(Wgu), _p(Wd), _p(Wsgu), _p(Wsd))
+def layer(Wr, Wgu, Wd, Wsgu=None, Wsd=None, Sgu=None, Sd=None, Ssgu=None, Ssd=None) -> Layer:
+    """Device pointers of one layer; the four row-scale tensors only with FP8 expert weights."""
+    return Layer(_p(Wr), _p(Wgu), _p(Wd), _p(Wsgu), _p(Wsd), _p(Sgu), _p(Sd), _p(Ssgu), _p(Ssd))
 
 
 def workspace_size(d: ModelDims, R: int) -> int:

@@ -35,6 +35,9 @@ bool g_route_plan = false;  // one request: the single cluster launch between ex
     } while (0)
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// element type of everything but the expert weights (router, activations, LM head)
+int act_dtype(int dtype) { return dtype == MOESTEP_FP8 ? MOESTEP_BF16 : dtype; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Token chunk of a unit (the MMA's N is at most this).  The expert GEMM caps it
@@ -56,7 +59,7 @@ struct Layout {
 Layout make_layout(const moestep_dims& d, int R) {
     Layout L{};
     const int T = R * d.P;
-    const size_t esz = d.dtype == MOESTEP_BF16 ? 2 : 4;
+    const size_t esz = d.dtype == MOESTEP_F32 ? 4 : 2;
     L.T = T;
     L.max_slots = T * d.k + T;
     L.max_chunks = T * d.k + d.E + T + 1;
@@ -118,11 +121,11 @@ P* at(void* ws, size_t off) {
 int check_dims(const moestep_dims* d) {
     if (d == nullptr) return MOESTEP_EINVAL;
     if (d->H <= 0 || d->E <= 0 || d->k <= 0 || d->I <= 0 || d->Is < 0 || d->P <= 0 || d->V <= 0) return MOESTEP_EINVAL;
-    if (d->dtype != MOESTEP_BF16 && d->dtype != MOESTEP_F32) return MOESTEP_EINVAL;
+    if (d->dtype != MOESTEP_BF16 && d->dtype != MOESTEP_F32 && d->dtype != MOESTEP_FP8) return MOESTEP_EINVAL;
     if (d->k > d->E || d->k > 32 || d->E > 1024 || d->P > 1024) return MOESTEP_EUNSUPPORTED;
     if (d->H % 8 || d->I % 4 || d->Is % 4) return MOESTEP_EUNSUPPORTED;
     if (8ll * (d->H > d->E ? d->H : d->E) * 4 > 200 * 1024) return MOESTEP_EUNSUPPORTED;  // router staging
-    if (d->dtype == MOESTEP_BF16 && (d->H % 128 || d->I % 64 || d->Is % 64)) return MOESTEP_EUNSUPPORTED;
+    if (d->dtype != MOESTEP_F32 && (d->H % 128 || d->I % 64 || d->Is % 64)) return MOESTEP_EUNSUPPORTED;
     return MOESTEP_OK;
 }
 
@@ -187,6 +190,23 @@ int get_encode() {
 
 // 2D bf16 tensor [rows][cols] (cols contiguous), boxes of 64 columns x box_rows
 // rows in the 128-byte swizzled shared-memory layout; out-of-range rows read as 0.
+// FP8 E4M3 weights: 64-byte rows of 64 elements, unswizzled (the expert launch's
+// converter warps write the swizzled f16 operand themselves)
+int make_map_fp8(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows) {
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols};
+    cuuint32_t box[2] = {64, 64};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        g_last_cuda = static_cast<int>(r);
+        return MOESTEP_ECUDA;
+    }
+    return MOESTEP_OK;
+}
+
 int make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
     cuuint64_t dims[2] = {cols, rows};
     cuuint64_t strides[1] = {cols * 2};
@@ -248,7 +268,7 @@ int run_route(const Ctx& c, int T, const void* x, const void* Wr, int32_t* idx, 
               float* logits) {
     const moestep_dims* d = c.d;
     float* lg = logits ? logits : at<float>(c.ws, c.L.logits);
-    MOESTEP_LAUNCH(0, launch_route(d->dtype, x, Wr, T, d->H, d->E, d->k, lg, idx, mass, gate,
+    MOESTEP_LAUNCH(0, launch_route(act_dtype(d->dtype), x, Wr, T, d->H, d->E, d->k, lg, idx, mass, gate,
                                    at<int>(c.ws, c.L.counters), at<int>(c.ws, c.L.hdr), c.s));
     return MOESTEP_OK;
 }
@@ -288,9 +308,9 @@ int run_coreset(const Ctx& c, int R, const float* top_p, const int32_t* idx, con
                 int32_t* sel, uint8_t* survive, float* gate_rr, const void* Wgu = nullptr,
                 const void* Wr_next = nullptr) {
     CoresetArgs a = coreset_args(c, R, top_p, idx, mass, n_sel, sel, survive, gate_rr);
-    if (Wgu != nullptr && c.d->dtype == MOESTEP_BF16 && c.sms > R) {
+    if (Wgu != nullptr && c.d->dtype != MOESTEP_F32 && c.sms > R) {
         a.pf_base = static_cast<const char*>(Wgu);
-        a.pf_stride = 2ll * c.d->I * c.d->H * 2;
+        a.pf_stride = 2ll * c.d->I * c.d->H * (c.d->dtype == MOESTEP_FP8 ? 1 : 2);
         a.pf_experts = kCoresetPrefetchExperts;
         a.pf_ctas = c.sms - R;
         a.pf_next = static_cast<const char*>(Wr_next);
@@ -339,7 +359,7 @@ int run_experts(const Ctx& c, int R, const void* x, const moestep_layer* layer, 
     const moestep_dims* d = c.d;
     const Layout& L = c.L;
     const int* plan = at<int>(c.ws, L.hdr) + 32;
-    const bool tc = d->dtype == MOESTEP_BF16;
+    const bool tc = d->dtype != MOESTEP_F32;
     if (!gathered)
         MOESTEP_LAUNCH(2, launch_gather(d->dtype, x, d->H, at<int32_t>(c.ws, L.slot_tok), plan, L.max_slots,
                                         at<void>(c.ws, L.xp), tc ? at<int>(c.ws, L.done) : nullptr, L.max_chunks,
@@ -356,12 +376,20 @@ int run_experts(const Ctx& c, int R, const void* x, const moestep_layer* layer, 
     }
     if (get_encode() != MOESTEP_OK) return MOESTEP_ECUDA;
     const bool sh = d->Is > 0;
+    const bool f8 = d->dtype == MOESTEP_FP8;
     TensorMaps m;
     int rc;
-    if ((rc = make_map(&m.a[0], layer->Wgu, d->H, 2ull * d->E * d->I, 64))) return rc;
-    if ((rc = make_map(&m.a[1], sh ? layer->Wsgu : layer->Wgu, d->H, sh ? 2ull * d->Is : 128, 64))) return rc;
-    if ((rc = make_map(&m.a[2], layer->Wd, d->I, 1ull * d->E * d->H, 64))) return rc;
-    if ((rc = make_map(&m.a[3], sh ? layer->Wsd : layer->Wd, sh ? d->Is : d->I, d->H, 64))) return rc;
+    if (f8) {
+        if ((rc = make_map_fp8(&m.a[0], layer->Wgu, d->H, 2ull * d->E * d->I))) return rc;
+        if ((rc = make_map_fp8(&m.a[1], sh ? layer->Wsgu : layer->Wgu, d->H, sh ? 2ull * d->Is : 128))) return rc;
+        if ((rc = make_map_fp8(&m.a[2], layer->Wd, d->I, 1ull * d->E * d->H))) return rc;
+        if ((rc = make_map_fp8(&m.a[3], sh ? layer->Wsd : layer->Wd, sh ? d->Is : d->I, d->H))) return rc;
+    } else {
+        if ((rc = make_map(&m.a[0], layer->Wgu, d->H, 2ull * d->E * d->I, 64))) return rc;
+        if ((rc = make_map(&m.a[1], sh ? layer->Wsgu : layer->Wgu, d->H, sh ? 2ull * d->Is : 128, 64))) return rc;
+        if ((rc = make_map(&m.a[2], layer->Wd, d->I, 1ull * d->E * d->H, 64))) return rc;
+        if ((rc = make_map(&m.a[3], sh ? layer->Wsd : layer->Wd, sh ? d->Is : d->I, d->H, 64))) return rc;
+    }
     if ((rc = make_map(&m.b[0], at<void>(c.ws, L.xp), d->H, L.max_slots, 16))) return rc;
     if ((rc = make_map(&m.b[1], at<void>(c.ws, L.act), L.act_ld, L.max_slots, 16))) return rc;
     GemmParams g{};
@@ -387,7 +415,11 @@ int run_experts(const Ctx& c, int R, const void* x, const moestep_layer* layer, 
     g.out2 = at<void>(c.ws, L.y);
     g.out2_ld = d->H;
     g.done = at<int>(c.ws, L.done);
-    MOESTEP_LAUNCH(3, launch_tc_gemm(kExperts, L.nch, m, g, c.sms, c.s));
+    g.sc[0] = layer->Sgu;
+    g.sc[1] = sh ? layer->Ssgu : layer->Sgu;
+    g.sc[2] = layer->Sd;
+    g.sc[3] = sh ? layer->Ssd : layer->Sd;
+    MOESTEP_LAUNCH(3, launch_tc_gemm(f8 ? kExpertsF8 : kExperts, L.nch, m, g, c.sms, c.s));
     return MOESTEP_OK;
 }
 
@@ -398,7 +430,7 @@ int run_lm_commit(const Ctx& c, int R, const void* hidden, const void* Wlm, floa
     const Layout& L = c.L;
     const int T = R * d->P;
     int n_tiles;
-    if (d->dtype == MOESTEP_BF16) {
+    if (d->dtype != MOESTEP_F32) {
         if (get_encode() != MOESTEP_OK) return MOESTEP_ECUDA;
         TensorMaps m;
         int rc;
@@ -441,6 +473,10 @@ int layer_ok(const moestep_dims* d, const moestep_layer* l) {
     if (d->Is > 0 && (!l->Wsgu || !l->Wsd)) return MOESTEP_EINVAL;
     if (!aligned16(l->Wr) || !aligned16(l->Wgu) || !aligned16(l->Wd)) return MOESTEP_EALIGN;
     if (d->Is > 0 && (!aligned16(l->Wsgu) || !aligned16(l->Wsd))) return MOESTEP_EALIGN;
+    if (d->dtype == MOESTEP_FP8) {
+        if (!l->Sgu || !l->Sd || (d->Is > 0 && (!l->Ssgu || !l->Ssd))) return MOESTEP_EINVAL;
+        if (d->H % 16 || d->I % 16 || d->Is % 16) return MOESTEP_EALIGN;  // FP8 row strides
+    }
     return MOESTEP_OK;
 }
 
@@ -646,7 +682,7 @@ int moe_block_ffn(const moestep_dims* dims, int R, const void* x, const moestep_
     MOESTEP_TRY(device_check(&sms));
     Ctx c{dims, make_layout(*dims, R), ws, static_cast<cudaStream_t>(stream), sms};
     MOESTEP_TRY(run_experts(c, R, x, layer));
-    MOESTEP_LAUNCH(5, launch_combine(0, dims->dtype, c.L.T, dims->H, dims->k, at<float>(ws, c.L.y),
+    MOESTEP_LAUNCH(5, launch_combine(0, act_dtype(dims->dtype), c.L.T, dims->H, dims->k, at<float>(ws, c.L.y),
                                      at<int32_t>(ws, c.L.slot_of), at<int32_t>(ws, c.L.slot_sh), gate_rr,
                                      dims->Is > 0, nullptr, nullptr, nullptr, nullptr, out, c.s));
     return MOESTEP_OK;
@@ -699,7 +735,7 @@ int block_embed(const moestep_dims* dims, int R, const int32_t* tokens, const ui
     if (mask_id < 0 || mask_id >= dims->V) return MOESTEP_EINVAL;
     MOESTEP_TRY(device_check(nullptr));
     Ctx c{dims, Layout{}, nullptr, static_cast<cudaStream_t>(stream), 0};
-    MOESTEP_LAUNCH(8, launch_embed(dims->dtype, R * dims->P, dims->H, dims->P, dims->V, tokens, masked, emb, pos,
+    MOESTEP_LAUNCH(8, launch_embed(act_dtype(dims->dtype), R * dims->P, dims->H, dims->P, dims->V, tokens, masked, emb, pos,
                                    mask_id, h, c.s));
     return MOESTEP_OK;
 }
@@ -730,7 +766,7 @@ int block_decode_step(const moestep_dims* dims, int R, int n_layers, const moest
     const bool one_block = g_route_plan && n_layers > 0 &&
                            route_plan_eligible(R, dims->dtype, T, dims->H, dims->E, k);
     if (!one_block)
-        MOESTEP_LAUNCH(5, launch_combine(2, dims->dtype, T, dims->H, k, nullptr, nullptr, nullptr, nullptr, 0, h_in,
+        MOESTEP_LAUNCH(5, launch_combine(2, act_dtype(dims->dtype), T, dims->H, k, nullptr, nullptr, nullptr, nullptr, 0, h_in,
                                          hres, x, n_layers == 0 ? hid_trace : nullptr, nullptr, c.s));
     for (int l = 0; l < n_layers; ++l) {
         int32_t* idx = (trace && trace->idx) ? trace->idx + static_cast<size_t>(l) * T * k : at<int32_t>(ws, L.idx);
@@ -743,7 +779,7 @@ int block_decode_step(const moestep_dims* dims, int R, int n_layers, const moest
                                        idx, nsel, sel));
             MOESTEP_TRY(run_experts(c, R, x, &layers[l], true));
             if (last)
-                MOESTEP_LAUNCH(5, launch_combine(1, dims->dtype, T, dims->H, k, at<float>(ws, L.y),
+                MOESTEP_LAUNCH(5, launch_combine(1, act_dtype(dims->dtype), T, dims->H, k, at<float>(ws, L.y),
                                                  at<int32_t>(ws, L.slot_of), at<int32_t>(ws, L.slot_sh),
                                                  at<float>(ws, L.gaterr), dims->Is > 0, nullptr, hres, x, hid_trace,
                                                  nullptr, c.s));
@@ -754,7 +790,7 @@ int block_decode_step(const moestep_dims* dims, int R, int n_layers, const moest
                                 at<uint8_t>(ws, L.survive), at<float>(ws, L.gaterr), layers[l].Wgu,
                                 last ? nullptr : layers[l + 1].Wr));
         MOESTEP_TRY(run_experts(c, R, x, &layers[l]));
-        MOESTEP_LAUNCH(5, launch_combine(1, dims->dtype, T, dims->H, k, at<float>(ws, L.y),
+        MOESTEP_LAUNCH(5, launch_combine(1, act_dtype(dims->dtype), T, dims->H, k, at<float>(ws, L.y),
                                          at<int32_t>(ws, L.slot_of), at<int32_t>(ws, L.slot_sh),
                                          at<float>(ws, L.gaterr), dims->Is > 0, nullptr, hres, x,
                                          last ? hid_trace : nullptr, nullptr, c.s));

@@ -40,6 +40,7 @@ namespace moestep {
 namespace {
 
 constexpr int kThreads = 192;
+constexpr int kThreadsF8 = 320;  // + four warps converting FP8 weight tiles to f16
 constexpr uint64_t kTeardownNs = 1000000000ull;  // fixed limit for draining in-flight copies/MMAs
 constexpr int kABytes = 16384;            // 128 rows x 64 bf16
 constexpr int kBoxBBytes = 16 * 128;      // 16 rows x 64 bf16
@@ -50,6 +51,20 @@ __host__ __device__ constexpr int num_stages(int nch) {
     return (kSmemBudget / stage_bytes(nch)) > 10 ? 10 : (kSmemBudget / stage_bytes(nch));
 }
 __host__ __device__ constexpr int smem_bytes(int nch) { return num_stages(nch) * stage_bytes(nch) + 512 + 1024; }
+
+// FP8 weights: shared memory is one long ring of slots that the TMA warp fills far
+// ahead, each with one 128 x 64 E4M3 weight tile and its token rows (the MMA's B
+// operand, read in place).  The converted f16 A operands live in tensor memory
+// (kF8AStages stages of 32 columns from column kF8AColumn), so the conversion adds
+// no shared-memory traffic beyond reading the FP8 tile once.
+constexpr int kF8Tile = 8192;     // 128 rows x 64 E4M3 bytes
+constexpr int kF8AStages = 8;     // f16 A operands in TMEM
+constexpr int kF8AColumn = 256;   // their first TMEM column (accumulators use 0 .. 2 NCH - 1 <= 128)
+__host__ __device__ constexpr int f8_slot_bytes(int nch) { return kF8Tile + nch * 128; }
+__host__ __device__ constexpr int f8_slots(int nch) {
+    return (kSmemBudget - 1024) / f8_slot_bytes(nch) > 24 ? 24 : (kSmemBudget - 1024) / f8_slot_bytes(nch);
+}
+__host__ __device__ constexpr int smem_bytes_f8(int nch) { return f8_slots(nch) * f8_slot_bytes(nch) + 1024 + 1024; }
 
 struct Unit {
     int kb, rowA0, rowA1, slot0, n, mt, c;
@@ -75,7 +90,7 @@ __device__ __forceinline__ Unit decode_unit(int u, const GemmParams& p, int nrc,
     }
     int rt = p.routed_tiles, st = p.shared_tiles, rkb = p.routed_kb, skb = p.shared_kb, rpe = p.rows_per_expert;
     bool dn = MODE == kDown;
-    if (MODE == kExperts) {
+    if (MODE == kExperts || MODE == kExpertsF8) {
         const int n_gu = nrc * p.routed_tiles + nsc * p.shared_tiles;
         if (u >= n_gu) {  // second half of the unit list: down projections
             u -= n_gu;
@@ -154,21 +169,29 @@ __device__ __forceinline__ void record_timeout(int* err, int role, int u, int kb
 }
 
 template <int MODE, int NCH>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ TensorMaps maps, const GemmParams p) {
-    constexpr int STAGES = num_stages(NCH);
-    constexpr int SB = stage_bytes(NCH);
-    constexpr uint32_t TMEM_COLS = (2 * NCH < 32) ? 32u : static_cast<uint32_t>(2 * NCH);
+    constexpr bool EXP = MODE == kExperts || MODE == kExpertsF8;  // whole routed + shared FFN
+    constexpr bool F8 = MODE == kExpertsF8;                       // FP8 weights, converted in shared memory
+    constexpr int STAGES = F8 ? kF8AStages : num_stages(NCH);  // F8: A stages in TMEM
+    constexpr int SB = F8 ? 0 : stage_bytes(NCH);
+    constexpr int S8 = F8 ? f8_slots(NCH) : 0;            // F8: slots of FP8 tile + token rows
+    constexpr int SL = f8_slot_bytes(NCH);
+    constexpr uint32_t TMEM_COLS = F8 ? 512u : ((2 * NCH < 32) ? 32u : static_cast<uint32_t>(2 * NCH));
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * SB);
+    uint8_t* f8ring = smem + STAGES * SB;  // F8: S8 slots of SL bytes
+    uint64_t* bars = reinterpret_cast<uint64_t*>(f8ring + S8 * SL);
     uint64_t* full = bars;
     uint64_t* empty = bars + STAGES;
     uint64_t* tfull = bars + 2 * STAGES;
     uint64_t* tempty = tfull + 2;
     uint64_t* fin = tempty + 2;
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(fin + 1);
+    uint64_t* conv = fin + 1;            // F8: the stage's weight tile is converted (count 1)
+    uint64_t* full8 = conv + STAGES;     // F8: the slot's FP8 tile and token rows landed (TMA bytes)
+    uint64_t* empty8 = full8 + S8;       // F8: the MMA is done with the slot (count 1)
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(empty8 + S8);
     int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
     int* zero_flag = abort_flag + 1;
 
@@ -185,6 +208,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::mbar_init(&tempty[b], 128);
         }
         tc::mbar_init(fin, 1);
+        if (F8) {
+            for (int s = 0; s < STAGES; ++s) tc::mbar_init(&conv[s], 4);  // one arrival per converter warp
+            for (int s = 0; s < S8; ++s) {
+                tc::mbar_init(&full8[s], 1);
+                tc::mbar_init(&empty8[s], 1);
+            }
+        }
         *abort_flag = 0;
         *zero_flag = 0;
         tc::fence_mbar_init();
@@ -192,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::prefetch_tmap(&maps.b[0]);
         if (MODE != kLmHead) {
             tc::prefetch_tmap(&maps.a[1]);
-            if (MODE == kExperts) {
+            if (EXP) {
                 tc::prefetch_tmap(&maps.a[2]);
                 tc::prefetch_tmap(&maps.a[3]);
                 tc::prefetch_tmap(&maps.b[1]);
@@ -217,12 +247,75 @@ __global__ void __launch_bounds__(kThreads, 1)
         nrc = p.plan[0];
         nsc = p.plan[1];
         n_units = nrc * p.routed_tiles + nsc * p.shared_tiles;
-        if (MODE == kExperts) n_units += nrc * p.dn_routed_tiles + nsc * p.dn_shared_tiles;
+        if (EXP) n_units += nrc * p.dn_routed_tiles + nsc * p.dn_shared_tiles;
     }
     volatile int* abortv = abort_flag;
     const uint64_t tmo = p.timeout_ns;
 
-    if (warp == 0) {
+    if (F8 && warp == 0) {
+        // ------------------------------------------------------------ FP8 tile producer
+        // Fills the FP8 slot ring in unit / K-block order, far ahead of the MMA stages; the
+        // token rows of each stage are loaded by the converter warp that owns the stage.
+        const uint64_t pol = tc::policy_evict_first();
+        uint32_t issued = 0, issued_parity = 0;
+        int slot = 0;
+        uint32_t ph8 = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+            const Unit w = decode_unit<MODE, NCH>(u, p, nrc, nsc);
+            const int nb = (w.n + 15) >> 4;
+            const CUtensorMap* mA = &maps.a[(w.dn ? 2 : 0) + (w.shared ? 1 : 0)];
+            const CUtensorMap* mB = &maps.b[w.dn ? 1 : 0];
+            if (w.dn) {
+                // the SwiGLU rows of this chunk come from gate/up units of other CTAs
+                int good = 1;
+                if (lane == 0)
+                    good = wait_count(&p.done[w.c], 4 * (w.shared ? p.shared_tiles : p.routed_tiles), abortv, tmo);
+                good = __shfl_sync(0xffffffffu, good, 0);
+                if (!good) {
+                    ok = false;
+                    if (lane == 0) record_timeout(p.err, 6, u, -1, -1, 0, n_units, w.n);
+                    break;
+                }
+            }
+            for (int kb = 0; kb < w.kb; ++kb) {
+                int good = 1;
+                if (lane == 0) {
+                    good = tc::mbar_wait(&empty8[slot], ph8 ^ 1u, abortv, tmo);
+                    if (good) {
+                        uint8_t* dst = f8ring + slot * SL;
+                        tc::mbar_arrive_expect_tx(&full8[slot], kF8Tile + nb * kBoxBBytes);
+                        tc::tma_load_2d_hint(dst, mA, &full8[slot], kb * 64, w.rowA0, pol);
+                        tc::tma_load_2d_hint(dst + kF8Tile / 2, mA, &full8[slot], kb * 64, w.rowA1, pol);
+                        for (int b = 0; b < nb; ++b)
+                            tc::tma_load_2d(dst + kF8Tile + b * kBoxBBytes, mB, &full8[slot], kb * 64,
+                                            w.slot0 + 16 * b);
+                        issued |= 1u << slot;
+                        issued_parity = (issued_parity & ~(1u << slot)) | (ph8 << slot);
+                    }
+                }
+                good = __shfl_sync(0xffffffffu, good, 0);
+                if (!good) {
+                    ok = false;
+                    if (lane == 0) record_timeout(p.err, 1, u, kb, slot, ph8, n_units, w.n);
+                    break;
+                }
+                if (++slot == S8) {
+                    slot = 0;
+                    ph8 ^= 1u;
+                }
+            }
+        }
+        if (lane == 0) {
+            if (!ok) {
+                *abort_flag = 1;
+                record_error(p.err, kErrTimeoutProducer);
+            }
+            for (int s = 0; s < S8; ++s)
+                if (issued & (1u << s)) tc::mbar_wait(&full8[s], (issued_parity >> s) & 1u, zero_flag, kTeardownNs);
+        }
+        __syncwarp();
+    } else if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         const uint64_t pol = tc::policy_evict_first();
         uint32_t issued = 0, issued_parity = 0;
@@ -232,9 +325,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
             const Unit w = decode_unit<MODE, NCH>(u, p, nrc, nsc);
             const int nb = (w.n + 15) >> 4;
-            const CUtensorMap* mA = &maps.a[(w.dn && MODE == kExperts ? 2 : 0) + (w.shared ? 1 : 0)];
-            const CUtensorMap* mB = &maps.b[w.dn && MODE == kExperts ? 1 : 0];
-            if (MODE == kExperts && w.dn) {
+            const CUtensorMap* mA = &maps.a[(w.dn && EXP ? 2 : 0) + (w.shared ? 1 : 0)];
+            const CUtensorMap* mB = &maps.b[w.dn && EXP ? 1 : 0];
+            if (EXP && w.dn) {
                 // the SwiGLU rows of this chunk come from gate/up units of other CTAs
                 int good = 1;
                 if (lane == 0)
@@ -252,9 +345,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     good = tc::mbar_wait(&empty[stage], phase ^ 1u, abortv, tmo);
                     if (good) {
                         uint8_t* sa = smem + stage * SB;
-                        tc::mbar_arrive_expect_tx(&full[stage], kABytes + nb * kBoxBBytes);
-                        tc::tma_load_2d_hint(sa, mA, &full[stage], kb * 64, w.rowA0, pol);
-                        tc::tma_load_2d_hint(sa + kABytes / 2, mA, &full[stage], kb * 64, w.rowA1, pol);
+                        if (F8) {
+                            // 128 x 64 FP8 bytes into the upper half of the A area (row r at 64 r);
+                            // the converter warps rewrite the whole area as swizzled f16
+                            tc::mbar_arrive_expect_tx(&full[stage], kABytes / 2 + nb * kBoxBBytes);
+                            tc::tma_load_2d_hint(sa + kABytes / 2, mA, &full[stage], kb * 64, w.rowA0, pol);
+                            tc::tma_load_2d_hint(sa + kABytes / 2 + kABytes / 4, mA, &full[stage], kb * 64,
+                                                 w.rowA1, pol);
+                        } else {
+                            tc::mbar_arrive_expect_tx(&full[stage], kABytes + nb * kBoxBBytes);
+                            tc::tma_load_2d_hint(sa, mA, &full[stage], kb * 64, w.rowA0, pol);
+                            tc::tma_load_2d_hint(sa + kABytes / 2, mA, &full[stage], kb * 64, w.rowA1, pol);
+                        }
                         for (int b = 0; b < nb; ++b)
                             tc::tma_load_2d(sa + kABytes + b * kBoxBBytes, mB, &full[stage], kb * 64,
                                             w.slot0 + 16 * b);
@@ -286,8 +388,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
+        // Lane 0 alone walks a unit's K blocks (no warp-wide step per block); the warp
+        // agrees on success once per unit.
         int stage = 0;
         uint32_t phase = 0;
+        int slot = 0;  // F8: the slot holding this K block's token rows
+        uint32_t ph8 = 0;
         bool ok = true;
         int it = 0;
         for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++it) {
@@ -295,23 +401,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int buf = it & 1;
             const uint32_t aph = (it >> 1) & 1;
             const int N = ((w.n + 15) >> 4) << 4;
-            const uint32_t idesc = tc::idesc_bf16(128, N);
+            const uint32_t idesc = F8 ? tc::idesc_f16(128, N) : tc::idesc_bf16(128, N);
             const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * NCH);
             int good = 1;
-            if (lane == 0) good = tc::mbar_wait(&tempty[buf], aph ^ 1u, abortv, tmo);
-            good = __shfl_sync(0xffffffffu, good, 0);
-            if (!good) {
-                ok = false;
-                if (lane == 0) record_timeout(p.err, 2, u, -1, buf, aph, n_units, w.n);
-                break;
-            }
-            tc::fence_after_sync();
-            for (int kb = 0; kb < w.kb; ++kb) {
-                good = 1;
-                if (lane == 0) {
-                    good = tc::mbar_wait(&full[stage], phase, abortv, tmo);
-                    if (good) {
-                        tc::fence_after_sync();
+            if (lane == 0) {
+                good = tc::mbar_wait(&tempty[buf], aph ^ 1u, abortv, tmo);
+                if (!good) record_timeout(p.err, 2, u, -1, buf, aph, n_units, w.n);
+                tc::fence_after_sync();
+                for (int kb = 0; kb < w.kb && good; ++kb) {
+                    // F8: the converted A operand (its converters saw the slot's token rows land)
+                    good = tc::mbar_wait(F8 ? &conv[stage] : &full[stage], phase, abortv, tmo);
+                    if (!good) {
+                        record_timeout(p.err, 3, u, kb, stage, phase, n_units, w.n);
+                        break;
+                    }
+                    tc::fence_after_sync();
+                    if (F8) {
+                        const uint32_t at = tmem_base + static_cast<uint32_t>(kF8AColumn + 32 * stage);
+                        const uint32_t sb = tc::smem_addr(f8ring + slot * SL + kF8Tile);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            tc::mma_f16_tmem_a(d_tmem, at + 8 * k, tc::sdesc_k_sw128(sb + 32 * k), idesc,
+                                               (kb | k) != 0);
+                        tc::mma_commit(&empty[stage]);
+                        tc::mma_commit(&empty8[slot]);
+                    } else {
                         const uint32_t sa = tc::smem_addr(smem + stage * SB);
                         const uint32_t sb = sa + kABytes;
 #pragma unroll
@@ -320,21 +434,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                                          idesc, (kb | k) != 0);
                         tc::mma_commit(&empty[stage]);
                     }
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                    if (F8 && ++slot == S8) {
+                        slot = 0;
+                        ph8 ^= 1u;
+                    }
                 }
-                good = __shfl_sync(0xffffffffu, good, 0);
-                if (!good) {
-                    ok = false;
-                    if (lane == 0) record_timeout(p.err, 3, u, kb, stage, phase, n_units, w.n);
-                    break;
-                }
-                if (++stage == STAGES) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
+                if (good) tc::mma_commit(&tfull[buf]);
             }
-            if (!ok) break;
-            if (lane == 0) tc::mma_commit(&tfull[buf]);
-            __syncwarp();
+            good = __shfl_sync(0xffffffffu, good, 0);
+            if (!good) ok = false;
         }
         if (lane == 0) {
             if (!ok) {
@@ -346,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::mbar_wait(fin, 0, zero_flag, kTeardownNs);
         }
         __syncwarp();
-    } else {
+    } else if (warp < 6) {
         // ------------------------------------------------------------ epilogue (warps 2..5)
         const int sp = warp & 3;  // TMEM sub-partition this warp may access: lanes 32*sp .. 32*sp+31
         int it = 0;
@@ -367,13 +479,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::fence_after_sync();
             const uint32_t tb = tmem_base + (static_cast<uint32_t>(32 * sp) << 16) + static_cast<uint32_t>(buf * NCH);
             const int L = 32 * sp + lane;  // accumulator row held by this thread
+            // F8: the scale of weight row L of this tile
+            // (times 2^8: the converted operand holds the E4M3 values times 2^-8)
+            const float rs = F8 ? 256.0f * __ldg(&p.sc[(w.dn ? 2 : 0) + (w.shared ? 1 : 0)][w.rowA0 + L]) : 1.0f;
             for (int c0 = 0; c0 < w.n; c0 += 32) {
                 float v[32];
                 tc::tmem_ld32(tb + c0, v);
                 const int cnt = min(32, w.n - c0);
-                if (MODE == kGateUp || (MODE == kExperts && !w.dn)) {
+                if (F8) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] *= rs;
+                }
+                if (MODE == kGateUp || (EXP && !w.dn)) {
                     // rows alternate gate / up of one intermediate index: partner lane holds the other half
-                    bf16* act = static_cast<bf16*>(p.out);
                     const int i = w.mt * 64 + (L >> 1);
                     const bool is_gate = (lane & 1) == 0;
 #pragma unroll
@@ -382,13 +500,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (j < cnt && (j & 1) == (lane & 1)) {
                             const float g = is_gate ? v[j] : o;
                             const float up = is_gate ? o : v[j];
-                            act[static_cast<size_t>(w.slot0 + c0 + j) * p.out_ld + i] =
-                                __float2bfloat16_rn(silu_f(g) * up);
+                            const size_t at = static_cast<size_t>(w.slot0 + c0 + j) * p.out_ld + i;
+                            if (F8)
+                                static_cast<__half*>(p.out)[at] = __float2half_rn(silu_f(g) * up);
+                            else
+                                static_cast<bf16*>(p.out)[at] = __float2bfloat16_rn(silu_f(g) * up);
                         }
                     }
-                } else if (MODE == kDown || MODE == kExperts) {
-                    float* y = static_cast<float*>(MODE == kExperts ? p.out2 : p.out);
-                    const int ld = MODE == kExperts ? p.out2_ld : p.out_ld;
+                } else if (MODE == kDown || EXP) {
+                    float* y = static_cast<float*>(EXP ? p.out2 : p.out);
+                    const int ld = EXP ? p.out2_ld : p.out_ld;
                     const int h = w.mt * 128 + L;
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
@@ -424,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            if (MODE == kExperts && !w.dn) {
+            if (EXP && !w.dn) {
                 // publish this warp's SwiGLU rows to the down units of the chunk (any CTA)
                 __threadfence();
                 __syncwarp();
@@ -433,6 +554,56 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::fence_before_sync();
             tc::mbar_arrive(&tempty[buf]);
         }
+    } else if (F8) {
+        // ------------------------------------------------------------ FP8 -> f16 converters (warps 6..9)
+        // Every K block: each converter warp takes the 32 weight rows of its TMEM lane
+        // quarter; thread i converts row 32q + i of the slot's FP8 tile (64 bytes) into 32
+        // f16x2 words (values times 2^-8, exactly) and stores them as TMEM lane 32q + i,
+        // columns kF8AColumn + 32 stage ..: A row i in lane i, elements 2c, 2c+1 in column c.
+        const int q = warp & 3;
+        const int row = 32 * q + lane;
+        const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(32 * q) << 16);
+        constexpr int S8d = S8 > 0 ? S8 : 1;
+        bool ok = true;
+        int seq = 0;
+        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+            const Unit w = decode_unit<MODE, NCH>(u, p, nrc, nsc);
+            for (int kb = 0; kb < w.kb; ++kb, ++seq) {
+                const int stage = seq % STAGES;
+                const uint32_t phase = (seq / STAGES) & 1u;
+                const int slot = seq % S8d;
+                const uint32_t ph8 = (seq / S8d) & 1u;
+                const bool got = __all_sync(0xffffffffu, tc::mbar_wait(&empty[stage], phase ^ 1u, abortv, tmo) &&
+                                                             tc::mbar_wait(&full8[slot], ph8, abortv, tmo));
+                if (!got) {
+                    ok = false;
+                    if (lane == 0) record_timeout(p.err, 8, u, kb, slot, ph8, n_units, w.n);
+                    break;
+                }
+                tc::fence_after_sync();
+                const uint4* src = reinterpret_cast<const uint4*>(f8ring + slot * SL + 64 * row);
+                uint32_t h[32];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint4 v = src[i];
+                    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        h[8 * i + 2 * j] = tc::e4m3x2_to_f16x2_div256(wv[j], 0);
+                        h[8 * i + 2 * j + 1] = tc::e4m3x2_to_f16x2_div256(wv[j], 2);
+                    }
+                }
+                tc::tmem_st32(lane_base + static_cast<uint32_t>(kF8AColumn + 32 * stage), h);
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&conv[stage]);
+            }
+        }
+        if (!ok && lane == 0) {
+            *abort_flag = 1;
+            record_error(p.err, kErrTimeoutProducer);
+        }
+        __syncwarp();
     }
 
     tc::fence_before_sync();
@@ -445,21 +616,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int MODE, int NCH>
 cudaError_t launch_one(const TensorMaps& maps, const GemmParams& p, int grid, cudaStream_t s) {
-    constexpr int bytes = smem_bytes(NCH);
+    constexpr int bytes = MODE == kExpertsF8 ? smem_bytes_f8(NCH) : smem_bytes(NCH);
     static int done[64] = {};
     cudaError_t e = ensure_smem(tc_gemm_kernel<MODE, NCH>, bytes, done);
     if (e != cudaSuccess) return e;
-    return launch_pdl(tc_gemm_kernel<MODE, NCH>, dim3(grid), dim3(kThreads), bytes, s, maps, p);
+    return launch_pdl(tc_gemm_kernel<MODE, NCH>, dim3(grid), dim3(MODE == kExpertsF8 ? kThreadsF8 : kThreads), bytes,
+                      s, maps, p);
 }
 
 template <int MODE>
 cudaError_t launch_mode(int nch, const TensorMaps& maps, const GemmParams& p, int grid, cudaStream_t s) {
-    switch (nch) {
-        case 32: return launch_one<MODE, 32>(maps, p, grid, s);
-        case 64: return launch_one<MODE, 64>(maps, p, grid, s);
-        case 128: return launch_one<MODE, 128>(maps, p, grid, s);
-        case 256: return launch_one<MODE, 256>(maps, p, grid, s);
-        default: return cudaErrorInvalidValue;
+    if constexpr (MODE == kExpertsF8) {  // token chunks of at most 64 (accumulators and A stages share the TMEM)
+        if (nch == 32) return launch_one<MODE, 32>(maps, p, grid, s);
+        if (nch == 64) return launch_one<MODE, 64>(maps, p, grid, s);
+        return cudaErrorInvalidValue;
+    } else {
+        switch (nch) {
+            case 32: return launch_one<MODE, 32>(maps, p, grid, s);
+            case 64: return launch_one<MODE, 64>(maps, p, grid, s);
+            case 128: return launch_one<MODE, 128>(maps, p, grid, s);
+            case 256: return launch_one<MODE, 256>(maps, p, grid, s);
+            default: return cudaErrorInvalidValue;
+        }
     }
 }
 
@@ -470,6 +648,7 @@ int tc_gemm_smem_bytes(int nch) { return smem_bytes(nch); }
 cudaError_t launch_tc_gemm(int mode, int nch, const TensorMaps& maps, const GemmParams& p, int grid, cudaStream_t s) {
     switch (mode) {
         case kExperts: return launch_mode<kExperts>(nch, maps, p, grid, s);
+        case kExpertsF8: return launch_mode<kExpertsF8>(nch, maps, p, grid, s);
         case kLmHead: return launch_mode<kLmHead>(nch, maps, p, grid, s);
         default: return cudaErrorInvalidValue;
     }

@@ -11,12 +11,15 @@
 namespace moestep {
 
 // ------------------------------------------------------------------ grouped tcgen05 GEMM
-enum GemmMode { kGateUp = 0, kDown = 1, kLmHead = 2, kExperts = 3 };
+enum GemmMode { kGateUp = 0, kDown = 1, kLmHead = 2, kExperts = 3, kExpertsF8 = 4 };
 
 // kExperts: one persistent launch runs every gate/up unit (a[0] routed / a[1]
 // shared weights, b[0] gathered activations), then every down unit (a[2] / a[3],
 // b[1] = SwiGLU output); a down unit of a chunk starts once all of that
 // chunk's gate/up units have signalled completion.  kLmHead uses a[0] and b[0].
+// kExpertsF8: as kExperts with FP8 E4M3 weight maps (a[0..3], 64x64-byte boxes,
+// no swizzle), f16 activations in b[0..1], per-row scales sc[0..3] (same order
+// as a[0..3]) applied to the accumulators, and the SwiGLU output stored as f16.
 struct TensorMaps {
     CUtensorMap a[4];
     CUtensorMap b[2];
@@ -53,6 +56,7 @@ struct GemmParams {
     int* done;
     int* err;
     unsigned long long timeout_ns;
+    const float* sc[4];    // kExpertsF8: row scales of the weights of a[0..3]
 };
 
 cudaError_t launch_tc_gemm(int mode, int nch, const TensorMaps& maps, const GemmParams& p, int grid, cudaStream_t s);

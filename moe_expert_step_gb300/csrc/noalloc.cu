@@ -64,7 +64,7 @@ extern "C" int moe_block_route_noalloc(const moestep_dims* dims, int T, const vo
     // the completion counters must start at zero; the logits are fully written before they are read
     if (cudaMemsetAsync(s->counters, 0, sizeof(int) * groups, st) != cudaSuccess) return MOESTEP_ECUDA;
     float* lg = logits ? logits : s->logits;
-    if (moestep::launch_route(dims->dtype, x, Wr, T, dims->H, dims->E, dims->k, lg, idx, mass, gate, s->counters,
+    if (moestep::launch_route(dims->dtype == MOESTEP_FP8 ? MOESTEP_BF16 : dims->dtype, x, Wr, T, dims->H, dims->E, dims->k, lg, idx, mass, gate, s->counters,
                               nullptr, st) != cudaSuccess)
         return MOESTEP_ECUDA;
     return MOESTEP_OK;

@@ -887,8 +887,22 @@ __global__ void __launch_bounds__(kPlanThreads, 1) route_plan_kernel(RoutePlanAr
     }
 }
 
-// One CTA per slot: xp[slot] = x[slot_tok[slot]]; CTA 0 also zeroes the
-// expert launch's chunk counters.
+// 8 bf16 -> 8 f16 (round to nearest even; exact unless below f16's normal range)
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
+    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+        const __half2 h = __floats2half2_rn(f.x, f.y);
+        w[i] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// One CTA per slot: xp[slot] = x[slot_tok[slot]] (TO_F16: bf16 rows stored as f16,
+// the activation type of the FP8 expert launch); CTA 0 also zeroes the expert
+// launch's chunk counters.
+template <bool TO_F16>
 __global__ void __launch_bounds__(256) gather_kernel(const uint4* __restrict__ x, int row_vec,
                                                      const int32_t* __restrict__ slot_tok, const int* __restrict__ plan,
                                                      uint4* __restrict__ xp, int* __restrict__ done, int n_done) {
@@ -899,8 +913,10 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint4* __restrict__ x
         for (int i = threadIdx.x; i < n_done; i += blockDim.x) done[i] = 0;
     if (slot < plan[2]) {
         const int t = slot_tok[slot];
-        for (int i = threadIdx.x; i < row_vec; i += blockDim.x)
-            xp[static_cast<size_t>(slot) * row_vec + i] = x[static_cast<size_t>(t) * row_vec + i];
+        for (int i = threadIdx.x; i < row_vec; i += blockDim.x) {
+            const uint4 v = x[static_cast<size_t>(t) * row_vec + i];
+            xp[static_cast<size_t>(slot) * row_vec + i] = TO_F16 ? bf16x8_to_f16x8(v) : v;
+        }
     }
 }
 
@@ -949,8 +965,11 @@ cudaError_t launch_coreset(const CoresetArgs& a, cudaStream_t s) {
 
 cudaError_t launch_gather(int dtype, const void* x, int H, const int32_t* slot_tok, const int* plan, int max_slots,
                           void* xp, int* done, int n_done, cudaStream_t s) {
-    const int row_vec = H * (dtype == MOESTEP_BF16 ? 2 : 4) / 16;
-    return launch_pdl(gather_kernel, dim3(max_slots), dim3(256), 0, s, static_cast<const uint4*>(x), row_vec,
+    const int row_vec = H * (dtype == MOESTEP_F32 ? 4 : 2) / 16;
+    if (dtype == MOESTEP_FP8)
+        return launch_pdl(gather_kernel<true>, dim3(max_slots), dim3(256), 0, s, static_cast<const uint4*>(x),
+                          row_vec, slot_tok, plan, static_cast<uint4*>(xp), done, n_done);
+    return launch_pdl(gather_kernel<false>, dim3(max_slots), dim3(256), 0, s, static_cast<const uint4*>(x), row_vec,
                       slot_tok, plan, static_cast<uint4*>(xp), done, n_done);
 }
 

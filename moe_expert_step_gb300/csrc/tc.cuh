@@ -128,6 +128,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
            | (static_cast<uint32_t>(M >> 4) << 24); // M / 16
 }
 
+// kind::f16 with f16 A and B (both operands must be the same type), f32 D
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
+    return (1u << 4)                                // D format: f32
+           | (static_cast<uint32_t>(N >> 3) << 17)  // N / 8 (A, B format 0: f16)
+           | (static_cast<uint32_t>(M >> 4) << 24); // M / 16
+}
+
 // Shared-memory matrix descriptor for a K-major operand stored in the 128-byte
 // swizzled layout that TMA's SWIZZLE_128B writes: rows of 128 bytes, groups of
 // 8 rows 1024 bytes apart.  `saddr` may be advanced by 32-byte steps inside a
@@ -152,6 +159,29 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// The same MMA with A read from tensor memory: A row i in TMEM lane i, its K
+// elements packed two per 32-bit column (K = 16 -> 8 columns from a_tmem).
+__device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                               uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Store 32 consecutive 32-bit columns into this warp's 32 TMEM lanes (thread i -> lane i)
+// and wait until the stores are done.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};\n\t"
+        "tcgen05.wait::st.sync.aligned;"
+        ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
 // Arrive once on `bar` when all tcgen05 operations issued so far by this thread complete.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -177,6 +207,34 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Named barrier over `nthreads` threads that also returns whether `pred` held in all of them.
+__device__ __forceinline__ bool named_bar_and(int id, int nthreads, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
+
+// Make this thread's generic-proxy shared-memory writes visible to the async
+// proxy (tcgen05.mma operand reads).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Two FP8 E4M3 bytes (bytes `lo` and `lo`+1 of w, low one first) -> two f16 holding
+// the values times 2^-8, exactly: a byte's seven magnitude bits shifted left by 7 are
+// the f16 pattern of value * 2^-8 (exponent 15 - 7 - 8 = bias difference minus 8; an
+// E4M3 subnormal m * 2^-9 lands on the f16 subnormal m * 2^-17), and adding the
+// shifted sign bit to itself moves it from bit 14 to bit 15.  Integer ops only.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2_div256(uint32_t w, int lo) {
+    const uint32_t x = __byte_perm(w, 0u, lo == 0 ? 0x4140u : 0x4342u);  // byte lo -> bits 0..7, lo+1 -> 16..23
+    const uint32_t y = x << 7;
+    return y + (y & 0x40004000u);
 }
 
 }  // namespace tc

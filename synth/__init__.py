@@ -107,6 +107,40 @@ def np_normal_bf16(key: int, start: int, n: int, std: float) -> np.ndarray:
     return f32_to_bf16_bits(np_normal_f32(key, start, n, std))
 
 
+def f32_to_e4m3(f: np.ndarray) -> np.ndarray:
+    """binary32 -> FP8 E4M3 codes (bias 7, 3 mantissa bits, max 448, subnormals m * 2^-9),
+    nearest-even, saturated to +-448 (the host and device copies' definition)."""
+    b = np.ascontiguousarray(f, dtype=np.float32).view(np.uint32)
+    sign = ((b >> np.uint32(31)) << np.uint32(7)).astype(np.uint32)
+    a = b & np.uint32(0x7FFFFFFF)
+    with np.errstate(over="ignore"):
+        r = (a + np.uint32(0x7FFFF) + ((a >> np.uint32(20)) & np.uint32(1))) >> np.uint32(20)
+        normal = np.minimum(r - np.uint32(120 << 3), np.uint32(0x7E))
+    sub = np.rint(a.view(np.float32) * np.float32(512.0)).astype(np.uint32)
+    code = np.where(a >= np.uint32(0x7F800000), np.uint32(0x7E),
+                    np.where(a >= np.uint32(0x3C800000), normal, sub))
+    return (code | sign).astype(np.uint8)
+
+
+def e4m3_to_f32(codes: np.ndarray) -> np.ndarray:
+    """Values of FP8 E4M3 codes (0x7F / 0xFF, the NaN codes, are never generated)."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int32)
+    e = (c >> 3) & 15
+    m = c & 7
+    mag = np.where(e == 0, m.astype(np.float64) * 2.0 ** -9, (8 + m).astype(np.float64) * np.exp2(e - 10.0))
+    return np.where(c & 0x80, -mag, mag).astype(np.float32)
+
+
+def np_e4m3(key: int, start: int, n: int, std: float) -> np.ndarray:
+    return f32_to_e4m3(np_normal_f32(key, start, n, std))
+
+
+def np_row_scales(key: int, start: int, n: int) -> np.ndarray:
+    """Per-row scales (16 + (u & 15)) * 2^-16, exact binary32."""
+    return ((16 + (np_u64(key, start, n) & np.uint64(15)).astype(np.int64)).astype(np.float32)
+            * np.float32(2.0 ** -16))
+
+
 def np_uniform01(key: int, start: int, n: int) -> np.ndarray:
     """Uniform doubles in [0, 1) from the top 53 bits of each output."""
     return (np_u64(key, start, n) >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
@@ -148,6 +182,9 @@ def host_lib():
         lib.synth_host_normal_f32.argtypes = [u64, u64, i64, f32, vp]
         lib.synth_host_normal_bf16.argtypes = [u64, u64, i64, f32, vp]
         lib.synth_host_bf16_to_f64.argtypes = [vp, i64, vp]
+        lib.synth_host_e4m3.argtypes = [u64, u64, i64, f32, vp]
+        lib.synth_host_row_scales.argtypes = [u64, u64, i64, vp]
+        lib.synth_host_f32_to_e4m3.argtypes = [vp, i64, vp]
         lib.synth_host_threads.restype = ctypes.c_int
         _host = lib
     return _host
@@ -163,14 +200,19 @@ def dev_lib():
                                               ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
         lib.synth_dev_fill_u64.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_int64, ctypes.c_void_p,
                                            ctypes.c_void_p]
+        lib.synth_dev_fill_row_scales.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_int64, ctypes.c_void_p,
+                                                  ctypes.c_void_p]
         _dev = lib
     return _dev
 
 
 def host_normal(key: int, start: int, n: int, std: float, dtype: str) -> np.ndarray:
-    """Host copy: float32 array (dtype 'f32') or uint16 bf16 bits (dtype 'bf16')."""
+    """Host copy: float32 array (dtype 'f32'), uint16 bf16 bits ('bf16') or uint8 FP8 E4M3 codes ('e4m3')."""
     lib = host_lib()
-    if dtype == "f32":
+    if dtype == "e4m3":
+        out = np.empty(n, np.uint8)
+        lib.synth_host_e4m3(key, start, n, float(scale_for_std(std)), out.ctypes.data)
+    elif dtype == "f32":
         out = np.empty(n, np.float32)
         lib.synth_host_normal_f32(key, start, n, float(scale_for_std(std)), out.ctypes.data)
     elif dtype == "bf16":
@@ -186,8 +228,23 @@ def host_normal_f64(key: int, start: int, n: int, std: float, dtype: str) -> np.
     a = host_normal(key, start, n, std, dtype)
     if dtype == "f32":
         return a.astype(np.float64)
+    if dtype == "e4m3":
+        return e4m3_to_f32(a).astype(np.float64)
     out = np.empty(n, np.float64)
     host_lib().synth_host_bf16_to_f64(a.ctypes.data, n, out.ctypes.data)
+    return out
+
+
+def host_f32_to_e4m3(f: np.ndarray) -> np.ndarray:
+    a = np.ascontiguousarray(f, dtype=np.float32)
+    out = np.empty(a.size, np.uint8)
+    host_lib().synth_host_f32_to_e4m3(a.ctypes.data, a.size, out.ctypes.data)
+    return out
+
+
+def host_row_scales(key: int, start: int, n: int) -> np.ndarray:
+    out = np.empty(n, np.float32)
+    host_lib().synth_host_row_scales(key, start, n, out.ctypes.data)
     return out
 
 
@@ -203,9 +260,15 @@ def host_threads() -> int:
 
 def dev_fill_normal(ptr: int, key: int, start: int, n: int, std: float, dtype: str, stream: int = 0) -> None:
     rc = dev_lib().synth_dev_fill_normal(key, start, n, float(scale_for_std(std)),
-                                         0 if dtype == "bf16" else 1, ptr, stream)
+                                         {"bf16": 0, "f32": 1, "e4m3": 2}[dtype], ptr, stream)
     if rc != 0:
         raise RuntimeError(f"synth_dev_fill_normal failed: cudaError {rc}")
+
+
+def dev_fill_row_scales(ptr: int, key: int, start: int, n: int, stream: int = 0) -> None:
+    rc = dev_lib().synth_dev_fill_row_scales(key, start, n, ptr, stream)
+    if rc != 0:
+        raise RuntimeError(f"synth_dev_fill_row_scales failed: cudaError {rc}")
 
 
 def dev_fill_u64(ptr: int, key: int, start: int, n: int, stream: int = 0) -> None:
@@ -221,5 +284,6 @@ def as_f64(bits_or_f32: np.ndarray, dtype: str) -> np.ndarray:
 __all__: Iterable[str] = [
     "tensor_key", "scale_for_std", "np_u64", "np_normal_f32", "np_normal_bf16", "np_uniform01",
     "f32_to_bf16_bits", "bf16_bits_to_f32", "build", "host_normal", "host_normal_f64", "host_u64",
-    "host_threads", "dev_fill_normal", "dev_fill_u64", "as_f64",
+    "host_threads", "dev_fill_normal", "dev_fill_u64", "as_f64", "f32_to_e4m3", "e4m3_to_f32", "np_e4m3",
+    "np_row_scales", "host_row_scales", "dev_fill_row_scales",
 ]

@@ -17,6 +17,7 @@
  * ONE IEEE-754 binary32 multiply with a caller-supplied scale.  bf16 output is
  * that float rounded to nearest-even on its upper 16 bits.
  */
+#include <math.h>
 #include <stdint.h>
 #include <string.h>
 
@@ -61,6 +62,48 @@ void synth_host_normal_bf16(uint64_t key, uint64_t start, int64_t n, float scale
 #pragma omp parallel for schedule(static)
     for (int64_t i = 0; i < n; ++i)
         out[i] = f32_to_bf16_rne(irwin_hall4(sm64_at(key, start + (uint64_t)i), scale));
+}
+
+/* float -> FP8 E4M3 (1 sign, 4 exponent bits with bias 7, 3 mantissa bits,
+ * largest finite value 448, subnormals m * 2^-9), rounded to nearest-even and
+ * saturated to +-448.  Normal range: round the binary32 pattern at its 20th
+ * bit (exact integer arithmetic) and rebias the exponent; below 2^-6 the value
+ * times 512 (exact) is rounded to an integer mantissa 0..8. */
+static inline uint8_t f32_to_e4m3_rne(float f) {
+    uint32_t b;
+    memcpy(&b, &f, 4);
+    const uint32_t sign = (b >> 31) << 7;
+    const uint32_t a = b & 0x7FFFFFFFu;
+    uint32_t code;
+    if (a >= 0x7F800000u) {
+        code = 0x7Eu;
+    } else if (a >= 0x3C800000u) { /* |f| >= 2^-6 */
+        const uint32_t r = (a + 0x7FFFFu + ((a >> 20) & 1u)) >> 20;
+        code = r - (120u << 3);
+        if (code > 0x7Eu) code = 0x7Eu;
+    } else {
+        float m;
+        memcpy(&m, &a, 4);
+        code = (uint32_t)rintf(m * 512.0f);
+    }
+    return (uint8_t)(code | sign);
+}
+
+/* FP8 E4M3 codes of normal values: round_e4m3(irwin_hall4 * scale). */
+void synth_host_e4m3(uint64_t key, uint64_t start, int64_t n, float scale, uint8_t* out) {
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) out[i] = f32_to_e4m3_rne(irwin_hall4(sm64_at(key, start + (uint64_t)i), scale));
+}
+
+/* The conversion alone, for checking it on chosen values. */
+void synth_host_f32_to_e4m3(const float* in, int64_t n, uint8_t* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = f32_to_e4m3_rne(in[i]);
+}
+
+/* Per-row scales (16 + (u & 15)) * 2^-16, exact in binary32. */
+void synth_host_row_scales(uint64_t key, uint64_t start, int64_t n, float* out) {
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) out[i] = (float)(16 + (int)(sm64_at(key, start + (uint64_t)i) & 15u)) * 0x1p-16f;
 }
 
 /* bf16 bit patterns -> float64, for handing weights to an fp64 consumer. */

@@ -15,6 +15,12 @@ Configurations (all seeds 0, tensors keyed by (seed, family, layer, name)):
                  top_p 0.9, residual h0 ~ N(0, 1).
 * lm_head        H=2048, V=152064, Wlm N(0, 0.02^2) bf16.
 * batched        R in {1, 4, 16} requests x 32 tokens through clover_stack40.
+* clover_layer_fp8, clover_stack40_fp8
+                 the same shapes with FP8 E4M3 expert weights (routed and shared):
+                 codes = e4m3(N(0, 64^2)), one fp32 scale per weight row
+                 (16 + u) * 2^-16 with u uniform on 0..15, so a dequantised weight
+                 has std ~0.023; router, LM head and activations as in the bf16
+                 configs.
 """
 from __future__ import annotations
 
@@ -22,7 +28,7 @@ from dataclasses import dataclass, replace
 
 import numpy as np
 
-from . import host_normal, host_normal_f64, np_uniform01, tensor_key
+from . import host_normal, host_normal_f64, host_row_scales, np_uniform01, tensor_key
 
 
 @dataclass(frozen=True)
@@ -48,13 +54,23 @@ class Config:
     def T(self) -> int:
         return self.R * self.P
 
+    @property
+    def act_dtype(self) -> str:
+        """Element type of the router, activations and LM head."""
+        return "f32" if self.dtype == "f32" else "bf16"
+
 
 TINY = Config("tiny_fp32", "tiny", 256, 16, 4, 128, 128, 1024, 8, "f32", 0.05, 0.05, 0.05, 1, (1.0, 0.9, 0.5))
 LAYER = Config("clover_layer", "clover", 2048, 256, 8, 512, 512, 152064, 32, "bf16", 0.02, 0.02, 0.02, 1,
                (1.0, 0.9, 0.7))
 STACK = replace(LAYER, name="clover_stack40", n_layers=40, top_ps=(0.9,))
 LMHEAD = LAYER
-CONFIGS = {c.name: c for c in (TINY, LAYER, STACK)}
+LAYER_FP8 = replace(LAYER, name="clover_layer_fp8", dtype="fp8")
+STACK_FP8 = replace(STACK, name="clover_stack40_fp8", dtype="fp8")
+CONFIGS = {c.name: c for c in (TINY, LAYER, STACK, LAYER_FP8, STACK_FP8)}
+FP8_CODE_STD = 64.0  # std of the E4M3 codes before the row scale
+EXPERT_TENSORS = ("Wgu", "Wd", "Wsgu", "Wsd")
+SCALE_OF = {"Wgu": "Sgu", "Wd": "Sd", "Wsgu": "Ssgu", "Wsd": "Ssd"}
 
 SEED = 0
 
@@ -66,20 +82,46 @@ def key(cfg: Config, *parts, seed: int = SEED) -> int:
 # ------------------------------------------------------------------------------------ shapes
 def layer_shapes(cfg: Config) -> dict:
     H, E, I, Is = cfg.H, cfg.E, cfg.I, cfg.Is
-    return {"Wr": (E, H), "Wgu": (E, I, 2, H), "Wd": (E, H, I), "Wsgu": (Is, 2, H), "Wsd": (H, Is)}
+    s = {"Wr": (E, H), "Wgu": (E, I, 2, H), "Wd": (E, H, I), "Wsgu": (Is, 2, H), "Wsd": (H, Is)}
+    if cfg.dtype == "fp8":
+        s.update({"Sgu": (E, 2 * I), "Sd": (E, H), "Ssgu": (2 * Is,), "Ssd": (H,)})
+    return s
 
 
 def layer_std(cfg: Config, name: str) -> float:
+    if cfg.dtype == "fp8" and name in EXPERT_TENSORS:
+        return FP8_CODE_STD
     return cfg.wr_std if name == "Wr" else cfg.w_std
+
+
+def tensor_dtype(cfg: Config, name: str) -> str:
+    """Storage of one layer tensor: 'bf16' / 'f32', 'e4m3' codes, or 'scale' (fp32 row scales)."""
+    if cfg.dtype != "fp8":
+        return cfg.dtype
+    if name in EXPERT_TENSORS:
+        return "e4m3"
+    return "scale" if name.startswith("S") else "bf16"
 
 
 # ------------------------------------------------------------------------------------ host copies
 def host_tensor(cfg: Config, layer: int, name: str, start: int = 0, n: int | None = None) -> np.ndarray:
-    """float64 values of (a slice of) one layer tensor, flattened."""
+    """float64 values of (a slice of) one layer tensor, flattened; FP8 expert tensors are
+    dequantised (code value times its row's scale)."""
     shape = layer_shapes(cfg)[name]
     total = int(np.prod(shape))
     n = total - start if n is None else n
-    return host_normal_f64(key(cfg, layer, name), start, n, layer_std(cfg, name), cfg.dtype)
+    dt = tensor_dtype(cfg, name)
+    if n == 0:
+        return np.zeros(0, np.float64)
+    if dt == "scale":
+        return host_row_scales(key(cfg, layer, name), start, n).astype(np.float64)
+    v = host_normal_f64(key(cfg, layer, name), start, n, layer_std(cfg, name), dt)
+    if dt == "e4m3":
+        row = shape[-1]                      # elements per weight row
+        assert start % row == 0 and n % row == 0
+        sc = host_tensor(cfg, layer, SCALE_OF[name], start // row, n // row)
+        v = (v.reshape(-1, row) * sc[:, None]).reshape(-1)
+    return v
 
 
 class HostLayer:
@@ -104,13 +146,13 @@ class HostLayer:
 def host_lm_head(cfg: Config, rows: slice | None = None) -> np.ndarray:
     """float64 LM-head weights [V][H] (or a row range)."""
     r0, r1 = (0, cfg.V) if rows is None else (rows.start, rows.stop)
-    v = host_normal_f64(key(cfg, "Wlm"), r0 * cfg.H, (r1 - r0) * cfg.H, cfg.lm_std, cfg.dtype)
+    v = host_normal_f64(key(cfg, "Wlm"), r0 * cfg.H, (r1 - r0) * cfg.H, cfg.lm_std, cfg.act_dtype)
     return v.reshape(r1 - r0, cfg.H)
 
 
 def host_activations(cfg: Config, name: str, rows: int, std: float = 1.0, dtype: str | None = None) -> np.ndarray:
     """[rows][H] activations (bf16 bits / float32 in the given dtype) as stored on the device."""
-    dt = dtype or cfg.dtype
+    dt = dtype or cfg.act_dtype
     return host_normal(key(cfg, name), 0, rows * cfg.H, std, dt).reshape(rows, cfg.H)
 
 
@@ -141,13 +183,17 @@ def device_layer(cfg: Config, layer: int, device="cuda"):
     """Fill one layer's weights directly in device memory (bit-identical to the host copies)."""
     import torch
 
-    from . import dev_fill_normal
-    tdt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
+    from . import dev_fill_normal, dev_fill_row_scales
+    tdt = {"bf16": torch.bfloat16, "f32": torch.float32, "e4m3": torch.uint8, "scale": torch.float32}
     out = {}
     stream = torch.cuda.current_stream(device).cuda_stream
     for name, shape in layer_shapes(cfg).items():
-        t = torch.empty(shape, dtype=tdt, device=device)
-        dev_fill_normal(t.data_ptr(), key(cfg, layer, name), 0, t.numel(), layer_std(cfg, name), cfg.dtype, stream)
+        dt = tensor_dtype(cfg, name)
+        t = torch.empty(shape, dtype=tdt[dt], device=device)
+        if dt == "scale":
+            dev_fill_row_scales(t.data_ptr(), key(cfg, layer, name), 0, t.numel(), stream)
+        else:
+            dev_fill_normal(t.data_ptr(), key(cfg, layer, name), 0, t.numel(), layer_std(cfg, name), dt, stream)
         out[name] = t
     return out
 
@@ -156,9 +202,9 @@ def device_lm_head(cfg: Config, device="cuda"):
     import torch
 
     from . import dev_fill_normal
-    tdt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
+    tdt = torch.bfloat16 if cfg.act_dtype == "bf16" else torch.float32
     t = torch.empty((cfg.V, cfg.H), dtype=tdt, device=device)
-    dev_fill_normal(t.data_ptr(), key(cfg, "Wlm"), 0, t.numel(), cfg.lm_std, cfg.dtype,
+    dev_fill_normal(t.data_ptr(), key(cfg, "Wlm"), 0, t.numel(), cfg.lm_std, cfg.act_dtype,
                     torch.cuda.current_stream(device).cuda_stream)
     return t
 
