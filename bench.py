@@ -44,6 +44,10 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-loop", action="store_true", help="skip the whole-block round-loop measurement")
+    ap.add_argument("--correlation", type=float, default=0.0,
+                    help="workload variant: tokens of a block share a hidden component (0 = independent)")
+    ap.add_argument("--block", type=int, default=None, help="workload variant: block size P (default 32)")
+    ap.add_argument("--threshold", type=float, default=THRESHOLD, help="LowConfidence threshold")
     ap.add_argument("--loop-scale", type=float, default=16.0,
                     help="logit scale of the round-loop measurement (1 = every round is a fallback)")
     ap.add_argument("--prof-all", action="store_true", help="time every kernel in the roofline pass")
@@ -140,15 +144,18 @@ def workload(name: str):
     return W.CONFIGS[name]
 
 
-def workload_desc(cfg, R: int) -> dict:
+def workload_desc(cfg, R: int, args=None) -> dict:
+    thr = args.threshold if args is not None else THRESHOLD
+    corr = args.correlation if args is not None else 0.0
     return {"workload": f"{cfg.name}: {cfg.n_layers}-layer MoE FFN stack (H={cfg.H}, {cfg.E} routed experts top-{cfg.k}, "
                         f"expert/shared SwiGLU I={cfg.I}, 1 shared expert, "
                         f"{'FP8 E4M3 expert weights with per-row fp32 scales, bf16 router and LM head' if cfg.dtype == 'fp8' else 'bf16 weights'}"
                         f", fp32 accumulate), "
                         f"block of {cfg.P} tokens x {R} request(s), coreset top_p {TOP_P}, RMSNorm eps 1e-6 "
-                        f"between layers, LM head V={cfg.V}, LowConfidence commit threshold {THRESHOLD}",
+                        f"between layers, LM head V={cfg.V}, LowConfidence commit threshold {thr}"
+                        + (f", block tokens correlated (a={corr})" if corr > 0 else ""),
             "layers": cfg.n_layers, "block_tokens": cfg.P, "requests": R, "top_p": TOP_P,
-            "threshold": THRESHOLD, "vocab": cfg.V,
+            "threshold": thr, "vocab": cfg.V, "token_correlation": corr,
             "l2": "inputs larger than L2: every step streams the selected experts' weights (tens of GB) from HBM",
             "parallelism": "replicas (one independent block step per GPU)",
             "launch": "one block_decode_step call per step, replayed as a CUDA graph (programmatic dependent launch "
@@ -179,7 +186,11 @@ def run_gpu(args, dist: Dist):
 
     torch.cuda.set_device(dist.local)
     cfg = workload(args.config)
+    if args.block:
+        from dataclasses import replace
+        cfg = replace(cfg, P=args.block)
     R = args.requests
+    THR = args.threshold
     T = R * cfg.P
     d = ms.ModelDims(H=cfg.H, E=cfg.E, k=cfg.k, I=cfg.I, Is=cfg.Is, V=cfg.V, P=cfg.P,
                      dtype=ms.FP8 if cfg.dtype == "fp8" else ms.BF16)
@@ -189,7 +200,7 @@ def run_gpu(args, dist: Dist):
                        l.get("Ssd")) for l in layers_t]
     Wlm = W.device_lm_head(cfg)
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
-    h0_host = W.host_h0(cfg, R)
+    h0_host = W.host_h0(cfg, R, correlation=args.correlation)
     masked_host = W.masked_subset(cfg, R).astype(np.uint8)
     h0 = dev(h0_host)
     tokens0 = torch.zeros(T, dtype=torch.int32, device="cuda")
@@ -209,7 +220,7 @@ def run_gpu(args, dist: Dist):
         tokens.copy_(tokens0)
         masked.copy_(masked0)
         kw = trace or {}
-        ms.block_decode_step(d, R, layers, Wlm, top_p, THRESHOLD, h_in, tokens, masked, choice, conf, accept, n_comm,
+        ms.block_decode_step(d, R, layers, Wlm, top_p, THR, h_in, tokens, masked, choice, conf, accept, n_comm,
                              ws, **kw)
 
     # one traced step: per-layer coreset sizes and the union of kept experts
@@ -296,7 +307,7 @@ def run_gpu(args, dist: Dist):
             tokens.copy_(t_pin, non_blocking=True)
             masked.copy_(m_pin, non_blocking=True)
             top_p.copy_(tp_pin, non_blocking=True)
-            ms.block_decode_step(d, R, layers, Wlm, top_p, THRESHOLD, h_dev, tokens, masked, choice, conf, accept,
+            ms.block_decode_step(d, R, layers, Wlm, top_p, THR, h_dev, tokens, masked, choice, conf, accept,
                                  n_comm, ws)
             out_tok.copy_(tokens, non_blocking=True)
             out_msk.copy_(masked, non_blocking=True)
@@ -320,7 +331,7 @@ def run_gpu(args, dist: Dist):
     # ---------------- the whole block: device-resident round loop vs rounds driven from the host
     round_loop = None
     if not args.no_loop:
-        round_loop = measure_round_loop(ms, W, cfg, d, R, layers, Wlm, top_p, ws, args.loop_scale, dist)
+        round_loop = measure_round_loop(ms, W, cfg, d, R, layers, Wlm, top_p, ws, args.loop_scale, dist, THR)
     if ms.read_device_error(ws) != ms.OK:
         raise RuntimeError("device error word set during the benchmark")
 
@@ -355,7 +366,7 @@ def run_gpu(args, dist: Dist):
         "warmup": max(3, args.warmup), "ms_per_step": round(ms_step, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 experts, bf16 rest" if cfg.dtype == "fp8" else "bf16",
         "data": "synthetic",
-        "config": {**workload_desc(cfg, R), "route_fusion": R == 1 and args.route_fusion},
+        "config": {**workload_desc(cfg, R, args), "route_fusion": R == 1 and args.route_fusion},
         "expert_weight_hbm": {
             "bytes_per_step": step_bytes, "expert_bytes_per_step": eb["expert_weights"],
             "experts_kept_per_layer": {"mean": round(statistics.mean(unions), 2), "min": min(unions),
@@ -381,7 +392,7 @@ def run_gpu(args, dist: Dist):
     return line, cfg
 
 
-def measure_round_loop(ms, W, cfg, d, R, layers, Wlm, top_p, ws, scale, dist, blocks=3):
+def measure_round_loop(ms, W, cfg, d, R, layers, Wlm, top_p, ws, scale, dist, thr, blocks=3):
     """Decode whole blocks (every position masked at the start) with block_decode_loop, the
     rounds as one CUDA-graph while loop, and with the same rounds driven from the host
     (block_embed + block_decode_step, reading `masked` back after each round)."""
@@ -403,7 +414,7 @@ def measure_round_loop(ms, W, cfg, d, R, layers, Wlm, top_p, ws, scale, dist, bl
     def device_block():
         tokens.zero_()
         masked.fill_(1)
-        ms.block_decode_loop(d, R, layers, Wlm, emb, pos, cfg.V - 1, top_p, THRESHOLD, tokens, masked, rounds, ws,
+        ms.block_decode_loop(d, R, layers, Wlm, emb, pos, cfg.V - 1, top_p, thr, tokens, masked, rounds, ws,
                              logit_scale=scale)
 
     def host_block():
@@ -412,7 +423,7 @@ def measure_round_loop(ms, W, cfg, d, R, layers, Wlm, top_p, ws, scale, dist, bl
         n = 0
         while bool(masked.any().item()) and n < cfg.P:
             ms.block_embed(d, R, tokens, masked, emb, pos, cfg.V - 1, h)
-            ms.block_decode_step(d, R, layers, Wlm, top_p, THRESHOLD, h, tokens, masked, choice, conf, accept,
+            ms.block_decode_step(d, R, layers, Wlm, top_p, thr, h, tokens, masked, choice, conf, accept,
                                  ncomm, ws, logit_scale=scale)
             n += 1
         return n
@@ -440,7 +451,7 @@ def measure_round_loop(ms, W, cfg, d, R, layers, Wlm, top_p, ws, scale, dist, bl
     ms_host = dist.max(time.perf_counter() - t0) * 1e3 / blocks
     del emb, pos
     return {"what": "whole blocks: all positions masked, rounds until none is (LowConfidence, threshold "
-                    f"{THRESHOLD}), R={R}; synthetic N(0,1) bf16 embedding and positional tables",
+                    f"{thr}), R={R}; synthetic N(0,1) bf16 embedding and positional tables",
             "logit_scale": scale, "rounds_per_block": n_rounds, "positions_per_round": round(T / n_rounds / R, 3),
             "ms_per_block_device_loop": round(ms_dev, 3), "ms_per_block_host_loop": round(ms_host, 3),
             "committed_tokens_per_s_device_loop": round(dist.world * T / (ms_dev / 1e3), 1),

@@ -156,9 +156,17 @@ def host_activations(cfg: Config, name: str, rows: int, std: float = 1.0, dtype:
     return host_normal(key(cfg, name), 0, rows * cfg.H, std, dt).reshape(rows, cfg.H)
 
 
-def host_h0(cfg: Config, R: int, tag: str = "h0") -> np.ndarray:
-    """fp32 residual-stream input of a block step, [R*P][H] ~ N(0, 1)."""
-    return host_normal(key(cfg, tag, R), 0, R * cfg.P * cfg.H, 1.0, "f32").reshape(R * cfg.P, cfg.H)
+def host_h0(cfg: Config, R: int, tag: str = "h0", correlation: float = 0.0) -> np.ndarray:
+    """fp32 residual-stream input of a block step, [R*P][H] ~ N(0, 1).  With correlation a > 0
+    every token of request r is a*c_r + sqrt(1 - a^2)*n_t (c_r, n_t independent N(0, 1) rows),
+    so the tokens of a block route alike (fewer distinct experts per block)."""
+    n = host_normal(key(cfg, tag, R), 0, R * cfg.P * cfg.H, 1.0, "f32").reshape(R, cfg.P, cfg.H)
+    if correlation <= 0.0:
+        return n.reshape(R * cfg.P, cfg.H)
+    c = host_normal(key(cfg, tag + "_common", R), 0, R * cfg.H, 1.0, "f32").reshape(R, 1, cfg.H)
+    a = float(correlation)
+    h = a * c.astype(np.float64) + np.sqrt(1.0 - a * a) * n.astype(np.float64)
+    return h.astype(np.float32).reshape(R * cfg.P, cfg.H)
 
 
 def tiny_tables(cfg: Config):

@@ -105,11 +105,14 @@ def fusion(request):
     ms.set_route_fusion(False)
 
 
-def test_clover_layer_step(fusion):
+@pytest.mark.parametrize("corr", [0.0, 0.9])
+def test_clover_layer_step(fusion, corr):
+    """corr = 0.9: the block's tokens share a hidden component, so they route alike (fewer
+    experts, up to 32 tokens per expert chunk)."""
     cfg = W.LAYER
     lay = W.device_layer(cfg, 0)
     Wlm_d = W.device_lm_head(cfg)
-    h0 = W.host_h0(cfg, 1)
+    h0 = W.host_h0(cfg, 1, correlation=corr)
     masked0 = W.masked_subset(cfg, 1)
     tokens = t(np.zeros(cfg.P, np.int32))
     masked = t(masked0.astype(np.uint8))

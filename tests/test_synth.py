@@ -88,3 +88,16 @@ def test_e4m3_codes_and_row_scales_numpy_equals_c():
         np.testing.assert_array_equal(synth.np_row_scales(key, start, n), synth.host_row_scales(key, start, n))
     s = synth.np_row_scales(key, 0, 10000)
     assert set(np.unique(s * 2.0 ** 16).astype(int)) <= set(range(16, 32))
+
+
+def test_correlated_block_inputs():
+    """host_h0 with correlation a: unit variance per element and correlation ~a^2 between two
+    tokens of one request, ~0 across requests."""
+    from synth import workloads as W
+    cfg = W.LAYER
+    h = W.host_h0(cfg, 2, correlation=0.9).astype(np.float64).reshape(2, cfg.P, cfg.H)
+    assert abs(h.std() - 1.0) < 0.02
+    same = np.corrcoef(h[0, 0], h[0, 5])[0, 1]
+    other = np.corrcoef(h[0, 0], h[1, 0])[0, 1]
+    assert abs(same - 0.81) < 0.05 and abs(other) < 0.08
+    np.testing.assert_array_equal(W.host_h0(cfg, 2), W.host_h0(cfg, 2, correlation=0.0))
