@@ -65,7 +65,8 @@ extern "C" {
 #define MOESTEP_FP8 2
 
 /* Model dimensions.  Supported: 1 <= k <= min(E, 32), E <= 1024, P <= 1024.
- * bf16 and fp8 paths additionally: H % 128 == 0, I % 64 == 0, Is % 64 == 0.
+ * bf16 and fp8 paths additionally: H % 128 == 0, I % 64 == 0, Is % 64 == 0;
+ * fp8 (calls that take expert weights): I % 128 == 0, Is % 128 == 0.
  * Is == 0 means no shared expert. */
 typedef struct {
     int H;     /* hidden size */

@@ -190,15 +190,16 @@ int get_encode() {
 
 // 2D bf16 tensor [rows][cols] (cols contiguous), boxes of 64 columns x box_rows
 // rows in the 128-byte swizzled shared-memory layout; out-of-range rows read as 0.
-// FP8 E4M3 weights: 64-byte rows of 64 elements, unswizzled (the expert launch's
+// FP8 E4M3 weights: boxes of 64 rows x 128 bytes (a K block of 128) in the 128-byte
+// swizzled layout, so the converter threads' row reads hit distinct banks (the expert launch's
 // converter warps write the swizzled f16 operand themselves)
 int make_map_fp8(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows) {
     cuuint64_t dims[2] = {cols, rows};
     cuuint64_t strides[1] = {cols};
-    cuuint32_t box[2] = {64, 64};
+    cuuint32_t box[2] = {128, 64};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
         g_last_cuda = static_cast<int>(r);
@@ -401,16 +402,17 @@ int run_experts(const Ctx& c, int R, const void* x, const moestep_layer* layer, 
     // gate/up: 128-row tiles of interleaved gate/up rows = 64 intermediate indices
     g.routed_tiles = 2 * d->I / 128;
     g.shared_tiles = 2 * d->Is / 128;
-    g.routed_kb = d->H / 64;
-    g.shared_kb = d->H / 64;
+    const int kbw = f8 ? 128 : 64;  // K per block: FP8 tiles are 128 bytes wide
+    g.routed_kb = d->H / kbw;
+    g.shared_kb = d->H / kbw;
     g.rows_per_expert = 2 * d->I;
     g.out = at<void>(c.ws, L.act);
     g.out_ld = L.act_ld;
     // down: 128-row tiles of the hidden dimension
     g.dn_routed_tiles = d->H / 128;
     g.dn_shared_tiles = d->H / 128;
-    g.dn_routed_kb = d->I / 64;
-    g.dn_shared_kb = d->Is / 64;
+    g.dn_routed_kb = d->I / kbw;
+    g.dn_shared_kb = d->Is / kbw;
     g.dn_rows_per_expert = d->H;
     g.out2 = at<void>(c.ws, L.y);
     g.out2_ld = d->H;
@@ -475,7 +477,7 @@ int layer_ok(const moestep_dims* d, const moestep_layer* l) {
     if (d->Is > 0 && (!aligned16(l->Wsgu) || !aligned16(l->Wsd))) return MOESTEP_EALIGN;
     if (d->dtype == MOESTEP_FP8) {
         if (!l->Sgu || !l->Sd || (d->Is > 0 && (!l->Ssgu || !l->Ssd))) return MOESTEP_EINVAL;
-        if (d->H % 16 || d->I % 16 || d->Is % 16) return MOESTEP_EALIGN;  // FP8 row strides
+        if (d->H % 128 || d->I % 128 || d->Is % 128) return MOESTEP_EUNSUPPORTED;  // K blocks of 128
     }
     return MOESTEP_OK;
 }

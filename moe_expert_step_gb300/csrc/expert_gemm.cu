@@ -40,7 +40,8 @@ namespace moestep {
 namespace {
 
 constexpr int kThreads = 192;
-constexpr int kThreadsF8 = 320;  // + four warps converting FP8 weight tiles to f16
+constexpr int kThreadsF8 = 480;  // + eight converter warps (two groups of four) and a second MMA warp
+constexpr int kMmaWarp2 = 14;    // FP8: issues the second 64-wide half of each K block into its own accumulator
 constexpr uint64_t kTeardownNs = 1000000000ull;  // fixed limit for draining in-flight copies/MMAs
 constexpr int kABytes = 16384;            // 128 rows x 64 bf16
 constexpr int kBoxBBytes = 16 * 128;      // 16 rows x 64 bf16
@@ -53,14 +54,15 @@ __host__ __device__ constexpr int num_stages(int nch) {
 __host__ __device__ constexpr int smem_bytes(int nch) { return num_stages(nch) * stage_bytes(nch) + 512 + 1024; }
 
 // FP8 weights: shared memory is one long ring of slots that the TMA warp fills far
-// ahead, each with one 128 x 64 E4M3 weight tile and its token rows (the MMA's B
-// operand, read in place).  The converted f16 A operands live in tensor memory
-// (kF8AStages stages of 32 columns from column kF8AColumn), so the conversion adds
-// no shared-memory traffic beyond reading the FP8 tile once.
-constexpr int kF8Tile = 8192;     // 128 rows x 64 E4M3 bytes
-constexpr int kF8AStages = 8;     // f16 A operands in TMEM
+// ahead, each with one 128 x 128 E4M3 weight tile (a K block of 128) and its token
+// rows as two 64-wide B boxes (the MMA's B operand, read in place).  The converted f16
+// A operands live in tensor memory (kF8AStages stages of 64 columns from column
+// kF8AColumn), so the conversion adds no shared-memory traffic beyond reading the FP8
+// tile once; eight MMAs per K block share one wait and two commits.
+constexpr int kF8Tile = 16384;    // 128 rows x 128 E4M3 bytes
+constexpr int kF8AStages = 4;     // f16 A operands in TMEM
 constexpr int kF8AColumn = 256;   // their first TMEM column (accumulators use 0 .. 2 NCH - 1 <= 128)
-__host__ __device__ constexpr int f8_slot_bytes(int nch) { return kF8Tile + nch * 128; }
+__host__ __device__ constexpr int f8_slot_bytes(int nch) { return kF8Tile + 2 * nch * 128; }
 __host__ __device__ constexpr int f8_slots(int nch) {
     return (kSmemBudget - 1024) / f8_slot_bytes(nch) > 24 ? 24 : (kSmemBudget - 1024) / f8_slot_bytes(nch);
 }
@@ -201,18 +203,18 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             tc::mbar_init(&full[s], 1);
-            tc::mbar_init(&empty[s], 1);
+            tc::mbar_init(&empty[s], F8 ? 2 : 1);  // F8: both MMA warps release a stage
         }
         for (int b = 0; b < 2; ++b) {
-            tc::mbar_init(&tfull[b], 1);
+            tc::mbar_init(&tfull[b], F8 ? 2 : 1);  // F8: both MMA warps commit
             tc::mbar_init(&tempty[b], 128);
         }
-        tc::mbar_init(fin, 1);
+        tc::mbar_init(fin, F8 ? 2 : 1);
         if (F8) {
-            for (int s = 0; s < STAGES; ++s) tc::mbar_init(&conv[s], 4);  // one arrival per converter warp
+            for (int s = 0; s < STAGES; ++s) tc::mbar_init(&conv[s], 4);  // one arrival per warp of a group
             for (int s = 0; s < S8; ++s) {
                 tc::mbar_init(&full8[s], 1);
-                tc::mbar_init(&empty8[s], 1);
+                tc::mbar_init(&empty8[s], 2);  // both MMA warps release a slot
             }
         }
         *abort_flag = 0;
@@ -284,12 +286,15 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
                     good = tc::mbar_wait(&empty8[slot], ph8 ^ 1u, abortv, tmo);
                     if (good) {
                         uint8_t* dst = f8ring + slot * SL;
-                        tc::mbar_arrive_expect_tx(&full8[slot], kF8Tile + nb * kBoxBBytes);
-                        tc::tma_load_2d_hint(dst, mA, &full8[slot], kb * 64, w.rowA0, pol);
-                        tc::tma_load_2d_hint(dst + kF8Tile / 2, mA, &full8[slot], kb * 64, w.rowA1, pol);
-                        for (int b = 0; b < nb; ++b)
-                            tc::tma_load_2d(dst + kF8Tile + b * kBoxBBytes, mB, &full8[slot], kb * 64,
+                        tc::mbar_arrive_expect_tx(&full8[slot], kF8Tile + 2 * nb * kBoxBBytes);
+                        tc::tma_load_2d_hint(dst, mA, &full8[slot], kb * 128, w.rowA0, pol);
+                        tc::tma_load_2d_hint(dst + kF8Tile / 2, mA, &full8[slot], kb * 128, w.rowA1, pol);
+                        for (int b = 0; b < nb; ++b) {
+                            tc::tma_load_2d(dst + kF8Tile + b * kBoxBBytes, mB, &full8[slot], kb * 128,
                                             w.slot0 + 16 * b);
+                            tc::tma_load_2d(dst + kF8Tile + NCH * 128 + b * kBoxBBytes, mB, &full8[slot],
+                                            kb * 128 + 64, w.slot0 + 16 * b);
+                        }
                         issued |= 1u << slot;
                         issued_parity = (issued_parity & ~(1u << slot)) | (ph8 << slot);
                     }
@@ -386,10 +391,13 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
                 if (issued & (1u << s)) tc::mbar_wait(&full[s], (issued_parity >> s) & 1u, zero_flag, kTeardownNs);
         }
         __syncwarp();
-    } else if (warp == 1) {
+    } else if (warp == 1 || (F8 && warp == kMmaWarp2)) {
         // ------------------------------------------------------------ MMA issuer
         // Lane 0 alone walks a unit's K blocks (no warp-wide step per block); the warp
-        // agrees on success once per unit.
+        // agrees on success once per unit.  F8: two MMA warps, warp 1 issuing the first
+        // 64-wide half of every K block into accumulator 0 and warp kMmaWarp2 the second
+        // half into accumulator 1 (TMEM columns 2 NCH ..); the epilogue adds the two.
+        const int mh = (F8 && warp == kMmaWarp2) ? 1 : 0;
         int stage = 0;
         uint32_t phase = 0;
         int slot = 0;  // F8: the slot holding this K block's token rows
@@ -402,7 +410,7 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
             const uint32_t aph = (it >> 1) & 1;
             const int N = ((w.n + 15) >> 4) << 4;
             const uint32_t idesc = F8 ? tc::idesc_f16(128, N) : tc::idesc_bf16(128, N);
-            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * NCH);
+            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(mh * 2 * NCH + buf * NCH);
             int good = 1;
             if (lane == 0) {
                 good = tc::mbar_wait(&tempty[buf], aph ^ 1u, abortv, tmo);
@@ -417,12 +425,12 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
                     }
                     tc::fence_after_sync();
                     if (F8) {
-                        const uint32_t at = tmem_base + static_cast<uint32_t>(kF8AColumn + 32 * stage);
-                        const uint32_t sb = tc::smem_addr(f8ring + slot * SL + kF8Tile);
+                        const uint32_t at = tmem_base + static_cast<uint32_t>(kF8AColumn + 64 * stage);
+                        const uint32_t sb = tc::smem_addr(f8ring + slot * SL + kF8Tile + mh * NCH * 128);
+                        uint64_t bd[4];  // this warp's 64-wide half of the K block, four K = 16 steps
 #pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            tc::mma_f16_tmem_a(d_tmem, at + 8 * k, tc::sdesc_k_sw128(sb + 32 * k), idesc,
-                                               (kb | k) != 0);
+                        for (int k = 0; k < 4; ++k) bd[k] = tc::sdesc_k_sw128(sb + 32 * k);
+                        tc::mma4_f16_tmem_a(d_tmem, at + 32 * mh, bd, idesc, kb != 0);
                         tc::mma_commit(&empty[stage]);
                         tc::mma_commit(&empty8[slot]);
                     } else {
@@ -487,8 +495,10 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
                 tc::tmem_ld32(tb + c0, v);
                 const int cnt = min(32, w.n - c0);
                 if (F8) {
+                    float v2[32];
+                    tc::tmem_ld32(tb + 2 * NCH + c0, v2);  // the second MMA warp's half of K
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] *= rs;
+                    for (int j = 0; j < 32; ++j) v[j] = (v[j] + v2[j]) * rs;
                 }
                 if (MODE == kGateUp || (EXP && !w.dn)) {
                     // rows alternate gate / up of one intermediate index: partner lane holds the other half
@@ -554,13 +564,16 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
             tc::fence_before_sync();
             tc::mbar_arrive(&tempty[buf]);
         }
-    } else if (F8) {
-        // ------------------------------------------------------------ FP8 -> f16 converters (warps 6..9)
-        // Every K block: each converter warp takes the 32 weight rows of its TMEM lane
-        // quarter; thread i converts row 32q + i of the slot's FP8 tile (64 bytes) into 32
-        // f16x2 words (values times 2^-8, exactly) and stores them as TMEM lane 32q + i,
-        // columns kF8AColumn + 32 stage ..: A row i in lane i, elements 2c, 2c+1 in column c.
+    } else if (F8 && warp < kMmaWarp2) {
+        // ------------------------------------------------------------ FP8 -> f16 converters (warps 6..13)
+        // Two groups of four warps take alternate K blocks.  Within a group each warp takes
+        // the 32 weight rows of its TMEM lane quarter; thread i converts row 32q + i of the
+        // slot's FP8 tile (128 bytes, 16-byte chunk j of row r at chunk j ^ (r & 7): the
+        // TMA's 128-byte swizzle, so a warp's reads hit distinct banks) into 64 f16x2 words
+        // (values times 2^-8, exactly) and stores them as TMEM lane 32q + i, columns
+        // kF8AColumn + 64 stage ..: A row i in lane i, elements 2c, 2c+1 in column c.
         const int q = warp & 3;
+        const int grp = (warp - 6) >> 2;
         const int row = 32 * q + lane;
         const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(32 * q) << 16);
         constexpr int S8d = S8 > 0 ? S8 : 1;
@@ -569,6 +582,7 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
         for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
             const Unit w = decode_unit<MODE, NCH>(u, p, nrc, nsc);
             for (int kb = 0; kb < w.kb; ++kb, ++seq) {
+                if ((seq & 1) != grp) continue;
                 const int stage = seq % STAGES;
                 const uint32_t phase = (seq / STAGES) & 1u;
                 const int slot = seq % S8d;
@@ -581,19 +595,22 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
                     break;
                 }
                 tc::fence_after_sync();
-                const uint4* src = reinterpret_cast<const uint4*>(f8ring + slot * SL + 64 * row);
-                uint32_t h[32];
+                const uint4* src = reinterpret_cast<const uint4*>(f8ring + slot * SL + 128 * row);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const uint4 v = src[i];
-                    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t h[32];
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        h[8 * i + 2 * j] = tc::e4m3x2_to_f16x2_div256(wv[j], 0);
-                        h[8 * i + 2 * j + 1] = tc::e4m3x2_to_f16x2_div256(wv[j], 2);
+                    for (int i = 0; i < 4; ++i) {
+                        const uint4 v = src[(4 * half + i) ^ (row & 7)];
+                        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            h[8 * i + 2 * j] = tc::e4m3x2_to_f16x2_div256(wv[j], 0);
+                            h[8 * i + 2 * j + 1] = tc::e4m3x2_to_f16x2_div256(wv[j], 2);
+                        }
                     }
+                    tc::tmem_st32(lane_base + static_cast<uint32_t>(kF8AColumn + 64 * stage + 32 * half), h);
                 }
-                tc::tmem_st32(lane_base + static_cast<uint32_t>(kF8AColumn + 32 * stage), h);
                 tc::fence_before_sync();
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(&conv[stage]);

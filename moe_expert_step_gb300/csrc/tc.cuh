@@ -171,6 +171,41 @@ __device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem,
         : "memory");
 }
 
+// Eight such MMAs in one statement (a 128-wide K block: A from TMEM columns a, a+8,
+// ..., a+56; B descriptors b[0..7]); the first accumulates into D only if acc0.
+__device__ __forceinline__ void mma8_f16_tmem_a(uint32_t d_tmem, uint32_t a, const uint64_t (&b)[8], uint32_t idesc,
+                                                uint32_t acc0) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %10, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %11, p;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%12], %3, %11, 1;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%13], %4, %11, 1;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%14], %5, %11, 1;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%15], %6, %11, 1;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%16], %7, %11, 1;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%17], %8, %11, 1;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%18], %9, %11, 1;\n\t}" ::"r"(d_tmem),
+        "r"(a), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]), "r"(acc0),
+        "r"(idesc), "r"(a + 8), "r"(a + 16), "r"(a + 24), "r"(a + 32), "r"(a + 40), "r"(a + 48), "r"(a + 56)
+        : "memory");
+}
+
+// Four MMAs with A from TMEM (a 64-wide K half: A columns a, a+8, a+16, a+24; B
+// descriptors b[0..3]); the first accumulates into D only if acc0.
+__device__ __forceinline__ void mma4_f16_tmem_a(uint32_t d_tmem, uint32_t a, const uint64_t (&b)[4], uint32_t idesc,
+                                                uint32_t acc0) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %7, p;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%8], %3, %7, 1;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%9], %4, %7, 1;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%10], %5, %7, 1;\n\t}" ::"r"(d_tmem),
+        "r"(a), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "r"(acc0), "r"(idesc), "r"(a + 8), "r"(a + 16), "r"(a + 24)
+        : "memory");
+}
+
 // Store 32 consecutive 32-bit columns into this warp's 32 TMEM lanes (thread i -> lane i)
 // and wait until the stores are done.
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {

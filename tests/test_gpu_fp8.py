@@ -98,7 +98,7 @@ def test_fp8_clover_layer_ffn(top_p):
 
 
 RAGGED8 = replace(W.LAYER_FP8, name="ragged_fp8", family="ragged8", H=256, E=64, k=6, I=128, Is=128, V=1024, P=7)
-NOSHARED8 = replace(W.LAYER_FP8, name="noshared_fp8", family="noshared8", H=384, E=48, k=4, I=192, Is=0, V=1024,
+NOSHARED8 = replace(W.LAYER_FP8, name="noshared_fp8", family="noshared8", H=384, E=48, k=4, I=256, Is=0, V=1024,
                     P=16)
 
 
@@ -155,7 +155,7 @@ def test_fp8_codes_convert_exactly(kind):
     f16 subnormals) or a mix of every code class (subnormal, normal, +-448, zero), each
     row scaled by 256 so the activations stay in f16's normal range.  A flushed subnormal
     would zero the 'subnormal' output entirely."""
-    H, E, k, I, Is, P = 128, 8, 8, 64, 64, 4
+    H, E, k, I, Is, P = 128, 8, 8, 128, 128, 4
     cfg = replace(W.LAYER_FP8, name=f"codes_{kind}", family=f"codes_{kind}", H=H, E=E, k=k, I=I, Is=Is, V=1024,
                   P=P)
     d = dims_of(cfg)
