@@ -190,13 +190,13 @@ int get_encode() {
 
 // 2D bf16 tensor [rows][cols] (cols contiguous), boxes of 64 columns x box_rows
 // rows in the 128-byte swizzled shared-memory layout; out-of-range rows read as 0.
-// FP8 E4M3 weights: boxes of 64 rows x 128 bytes (a K block of 128) in the 128-byte
+// FP8 E4M3 weights: boxes of 128 rows x 128 bytes (a K block of 128) in the 128-byte
 // swizzled layout, so the converter threads' row reads hit distinct banks (the expert launch's
 // converter warps write the swizzled f16 operand themselves)
 int make_map_fp8(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows) {
     cuuint64_t dims[2] = {cols, rows};
     cuuint64_t strides[1] = {cols};
-    cuuint32_t box[2] = {128, 64};
+    cuuint32_t box[2] = {128, 128};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

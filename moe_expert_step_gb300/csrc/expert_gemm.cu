@@ -40,8 +40,10 @@ namespace moestep {
 namespace {
 
 constexpr int kThreads = 192;
-constexpr int kThreadsF8 = 480;  // + eight converter warps (two groups of four) and a second MMA warp
+constexpr int kThreadsF8 = 512;  // + eight converter warps (two groups of four), a second MMA warp and a
+                                 // second TMA warp
 constexpr int kMmaWarp2 = 14;    // FP8: issues the second 64-wide half of each K block into its own accumulator
+constexpr int kTmaWarp2 = 15;    // FP8: loads the odd K blocks' slots
 constexpr uint64_t kTeardownNs = 1000000000ull;  // fixed limit for draining in-flight copies/MMAs
 constexpr int kABytes = 16384;            // 128 rows x 64 bf16
 constexpr int kBoxBBytes = 16 * 128;      // 16 rows x 64 bf16
@@ -63,9 +65,14 @@ constexpr int kF8Tile = 16384;    // 128 rows x 128 E4M3 bytes
 constexpr int kF8AStages = 4;     // f16 A operands in TMEM
 constexpr int kF8AColumn = 256;   // their first TMEM column (accumulators use 0 .. 2 NCH - 1 <= 128)
 __host__ __device__ constexpr int f8_slot_bytes(int nch) { return kF8Tile + 2 * nch * 128; }
+// Even, so that with two TMA warps taking alternate K blocks each slot is always filled by
+// the same warp: a warp then never reaches a slot's next use before it filled the current
+// one, which the parity waits on the slot's barriers rely on (they tell two phases apart).
 __host__ __device__ constexpr int f8_slots(int nch) {
-    return (kSmemBudget - 1024) / f8_slot_bytes(nch) > 24 ? 24 : (kSmemBudget - 1024) / f8_slot_bytes(nch);
+    return ((kSmemBudget - 1024) / f8_slot_bytes(nch) > 24 ? 24 : (kSmemBudget - 1024) / f8_slot_bytes(nch)) & ~1;
 }
+static_assert(f8_slots(32) % 2 == 0 && f8_slots(64) % 2 == 0 && f8_slots(64) >= 4, "FP8 slot ring");
+static_assert(kF8AStages % 2 == 0, "each converter group must own its A stages");
 __host__ __device__ constexpr int smem_bytes_f8(int nch) { return f8_slots(nch) * f8_slot_bytes(nch) + 1024 + 1024; }
 
 struct Unit {
@@ -254,14 +261,15 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
     volatile int* abortv = abort_flag;
     const uint64_t tmo = p.timeout_ns;
 
-    if (F8 && warp == 0) {
-        // ------------------------------------------------------------ FP8 tile producer
-        // Fills the FP8 slot ring in unit / K-block order, far ahead of the MMA stages; the
-        // token rows of each stage are loaded by the converter warp that owns the stage.
+    if (F8 && (warp == 0 || warp == kTmaWarp2)) {
+        // ------------------------------------------------------------ FP8 tile producers
+        // Fill the slot ring in unit / K-block order, far ahead of the MMAs: warp 0 the even
+        // K blocks, warp kTmaWarp2 the odd ones (one TMA issuer alone does not keep up).
+        const int pg = warp == 0 ? 0 : 1;
         const uint64_t pol = tc::policy_evict_first();
         uint32_t issued = 0, issued_parity = 0;
-        int slot = 0;
-        uint32_t ph8 = 0;
+        constexpr int S8d = S8 > 0 ? S8 : 1;
+        int seq = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
             const Unit w = decode_unit<MODE, NCH>(u, p, nrc, nsc);
@@ -280,7 +288,10 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
                     break;
                 }
             }
-            for (int kb = 0; kb < w.kb; ++kb) {
+            for (int kb = 0; kb < w.kb; ++kb, ++seq) {
+                if ((seq & 1) != pg) continue;
+                const int slot = seq % S8d;
+                const uint32_t ph8 = (seq / S8d) & 1u;
                 int good = 1;
                 if (lane == 0) {
                     good = tc::mbar_wait(&empty8[slot], ph8 ^ 1u, abortv, tmo);
@@ -288,7 +299,6 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
                         uint8_t* dst = f8ring + slot * SL;
                         tc::mbar_arrive_expect_tx(&full8[slot], kF8Tile + 2 * nb * kBoxBBytes);
                         tc::tma_load_2d_hint(dst, mA, &full8[slot], kb * 128, w.rowA0, pol);
-                        tc::tma_load_2d_hint(dst + kF8Tile / 2, mA, &full8[slot], kb * 128, w.rowA1, pol);
                         for (int b = 0; b < nb; ++b) {
                             tc::tma_load_2d(dst + kF8Tile + b * kBoxBBytes, mB, &full8[slot], kb * 128,
                                             w.slot0 + 16 * b);
@@ -304,10 +314,6 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
                     ok = false;
                     if (lane == 0) record_timeout(p.err, 1, u, kb, slot, ph8, n_units, w.n);
                     break;
-                }
-                if (++slot == S8) {
-                    slot = 0;
-                    ph8 ^= 1u;
                 }
             }
         }
