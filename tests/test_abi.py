@@ -94,3 +94,60 @@ def test_binding_raises_on_error(L):
     with pytest.raises(ms.MoeStepError) as ei:
         ms.workspace_size(ms.ModelDims(H=2048, E=256, k=0, I=512, Is=512, V=10), 1)
     assert ei.value.code == ms.EINVAL
+
+
+CLOVER8 = ms.ModelDims(H=2048, E=256, k=8, I=512, Is=512, V=152064, P=32, dtype=ms.FP8)
+
+
+def test_fp8_dims_and_workspace(L):
+    """FP8 expert weights keep 2-byte activations: the same workspace as bf16."""
+    assert ms.workspace_size(CLOVER8, 1) == ms.workspace_size(CLOVER, 1)
+    assert ms.workspace_size(CLOVER8, 16) == ms.workspace_size(CLOVER, 16)
+    for bad in (dict(H=2000), dict(I=500)):
+        d = ms.ModelDims(**{**CLOVER8.__dict__, **bad})
+        n = ctypes.c_size_t(0)
+        assert L.moestep_workspace_size(ctypes.byref(d.c()), 1, ctypes.byref(n)) == ms.EUNSUPPORTED
+
+
+def test_fp8_layer_checks_before_launch(L):
+    """An FP8 layer needs its four row-scale tensors (three when there is no shared
+    expert is not allowed: Is > 0 needs the shared scales) and K blocks of 128."""
+    fake = 1 << 20
+    d = CLOVER8.c()
+    ws_bytes = ms.workspace_size(CLOVER8, 1)
+    no_scales = ms.Layer(fake, fake, fake, fake, fake)
+    rc = L.moe_block_ffn(ctypes.byref(d), 1, fake, ctypes.byref(no_scales), fake, fake, fake, ws_bytes, None)
+    assert rc == ms.EINVAL
+    no_shared_scales = ms.Layer(fake, fake, fake, fake, fake, fake, fake, None, None)
+    rc = L.moe_block_ffn(ctypes.byref(d), 1, fake, ctypes.byref(no_shared_scales), fake, fake, fake, ws_bytes, None)
+    assert rc == ms.EINVAL
+    odd = ms.ModelDims(**{**CLOVER8.__dict__, "I": 192}).c()      # I % 64 == 0 but not % 128
+    full = ms.Layer(fake, fake, fake, fake, fake, fake, fake, fake, fake)
+    rc = L.moe_block_ffn(ctypes.byref(odd), 1, fake, ctypes.byref(full), fake, fake, fake,
+                         ms.workspace_size(ms.ModelDims(**{**CLOVER8.__dict__, "I": 192}), 1), None)
+    assert rc == ms.EUNSUPPORTED
+    arr = (ms.Layer * 1)(no_scales)
+    rc = L.block_decode_step(ctypes.byref(d), 1, 1, arr, fake, fake, 1.0, 0.95, fake, None, fake, fake, fake, fake,
+                             fake, fake, None, fake, ws_bytes, None)
+    assert rc == ms.EINVAL
+
+
+def test_loop_and_fusion_arguments(L):
+    fake = 1 << 20
+    d = CLOVER.c()
+    ws_bytes = ms.workspace_size(CLOVER, 1)
+    arr = (ms.Layer * 1)(ms.Layer(fake, fake, fake, fake, fake))
+    # negative round cap, missing rounds output, missing embedding
+    rc = L.block_decode_loop(ctypes.byref(d), 1, 1, arr, fake, fake, fake, 5, fake, 1.0, 0.95, -1, fake, fake, fake,
+                             fake, ws_bytes, None)
+    assert rc == ms.EINVAL
+    rc = L.block_decode_loop(ctypes.byref(d), 1, 1, arr, fake, fake, fake, 5, fake, 1.0, 0.95, 8, fake, fake, None,
+                             fake, ws_bytes, None)
+    assert rc == ms.EINVAL
+    rc = L.block_decode_loop(ctypes.byref(d), 1, 1, arr, fake, None, fake, 5, fake, 1.0, 0.95, 8, fake, fake, fake,
+                             fake, ws_bytes, None)
+    assert rc == ms.EINVAL
+    rc = L.block_decode_loop(ctypes.byref(d), 1, 1, arr, fake, fake, fake, 5, fake, 1.0, 0.95, 8, fake, fake, fake,
+                             fake, ws_bytes - 256, None)
+    assert rc == ms.EWORKSPACE
+    assert L.moestep_set_route_fusion(1) == ms.OK and L.moestep_set_route_fusion(0) == ms.OK
