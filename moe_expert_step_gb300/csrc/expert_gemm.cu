@@ -29,6 +29,19 @@
 //                          weight layout, so the pair meets in one shuffle)
 //                 down:    y (fp32) per token slot
 //                 LM head: per position and 32-row slice: (max, argmax, sum exp)
+//
+// FP8 E4M3 weights (kExpertsF8, 512 threads), K blocks of 128:
+//   warps 0, 15 TMA producers on alternate K blocks: a ring of shared-memory
+//               slots, each one 128 x 128-byte FP8 tile (128-byte swizzle) and
+//               its token rows as two 64-wide f16 B boxes.
+//   warps 6-13  converters, two groups of four on alternate K blocks: each
+//               warp turns the 32 tile rows of its TMEM lane quarter into f16
+//               (exact, values times 2^-8) and stores them with tcgen05.st
+//               as the MMA's A operand in tensor memory.
+//   warps 1, 14 MMA issuers, one 64-wide half of every K block each, into
+//               their own accumulators (the issue cost is per issuing thread).
+//   warps 2-5   epilogue as above, adding the two accumulators and applying
+//               2^8 times each weight row's scale; SwiGLU rows stored as f16.
 // The epilogue warps never wait on each other, and every wait is bounded
 // (timeout -> error word, orderly teardown), so no wait can hang the GPU.
 #include "common.cuh"

@@ -17,9 +17,10 @@ enum GemmMode { kGateUp = 0, kDown = 1, kLmHead = 2, kExperts = 3, kExpertsF8 = 
 // shared weights, b[0] gathered activations), then every down unit (a[2] / a[3],
 // b[1] = SwiGLU output); a down unit of a chunk starts once all of that
 // chunk's gate/up units have signalled completion.  kLmHead uses a[0] and b[0].
-// kExpertsF8: as kExperts with FP8 E4M3 weight maps (a[0..3], 64x64-byte boxes,
-// no swizzle), f16 activations in b[0..1], per-row scales sc[0..3] (same order
-// as a[0..3]) applied to the accumulators, and the SwiGLU output stored as f16.
+// kExpertsF8: as kExperts with FP8 E4M3 weight maps (a[0..3], boxes of 128 rows x
+// 128 bytes, 128-byte swizzle; K blocks of 128), f16 activations in b[0..1], per-row
+// scales sc[0..3] (same order as a[0..3]) applied to the accumulators, and the
+// SwiGLU output stored as f16.
 struct TensorMaps {
     CUtensorMap a[4];
     CUtensorMap b[2];
