@@ -544,28 +544,62 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
                     for (int j = 0; j < 32; ++j)
                         if (j < cnt) y[static_cast<size_t>(w.slot0 + c0 + j) * ld + h] = v[j];
                 } else {
-                    // per (position, 32-row slice): max logit, its lowest row, sum of exp(l - max)
+                    // per (position, 32-row slice): max logit, its lowest row, sum of exp(l - max).
+                    // Transposed butterfly over the warp: at offset o each lane keeps the half of
+                    // its columns whose bit o matches its own and takes its partner's partial of
+                    // them, so after five steps lane j holds column j reduced over the 32 rows
+                    // (31 shuffles per quantity instead of 10 per column).
                     const int row = w.mt * 128 + L;
                     const bool valid = row < p.V;
-                    float mm = -INFINITY, ss = 0.f;
-                    int aa = 0;
+                    float lg[32];
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
-                        if (j < cnt) {
-                            const float l = valid ? v[j] * p.scale : -INFINITY;
-                            if (p.logits != nullptr && valid)
-                                p.logits[static_cast<size_t>(w.slot0 + c0 + j) * p.V + row] = l;
-                            float m = l;
-                            int a = row;
-                            warp_argmax(m, a);
-                            const float s = (m == -INFINITY) ? 0.f : warp_sum(valid ? __expf(l - m) : 0.f);
-                            if (lane == j) {
-                                mm = m;
-                                aa = a;
-                                ss = s;
-                            }
+                        lg[j] = (valid && j < cnt) ? v[j] * p.scale : -INFINITY;
+                        if (p.logits != nullptr && valid && j < cnt)
+                            p.logits[static_cast<size_t>(w.slot0 + c0 + j) * p.V + row] = lg[j];
+                    }
+                    float m[32];
+                    int ar[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        m[j] = lg[j];
+                        ar[j] = row;
+                    }
+#pragma unroll
+                    for (int o = 16; o >= 1; o >>= 1) {
+                        const bool up = (lane & o) != 0;
+#pragma unroll
+                        for (int i = 0; i < o; ++i) {
+                            const float give_m = up ? m[i] : m[i + o];
+                            const int give_a = up ? ar[i] : ar[i + o];
+                            const float km = up ? m[i + o] : m[i];
+                            const int ka = up ? ar[i + o] : ar[i];
+                            const float rm = __shfl_xor_sync(0xffffffffu, give_m, o);
+                            const int ra = __shfl_xor_sync(0xffffffffu, give_a, o);
+                            const bool take = rm > km || (rm == km && ra < ka);
+                            m[i] = take ? rm : km;
+                            ar[i] = take ? ra : ka;
                         }
                     }
+                    const float mm = m[0];  // column `lane`
+                    const int aa = ar[0];
+                    float e[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const float mj = __shfl_sync(0xffffffffu, mm, j);
+                        e[j] = (mj == -INFINITY || lg[j] == -INFINITY) ? 0.f : __expf(lg[j] - mj);
+                    }
+#pragma unroll
+                    for (int o = 16; o >= 1; o >>= 1) {
+                        const bool up = (lane & o) != 0;
+#pragma unroll
+                        for (int i = 0; i < o; ++i) {
+                            const float give = up ? e[i] : e[i + o];
+                            const float keep = up ? e[i + o] : e[i];
+                            e[i] = keep + __shfl_xor_sync(0xffffffffu, give, o);
+                        }
+                    }
+                    const float ss = e[0];
                     if (lane < cnt) {
                         const size_t o = static_cast<size_t>(w.mt * 4 + sp) * p.n_pos + (w.slot0 + c0 + lane);
                         p.pmax[o] = mm;
