@@ -155,7 +155,7 @@ struct Vec8<float> {
     }
 };
 
-// grid (ceil(T/8), ceil(E/8)), 256 threads.  Each CTA stages 8 tokens of x in
+// grid (ceil(T/4), ceil(E/8)), 256 threads.  Each CTA stages 4 tokens of x in
 // shared memory; each warp computes one expert's logits for those tokens (every
 // lane's 16-byte weight loads are issued before any is used).  The last CTA to
 // finish a token group (atomic counter, reset by that CTA) runs the softmax and
@@ -698,6 +698,118 @@ __device__ __forceinline__ uint32_t word8(const uint4& lo, const uint4& hi, int 
     return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
 }
 
+// Tensor-core router for bf16 (E % 32 == 0, H % 512 == 0): grid (ceil(T / (8 NT)),
+// E / 32), 512 threads.  A CTA computes the logits of 32 experts for 8*NT tokens
+// with mma.sync m16n8k16 (bf16 in, fp32 accumulation): warp w takes the 16-expert
+// half w & 1 and the K eighth w >> 1, reads its weight rows and token rows straight
+// from global memory (16-byte loads, the K permutation of the layer-head kernel
+// above), and the eight K partial sums of every logit are added in K order through
+// shared memory.  The last CTA of a token tile (self-resetting counter) runs the
+// softmax and top-k of the tile's tokens.
+constexpr int kRouteTcThreads = 512;
+constexpr int kRouteTcExperts = 32;
+
+__host__ __device__ inline size_t route_tc_smem_bytes(int nt, int E) {
+    const size_t part = static_cast<size_t>(kRouteTcThreads / 32) * nt * 32 * 4 * sizeof(float);
+    const size_t zs = static_cast<size_t>(8) * nt * E * sizeof(float);
+    return part > zs ? part : zs;
+}
+
+template <int NT>
+__global__ void __launch_bounds__(kRouteTcThreads, 1)
+    route_tc_kernel(const bf16* __restrict__ x, const bf16* __restrict__ Wr, int ntok, int H, int E, int k,
+                    float* __restrict__ logits, int32_t* idx, float* mass, float* gate, int* counters) {
+    extern __shared__ __align__(16) uint8_t rtc_smem[];
+    float* part = reinterpret_cast<float*>(rtc_smem);  // [16 warps][NT][32 lanes][4]
+    __shared__ int last;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, tig = lane & 3;
+    const int eh = warp & 1, q = warp >> 1;
+    const int t0 = blockIdx.x * 8 * NT;
+    const int e0 = blockIdx.y * kRouteTcExperts;
+    const int kspan = H >> 3;
+    {  // router weights are never written: hint this CTA's rows before waiting
+        const char* w = reinterpret_cast<const char*>(Wr + static_cast<size_t>(e0) * H);
+        const int lines = kRouteTcExperts * H * 2 / 128;
+        for (int l = threadIdx.x; l < lines; l += kRouteTcThreads)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(w + 128ll * l));
+    }
+    pdl_trigger();
+    pdl_wait();
+    float d[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) d[nt][r] = 0.f;
+    const bf16* w0 = Wr + static_cast<size_t>(e0 + eh * 16 + g) * H;
+    const bf16* w1 = w0 + static_cast<size_t>(8) * H;
+    const bf16* xr[NT];
+    bool ok[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int t = t0 + nt * 8 + g;
+        ok[nt] = t < ntok;
+        xr[nt] = x + static_cast<size_t>(ok[nt] ? t : 0) * H;
+    }
+#pragma unroll 2
+    for (int h0 = q * kspan; h0 < (q + 1) * kspan; h0 += 64) {
+        const int hb = h0 + 16 * tig;
+        const uint4 a00 = __ldg(reinterpret_cast<const uint4*>(w0 + hb));
+        const uint4 a01 = __ldg(reinterpret_cast<const uint4*>(w0 + hb + 8));
+        const uint4 a10 = __ldg(reinterpret_cast<const uint4*>(w1 + hb));
+        const uint4 a11 = __ldg(reinterpret_cast<const uint4*>(w1 + hb + 8));
+        uint4 b0[NT], b1[NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            b0[nt] = ok[nt] ? __ldcg(reinterpret_cast<const uint4*>(xr[nt] + hb)) : make_uint4(0, 0, 0, 0);
+            b1[nt] = ok[nt] ? __ldcg(reinterpret_cast<const uint4*>(xr[nt] + hb + 8)) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                mma_16816(d[nt], word8(a00, a01, 2 * j), word8(a10, a11, 2 * j), word8(a00, a01, 2 * j + 1),
+                          word8(a10, a11, 2 * j + 1), word8(b0[nt], b1[nt], 2 * j), word8(b0[nt], b1[nt], 2 * j + 1));
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+        *reinterpret_cast<float4*>(part + ((warp * NT + nt) * 32 + lane) * 4) =
+            make_float4(d[nt][0], d[nt][1], d[nt][2], d[nt][3]);
+    __syncthreads();
+    // element r of lane ln in an MMA tile: expert g + 8*(r >= 2), token 2*tig + (r & 1)
+    for (int i = threadIdx.x; i < 2 * NT * 128; i += kRouteTcThreads) {
+        const int tile = i >> 7, ln = (i >> 2) & 31, r = i & 3;
+        const int h = tile / NT, nt = tile % NT;
+        float v = 0.f;
+#pragma unroll
+        for (int qq = 0; qq < 8; ++qq) v += part[(((qq * 2 + h) * NT + nt) * 32 + ln) * 4 + r];
+        const int e = e0 + h * 16 + (ln >> 2) + (r >= 2 ? 8 : 0);
+        const int t = t0 + nt * 8 + 2 * (ln & 3) + (r & 1);
+        if (t < ntok) logits[static_cast<size_t>(t) * E + e] = v;
+    }
+    // ---- last CTA of this token tile does the softmax / top-k
+    __threadfence();
+    __syncthreads();
+    if (gridDim.y > 1) {
+        if (threadIdx.x == 0) {
+            const int prev = atomicAdd(&counters[blockIdx.x], 1);
+            last = (prev == static_cast<int>(gridDim.y) - 1);
+            if (last) counters[blockIdx.x] = 0;
+        }
+        __syncthreads();
+        if (!last) return;
+        __threadfence();
+    }
+    const int nt_tok = min(8 * NT, ntok - t0);
+    float* zs = reinterpret_cast<float*>(rtc_smem);  // reuse: [8 NT][E]
+    const int n = nt_tok * E;
+#pragma unroll 4
+    for (int i = threadIdx.x; i < n; i += kRouteTcThreads) zs[i] = __ldcg(&logits[static_cast<size_t>(t0) * E + i]);
+    __syncthreads();
+    for (int tt = warp; tt < nt_tok; tt += kRouteTcThreads / 32)
+        topk_one_token(zs + tt * E, E, k, t0 + tt, idx, mass, gate);
+}
+
 struct PlanLayout {
     int LD;             // staged row length (elements): H + 8, so the 8 rows of an MMA tile hit distinct banks
     size_t region;      // staged rows / K-split partial sums / coreset scratch (aliased in turn)
@@ -931,7 +1043,23 @@ cudaError_t launch_route(int dtype, const void* x, const void* Wr, int T, int H,
     const size_t zs_bytes = static_cast<size_t>(kRouteTokens) * E * sizeof(float);
     const size_t smem = xs_bytes > zs_bytes ? xs_bytes : zs_bytes;
     cudaError_t e;
-    static int done_bf16[64] = {}, done_f32[64] = {};
+    static int done_bf16[64] = {}, done_f32[64] = {}, done_tc[3][64] = {};
+    if (dtype == MOESTEP_BF16 && E % kRouteTcExperts == 0 && H % 512 == 0 && E <= 1024) {
+        // 8*NT tokens per CTA: about one CTA per SM on large batches, more CTAs on small ones
+        const int nt = T > 256 ? 2 : 1;
+        const dim3 g((T + 8 * nt - 1) / (8 * nt), E / kRouteTcExperts);
+        const size_t sm = route_tc_smem_bytes(nt, E);
+        const bf16* xb = static_cast<const bf16*>(x);
+        const bf16* wb = static_cast<const bf16*>(Wr);
+        if (nt == 2) {
+            if ((e = ensure_smem(route_tc_kernel<2>, sm, done_tc[1])) != cudaSuccess) return e;
+            return launch_pdl(route_tc_kernel<2>, g, dim3(kRouteTcThreads), sm, s, xb, wb, T, H, E, k, logits, idx,
+                              mass, gate, counters);
+        }
+        if ((e = ensure_smem(route_tc_kernel<1>, sm, done_tc[0])) != cudaSuccess) return e;
+        return launch_pdl(route_tc_kernel<1>, g, dim3(kRouteTcThreads), sm, s, xb, wb, T, H, E, k, logits, idx, mass,
+                          gate, counters);
+    }
     if (dtype == MOESTEP_BF16) {
         if ((e = ensure_smem(route_kernel<bf16>, smem, done_bf16)) != cudaSuccess) return e;
         return launch_pdl(route_kernel<bf16>, grid, dim3(256), smem, s, static_cast<const bf16*>(x),

@@ -34,6 +34,41 @@ def topk_margins(z: np.ndarray, k: int) -> np.ndarray:
     return s[:, k - 1] - s[:, k]
 
 
+def match_topk(idx, oi, z, k: int, eps: float = 1e-4) -> np.ndarray:
+    """Check a kernel's top-k lists `idx` [T][k] against the oracle's `oi` and return
+    the column permutation that aligns them (perm[t, j] = column of idx[t] holding
+    oi[t, j]).
+
+    The order of the k picks is a floating-point decision like the k-th/(k+1)-th
+    boundary (callers check that one with topk_margins): the kernel accumulates
+    logits in fp32 in its own order, so two picks whose fp64 logits lie within
+    `eps` of each other may come out in either order.  Such runs of neighbours
+    must hold the same experts on both sides; everywhere else the order is
+    exact."""
+    idx = np.asarray(idx)
+    oi = np.asarray(oi)
+    assert idx.shape == oi.shape
+    zs = np.take_along_axis(np.asarray(z, np.float64), oi.astype(np.int64), axis=1)
+    perm = np.empty(oi.shape, np.int64)
+    for t in range(oi.shape[0]):
+        j = 0
+        while j < k:
+            e = j + 1
+            while e < k and zs[t, e - 1] - zs[t, e] <= eps:
+                e += 1
+            got = [int(v) for v in idx[t, j:e]]
+            assert sorted(got) == sorted(int(v) for v in oi[t, j:e]), (t, j, idx[t], oi[t])
+            for u in range(j, e):
+                perm[t, u] = j + got.index(int(oi[t, u]))
+            j = e
+    return perm
+
+
+def aligned(a, perm) -> np.ndarray:
+    """Columns of a per-pick array [T][k] reordered by match_topk's permutation."""
+    return np.take_along_axis(np.asarray(a), perm, axis=1)
+
+
 def coreset_margin(cs: oracle.CoresetResult) -> float:
     """Smallest relative distance between a request's target and the cumulative sums
     around its cut (how much the masses may move before the kept set changes)."""

@@ -17,7 +17,7 @@ import moe_expert_step_gb300 as ms
 import oracle
 import synth
 from synth import workloads as W
-from tests.helpers import BF16_TOL, F32_TOL, coreset_margin, max_rel, np_, oracle_layer, t, topk_margins
+from tests.helpers import BF16_TOL, F32_TOL, coreset_margin, match_topk, max_rel, np_, oracle_layer, t, topk_margins
 
 pytestmark = pytest.mark.gpu
 THR = 0.95
@@ -124,7 +124,7 @@ def test_clover_layer_step(fusion, corr):
         np.zeros(cfg.P, np.int32), masked0, bf16=True, trace=trace)
     tr = trace[0]
     assert (topk_margins(tr["z"], cfg.k) > 1e-4).all() and coreset_margin(tr["coreset"]) > 1e-5
-    np.testing.assert_array_equal(np_(st.idx)[0], tr["idx"])
+    match_topk(np_(st.idx)[0], tr["idx"], tr["z"], cfg.k)
     assert np_(st.n_sel)[0, 0] == tr["coreset"].n_sel[0]
     assert max_rel(np_(st.h_out), h) <= BF16_TOL
     assert max_rel(np_(st.h_out) - h0, h - h0) <= BF16_TOL       # the MoE update itself
@@ -160,7 +160,7 @@ def test_stack_layer_from_oracle_state(stack, depth, fusion):
     tr = trace[0]
     ok = topk_margins(tr["z"], cfg.k) > 1e-4
     assert ok.all() and coreset_margin(tr["coreset"]) > 1e-5
-    np.testing.assert_array_equal(np_(st.idx)[0], tr["idx"])
+    match_topk(np_(st.idx)[0], tr["idx"], tr["z"], cfg.k)
     assert np_(st.n_sel)[0, 0] == tr["coreset"].n_sel[0]
     assert max_rel(np_(st.h_out) - h_in, h_ref - h_in) <= BF16_TOL
     assert max_rel(np_(st.h_out), h_ref) <= BF16_TOL
@@ -182,7 +182,7 @@ def test_stack_full_step(stack, fusion):
     ol = oracle_layer(cfg, 0)
     oi, om, _, oz = oracle.route(x0, ol.Wr, cfg.k)
     assert (topk_margins(oz, cfg.k) > 1e-4).all()
-    np.testing.assert_array_equal(idx[0], oi)
+    match_topk(idx[0], oi, oz, cfg.k)
     assert n_sel[0] == oracle.coreset_select(oi, om, 0.9, cfg.P).n_sel[0]
     # properties at every depth: each coreset keeps a prefix covering 90% of its own routing
     for l in range(cfg.n_layers):
@@ -215,10 +215,15 @@ def test_route_fusion_matches_separate_launches(stack):
     finally:
         ms.set_route_fusion(False)
     (i1, n1, h1, x1), (i2, n2, h2, x2) = out
-    # layer 0: identical inputs, decisions are exact on both sides
-    np.testing.assert_array_equal(i1[0], i2[0])
-    assert n1[0, 0] == n2[0, 0]
-    agree = [(i1[l] == i2[l]).all() and n1[l, 0] == n2[l, 0] for l in range(cfg.n_layers)]
+    # layer 0: identical inputs; both match the oracle's picks (order inside near-tied
+    # runs of logits is a rounding decision of each kernel's summation order)
+    x0 = oracle.round_bf16(oracle.rmsnorm(h0.astype(np.float64)))
+    oi, om, _, oz = oracle.route(x0, oracle_layer(cfg, 0).Wr, cfg.k)
+    assert (topk_margins(oz, cfg.k) > 1e-4).all()
+    match_topk(i1[0], oi, oz, cfg.k)
+    match_topk(i2[0], oi, oz, cfg.k)
+    assert n1[0, 0] == n2[0, 0] == oracle.coreset_select(oi, om, 0.9, cfg.P).n_sel[0]
+    agree = [(np.sort(i1[l], 1) == np.sort(i2[l], 1)).all() and n1[l, 0] == n2[l, 0] for l in range(cfg.n_layers)]
     if all(agree):
         assert max_rel(h1, h2) <= BF16_TOL and max_rel(x1, x2) <= BF16_TOL
     else:   # a near-tie flipped deep in the stack: the layers before it still agree
