@@ -325,7 +325,22 @@ struct CoresetScratch {  // shared memory of one coreset CTA
     uint8_t csurv[kCandCache];
 };
 
-__device__ void coreset_body(const CoresetArgs& a, int r, int nreq, uint32_t* masks, CoresetScratch& sc) {
+// Slots of the work plan staged in shared memory (token and expert of each slot)
+// by the coreset launch's plan step when several requests share it, so the plan
+// goes out as coalesced stores: up to kSlotStage slots, within the CTA's limit.
+constexpr int kSlotStage = 8192;
+__host__ __device__ inline size_t coreset_masks_bytes(int E, int T) {
+    return (static_cast<size_t>(E) * ((T + 31) / 32) * 4 + 15) / 16 * 16;
+}
+__host__ __device__ inline int coreset_stage_slots(int E, int T, int k) {
+    const size_t slots = static_cast<size_t>(T) * (k + 1);
+    const size_t bytes = sizeof(CoresetScratch) + coreset_masks_bytes(E, T) + slots * 8;
+    return (slots <= kSlotStage && bytes <= 227 * 1024) ? static_cast<int>(slots) : 0;
+}
+
+// stage: shared memory for coreset_stage_slots(E, T, k) slots (2 ints each), or NULL
+__device__ void coreset_body(const CoresetArgs& a, int r, int nreq, uint32_t* masks, CoresetScratch& sc,
+                             int* stage = nullptr, int nstage = 0) {
     long long* A = sc.A;
     long long* cum = sc.cum;
     int* cnt = sc.cnt;
@@ -372,7 +387,7 @@ __device__ void coreset_body(const CoresetArgs& a, int r, int nreq, uint32_t* ma
         atomicAdd(&cnt[e], 1);
         if (local) {
             const int t = c / k;
-            atomicOr(&masks[e * TWl + (t >> 5)], 1u << (t & 31));
+            atomicOr(&masks[(t >> 5) * E + e], 1u << (t & 31));
         }
     }
     __syncthreads();
@@ -526,22 +541,52 @@ __device__ void coreset_body(const CoresetArgs& a, int r, int nreq, uint32_t* ma
     }
     const int T = a.T;
     const int TW = (T + 31) >> 5;
-    if (!local) {  // count survivors per expert over every request
+    const int nck = T * k;
+    // Every request's candidates: expert id, or -1 if pruned.  Staged in shared memory
+    // (int16 over the dead aggregates) when they fit, with all of a thread's loads in
+    // flight at once; otherwise read from global memory where used.
+    int16_t* pk = reinterpret_cast<int16_t*>(A);
+    const bool staged = !local && nck <= static_cast<int>(sizeof(sc.A) / sizeof(int16_t));
+    if (!local) {  // survivors per expert over every request: a token bitmask per expert
         for (int i = tid; i < E * TW; i += blockDim.x) masks[i] = 0u;
-        if (tid < E) cnt[tid] = 0;
+        if (staged) {
+            const int nth = blockDim.x;
+            for (int c0 = tid; c0 < nck; c0 += 4 * nth) {
+                int e4[4];
+                uint8_t s4[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int c = c0 + u * nth;
+                    e4[u] = c < nck ? __ldcg(&a.idx[c]) : 0;
+                    s4[u] = c < nck ? __ldcg(&a.survive[c]) : 0;
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int c = c0 + u * nth;
+                    if (c < nck) pk[c] = static_cast<int16_t>(s4[u] != 0 ? e4[u] : -1);
+                }
+            }
+        }
         __syncthreads();
-        for (int c = tid; c < T * k; c += blockDim.x) {
-            if (__ldcg(&a.survive[c]) != 0) {
-                const int e = __ldcg(&a.idx[c]);
+        for (int c = tid; c < nck; c += blockDim.x) {
+            const int e = staged ? pk[c] : (__ldcg(&a.survive[c]) != 0 ? __ldcg(&a.idx[c]) : -1);
+            if (e >= 0) {
                 const int t = c / k;
-                atomicAdd(&cnt[e], 1);
-                atomicOr(&masks[e * TW + (t >> 5)], 1u << (t & 31));
+                atomicOr(&masks[(t >> 5) * E + e], 1u << (t & 31));
             }
         }
         __syncthreads();
     }
-    // one request: every candidate of a kept expert survives, so phase 1's counts and masks hold
-    const int my_cnt = tid < E ? ((local && !keep[tid]) ? 0 : cnt[tid]) : 0;
+    // one request: every candidate of a kept expert survives, so phase 1's counts and masks
+    // hold; several: an expert's survivors are the bits of its mask
+    int my_cnt = 0;
+    if (tid < E) {
+        if (local) {
+            my_cnt = keep[tid] ? cnt[tid] : 0;
+        } else {
+            for (int w = 0; w < TW; ++w) my_cnt += __popc(masks[w * E + tid]);
+        }
+    }
     const int my_nch = (my_cnt + a.nch - 1) / a.nch;
     // one scan of (chunks << 32 | slots)
     const long long both = block_inclusive_scan<long long>(
@@ -561,18 +606,28 @@ __device__ void coreset_body(const CoresetArgs& a, int r, int nreq, uint32_t* ma
     }
     __syncthreads();
     const int NR = s_nr, nrc = s_nrc;
-    for (int c = tid; c < T * k; c += blockDim.x) {
-        const bool sv = local ? csurv[c] != 0 : __ldcg(&a.survive[c]) != 0;
-        if (sv) {
-            const int e = local ? cidx[c] : __ldcg(&a.idx[c]);
+    for (int c = tid; c < nck; c += blockDim.x) {
+        int e;
+        if (local)
+            e = csurv[c] != 0 ? cidx[c] : -1;
+        else if (staged)
+            e = pk[c];
+        else
+            e = __ldcg(&a.survive[c]) != 0 ? __ldcg(&a.idx[c]) : -1;
+        if (e >= 0) {
             const int t = c / k;
             const int w = t >> 5;
             int pos = order[e];
-            for (int q = 0; q < w; ++q) pos += __popc(masks[e * TW + q]);
-            pos += __popc(masks[e * TW + w] & ((1u << (t & 31)) - 1u));
+            for (int q = 0; q < w; ++q) pos += __popc(masks[q * E + e]);
+            pos += __popc(masks[w * E + e] & ((1u << (t & 31)) - 1u));
             a.slot_of[c] = pos;
-            a.slot_tok[pos] = t;
-            a.slot_exp[pos] = e;
+            if (stage != nullptr) {
+                stage[pos] = t;
+                stage[nstage + pos] = e;
+            } else {
+                a.slot_tok[pos] = t;
+                a.slot_exp[pos] = e;
+            }
         } else {
             a.slot_of[c] = -1;
         }
@@ -582,8 +637,13 @@ __device__ void coreset_body(const CoresetArgs& a, int r, int nreq, uint32_t* ma
         nsc = (T + a.nch - 1) / a.nch;
         for (int t = tid; t < T; t += blockDim.x) {
             a.slot_sh[t] = NR + t;
-            a.slot_tok[NR + t] = t;
-            a.slot_exp[NR + t] = E;
+            if (stage != nullptr) {
+                stage[NR + t] = t;
+                stage[nstage + NR + t] = E;
+            } else {
+                a.slot_tok[NR + t] = t;
+                a.slot_exp[NR + t] = E;
+            }
         }
         for (int i = tid; i < nsc; i += blockDim.x)
             a.chunks[nrc + i] = make_int4(E, NR + i * a.nch, min(a.nch, T - i * a.nch), 0);
@@ -592,6 +652,14 @@ __device__ void coreset_body(const CoresetArgs& a, int r, int nreq, uint32_t* ma
         a.plan[0] = nrc;
         a.plan[1] = nsc;
         a.plan[2] = NR + (a.has_shared ? T : 0);
+    }
+    if (stage != nullptr) {  // the staged slots, in order
+        __syncthreads();
+        const int ns = NR + (a.has_shared ? T : 0);
+        for (int i = tid; i < ns; i += blockDim.x) {
+            a.slot_tok[i] = stage[i];
+            a.slot_exp[i] = stage[nstage + i];
+        }
     }
 }
 
@@ -650,15 +718,20 @@ __device__ void coreset_prefetch(const CoresetArgs& a, uint32_t* bits) {
 
 // grid R (+ pf_ctas hint CTAs), 1024 threads: one CTA per request (see coreset_body).
 __global__ void __launch_bounds__(kCoresetThreads) coreset_kernel(CoresetArgs a) {
-    extern __shared__ __align__(16) uint8_t coreset_smem[];  // scratch, then masks [E][ceil(T/32)]
+    extern __shared__ __align__(16) uint8_t coreset_smem[];  // scratch, masks [ceil(T/32)][E], slot staging
     pdl_trigger();
     pdl_wait();
     if (static_cast<int>(blockIdx.x) >= a.R) {
         coreset_prefetch(a, reinterpret_cast<uint32_t*>(coreset_smem));
         return;
     }
+    // slot staging only pays when several requests share the plan step
+    const int nstage = a.R > 1 ? coreset_stage_slots(a.E, a.T, a.k) : 0;
+    int* stage = nstage > 0 ? reinterpret_cast<int*>(coreset_smem + sizeof(CoresetScratch) +
+                                                     coreset_masks_bytes(a.E, a.T))
+                            : nullptr;
     coreset_body(a, blockIdx.x, a.R, reinterpret_cast<uint32_t*>(coreset_smem + sizeof(CoresetScratch)),
-                 *reinterpret_cast<CoresetScratch*>(coreset_smem));
+                 *reinterpret_cast<CoresetScratch*>(coreset_smem), stage, nstage);
 }
 
 // ---------------------------------------------------------------------------- single-block layer head
@@ -1043,9 +1116,9 @@ cudaError_t launch_route(int dtype, const void* x, const void* Wr, int T, int H,
     const size_t zs_bytes = static_cast<size_t>(kRouteTokens) * E * sizeof(float);
     const size_t smem = xs_bytes > zs_bytes ? xs_bytes : zs_bytes;
     cudaError_t e;
-    static int done_bf16[64] = {}, done_f32[64] = {}, done_tc[3][64] = {};
+    static int done_bf16[64] = {}, done_f32[64] = {}, done_tc[2][64] = {};
     if (dtype == MOESTEP_BF16 && E % kRouteTcExperts == 0 && H % 512 == 0 && E <= 1024) {
-        // 8*NT tokens per CTA: about one CTA per SM on large batches, more CTAs on small ones
+        // 8*NT tokens per CTA: 16 above 256 tokens (measured faster at 512 tokens than 8 or 32), else 8
         const int nt = T > 256 ? 2 : 1;
         const dim3 g((T + 8 * nt - 1) / (8 * nt), E / kRouteTcExperts);
         const size_t sm = route_tc_smem_bytes(nt, E);
@@ -1080,10 +1153,11 @@ cudaError_t launch_topk_from_logits(const float* logits, int T, int E, int k, in
                       gate);
 }
 
-int coreset_smem_bytes(int E, int T) { return static_cast<int>(sizeof(CoresetScratch)) + E * ((T + 31) / 32) * 4; }
+int coreset_smem_bytes(int E, int T) { return static_cast<int>(sizeof(CoresetScratch) + coreset_masks_bytes(E, T)); }
 
 cudaError_t launch_coreset(const CoresetArgs& a, cudaStream_t s) {
-    const size_t smem = coreset_smem_bytes(a.E, a.T);
+    const size_t smem = coreset_smem_bytes(a.E, a.T) +
+                        (a.R > 1 ? static_cast<size_t>(coreset_stage_slots(a.E, a.T, a.k)) * 8 : 0);
     static int done[64] = {};
     cudaError_t e = ensure_smem(coreset_kernel, smem, done);
     if (e != cudaSuccess) return e;

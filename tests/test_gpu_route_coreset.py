@@ -58,8 +58,10 @@ def test_topk_from_fed_logits_exact(E, k, T):
     assert max_rel(gate, og) < 1e-5
 
 
-@pytest.mark.parametrize("cfg_name,T", [("tiny_fp32", 8), ("clover_layer", 32), ("clover_layer", 71)])
+@pytest.mark.parametrize("cfg_name,T", [("tiny_fp32", 8), ("clover_layer", 32), ("clover_layer", 71),
+                                        ("clover_layer", 300), ("clover_layer", 517)])
 def test_route_matches_oracle(cfg_name, T):
+    """Computed logits; T = 300 and 517 take the 16- and 32-token router tiles, with ragged tails."""
     cfg = W.CONFIGS[cfg_name]
     d = dims_of(cfg)
     lay = W.device_layer(cfg, 0)
