@@ -53,7 +53,10 @@ def parse():
     ap.add_argument("--prof-all", action="store_true", help="time every kernel in the roofline pass")
     ap.add_argument("--no-graph", action="store_true", help="time direct launches instead of CUDA-graph replays")
     ap.add_argument("--route-fusion", action="store_true",
-                    help="one request: one cluster launch between expert launches instead of four")
+                    help="one request: one cluster launch between expert launches (same as --layer-head 1)")
+    ap.add_argument("--layer-head", type=int, choices=(0, 1, 2), default=None,
+                    help="between expert launches: 0 separate combine/router/coreset/gather launches, 1 one "
+                         "cluster launch (one request), 2 combine inside the router launch (library default)")
     return ap.parse_args()
 
 
@@ -212,7 +215,8 @@ def run_gpu(args, dist: Dist):
     accept = torch.zeros(T, dtype=torch.uint8, device="cuda")
     n_comm = torch.zeros(R, dtype=torch.int32, device="cuda")
     ws = ms.workspace(d, R)
-    ms.set_route_fusion(args.route_fusion)
+    if args.route_fusion or args.layer_head is not None:
+        ms.set_route_fusion(1 if args.route_fusion else args.layer_head)
     torch.cuda.synchronize()
     t_setup = time.time() - t_setup
 
@@ -366,7 +370,7 @@ def run_gpu(args, dist: Dist):
         "warmup": max(3, args.warmup), "ms_per_step": round(ms_step, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 experts, bf16 rest" if cfg.dtype == "fp8" else "bf16",
         "data": "synthetic",
-        "config": {**workload_desc(cfg, R, args), "route_fusion": R == 1 and args.route_fusion},
+        "config": {**workload_desc(cfg, R, args), "layer_head": layer_head_desc(cfg, R)},
         "expert_weight_hbm": {
             "bytes_per_step": step_bytes, "expert_bytes_per_step": eb["expert_weights"],
             "experts_kept_per_layer": {"mean": round(statistics.mean(unions), 2), "min": min(unions),
@@ -477,6 +481,18 @@ def kernel_sources_sha() -> str:
     for f in ("expert_gemm.cu", "tc.cuh", "common.cuh"):
         h.update(open(os.path.join(ROOT, "moe_expert_step_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
+
+
+def layer_head_desc(cfg, R: int) -> str:
+    """What ran between expert launches (the library's mode, where the shape qualifies for it)."""
+    import moe_expert_step_gb300 as ms
+
+    mode = ms.route_fusion()
+    if mode == 1 and R == 1 and cfg.P <= 32:
+        return "one cluster launch: combine + RMSNorm, router, top-k, coreset, plan, gather"
+    if mode == 2 and R * cfg.P <= 256 and cfg.E % 32 == 0 and cfg.E <= 256 and cfg.H % 512 == 0:
+        return "combine + RMSNorm inside the router's cluster launch; coreset; gather"
+    return "separate launches: combine + RMSNorm, router, coreset, gather"
 
 
 def load_traffic(experts_per_launch: float):

@@ -259,8 +259,8 @@ long long moestep_launch_count(void);
  * with events (0 turns timing off; enabling clears earlier records);
  * moestep_prof_read() synchronises and returns, per kernel id, the number of
  * timed launches and their summed duration in ms.  Kernel ids: 0 route
- * (with fusion on: the single-request cluster launch, see
- * moestep_set_route_fusion),
+ * (with the fused layer heads of moestep_set_route_fusion: the cluster
+ * launch that holds the router),
  * 1 coreset, 2 gather, 3 expert FFN (bf16: gate/up + SwiGLU + down in one
  * launch; fp32: gate/up), 4 fp32 expert down, 5 combine/norm, 6 LM head,
  * 7 commit, 8 other.  Not thread-safe. */
@@ -275,16 +275,24 @@ int moestep_prof_read(int kernel_id, int* launches, double* total_ms);
  * hook for that path. */
 int moestep_set_wait_timeout_ns(unsigned long long ns);
 
-/* Whether block_decode_step runs, for a single request, everything between
- * two expert launches (the previous layer's combine and RMSNorm, router,
- * top-k, coreset, work plan and token gather) as one cluster launch (on: 1)
- * or as the separate combine / moe_block_route / coreset_select / gather
- * launches (0, the default).  Only bf16 models with R == 1, P <= 32, E a multiple
- * of 128 up to 512 and H a multiple of 64 * 32 / (E / 128) up to 4096
- * qualify; others always take the separate launches.  The two paths differ
- * only in the summation order of the router logits.  Process-wide; not
- * thread-safe. */
-int moestep_set_route_fusion(int on);
+/* What block_decode_step runs between two expert launches (the previous
+ * layer's combine and RMSNorm, router, top-k, coreset, work plan and token
+ * gather):
+ *   0  separate launches: combine, router, coreset, gather;
+ *   1  one cluster launch for all of them, for a single request: bf16 models
+ *      with R == 1, P <= 32, E a multiple of 128 up to 512 and H a multiple of
+ *      64 * 32 / (E / 128) up to 4096;
+ *   2  (the default) the combine and RMSNorm inside the router's launch (a
+ *      cluster of E / 32 CTAs per 8 tokens), then coreset and gather: bf16
+ *      activations, at most 256 block tokens, E a multiple of 32 up to 256 and
+ *      H a multiple of 512.
+ * Shapes a mode does not cover take the separate launches.  Modes 0 and 2
+ * compute bit-identical results; mode 1 differs from them only in the
+ * summation order of the router logits.  Returns MOESTEP_EINVAL for another
+ * mode.  Process-wide; not thread-safe. */
+int moestep_set_route_fusion(int mode);
+/* The mode set by moestep_set_route_fusion. */
+int moestep_route_fusion(void);
 
 #ifdef __cplusplus
 }

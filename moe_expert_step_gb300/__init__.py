@@ -34,7 +34,8 @@ EXPORTS = [
     "lm_head_commit", "lm_commit_from_logits", "block_embed", "block_decode_step", "block_decode_loop",
     "moestep_read_device_error",
     "moestep_error_string", "moestep_last_cuda_error", "moestep_prof_enable", "moestep_prof_read",
-    "moestep_set_wait_timeout_ns", "moestep_set_route_fusion", "moestep_launch_count", "moe_block_route_noalloc",
+    "moestep_set_wait_timeout_ns", "moestep_set_route_fusion", "moestep_route_fusion", "moestep_launch_count",
+    "moe_block_route_noalloc",
 ]
 
 
@@ -94,6 +95,7 @@ def lib():
             "moestep_prof_read": [i, ctypes.POINTER(i), ctypes.POINTER(ctypes.c_double)],
             "moestep_set_wait_timeout_ns": [ctypes.c_ulonglong],
             "moestep_set_route_fusion": [ctypes.c_int],
+            "moestep_route_fusion": [],
             "moestep_launch_count": [],
         }
         for name, args in sig.items():
@@ -245,10 +247,20 @@ def read_device_error(ws, stream=None) -> int:
     return w.value
 
 
-def set_route_fusion(on: bool) -> None:
-    """One request in block_decode_step: one cluster launch between expert launches (True) or
-    the separate combine / router / coreset / gather launches (False, the default)."""
-    _check(lib().moestep_set_route_fusion(1 if on else 0), "moestep_set_route_fusion")
+SEPARATE_HEAD, CLUSTER_HEAD, FUSED_COMBINE_HEAD = 0, 1, 2
+
+
+def set_route_fusion(mode) -> None:
+    """What block_decode_step runs between expert launches: SEPARATE_HEAD (0, also False)
+    the combine / router / coreset / gather launches; CLUSTER_HEAD (1, also True) one cluster
+    launch for all of them (one request); FUSED_COMBINE_HEAD (2, the default) the combine
+    inside the router's launch."""
+    _check(lib().moestep_set_route_fusion(int(mode)), "moestep_set_route_fusion")
+
+
+def route_fusion() -> int:
+    """The mode last set by set_route_fusion."""
+    return int(lib().moestep_route_fusion())
 
 
 def set_wait_timeout_ns(ns: int) -> None:

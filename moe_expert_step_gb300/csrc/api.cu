@@ -23,7 +23,10 @@ namespace {
 
 thread_local int g_last_cuda = 0;
 unsigned long long g_timeout_ns = 2000000000ull;  // bounded waits inside the tcgen05 kernels
-bool g_route_plan = false;  // one request: the single cluster launch between expert launches
+// What runs between two expert launches of block_decode_step: 0 separate combine /
+// router / coreset / gather launches; 1 one cluster launch for all of them (one
+// request); 2 the combine fused into the router's cluster launch
+int g_layer_head = 2;
 
 #define MOESTEP_CK(expr)                             \
     do {                                             \
@@ -351,6 +354,33 @@ int run_route_plan(const Ctx& c, int mode, const float* h_in, const void* Wr, co
     a.done = at<int>(c.ws, L.done);
     a.n_done = L.max_chunks;
     MOESTEP_LAUNCH(0, launch_route_plan(a, c.s));
+    return MOESTEP_OK;
+}
+
+// the previous layer's combine (mode 1) or the input norm (mode 2), then the router
+int run_route_combine(const Ctx& c, int mode, const float* h_in, const void* Wr, int32_t* idx) {
+    const moestep_dims* d = c.d;
+    const Layout& L = c.L;
+    RouteCombineArgs a{};
+    a.mode = mode;
+    a.y = at<float>(c.ws, L.y);
+    a.slot_of = at<int32_t>(c.ws, L.slot_of);
+    a.slot_sh = at<int32_t>(c.ws, L.slot_sh);
+    a.gate_rr_prev = at<float>(c.ws, L.gaterr);
+    a.has_shared = d->Is > 0;
+    a.h_in = h_in;
+    a.hres = at<float>(c.ws, L.hres);
+    a.x = at<__nv_bfloat16>(c.ws, L.x);
+    a.Wr = static_cast<const __nv_bfloat16*>(Wr);
+    a.T = L.T;
+    a.H = d->H;
+    a.E = d->E;
+    a.k = d->k;
+    a.logits = nullptr;
+    a.idx = idx;
+    a.mass = at<float>(c.ws, L.mass);
+    a.gate = at<float>(c.ws, L.gate);
+    MOESTEP_LAUNCH(0, launch_route_combine(a, c.s));
     return MOESTEP_OK;
 }
 
@@ -765,9 +795,11 @@ int block_decode_step(const moestep_dims* dims, int R, int n_layers, const moest
     void* x = at<void>(ws, L.x);
     MOESTEP_CK(cudaMemsetAsync(at<char>(ws, L.counters), 0, L.counters_bytes, c.s));
     float* hid_trace = trace ? trace->hidden : nullptr;
-    const bool one_block = g_route_plan && n_layers > 0 &&
+    const bool one_block = g_layer_head == 1 && n_layers > 0 &&
                            route_plan_eligible(R, dims->dtype, T, dims->H, dims->E, k);
-    if (!one_block)
+    const bool fused_head = !one_block && g_layer_head == 2 && n_layers > 0 &&
+                            route_combine_eligible(act_dtype(dims->dtype), T, dims->H, dims->E, k);
+    if (!one_block && !fused_head)
         MOESTEP_LAUNCH(5, launch_combine(2, act_dtype(dims->dtype), T, dims->H, k, nullptr, nullptr, nullptr, nullptr, 0, h_in,
                                          hres, x, n_layers == 0 ? hid_trace : nullptr, nullptr, c.s));
     for (int l = 0; l < n_layers; ++l) {
@@ -787,15 +819,21 @@ int block_decode_step(const moestep_dims* dims, int R, int n_layers, const moest
                                                  nullptr, c.s));
             continue;
         }
-        MOESTEP_TRY(run_route(c, T, x, layers[l].Wr, idx, at<float>(ws, L.mass), at<float>(ws, L.gate), nullptr));
+        if (fused_head) {
+            // the combine of layer l-1 (or the input norm) runs inside the layer-l router launch
+            MOESTEP_TRY(run_route_combine(c, l == 0 ? 2 : 1, h_in, layers[l].Wr, idx));
+        } else {
+            MOESTEP_TRY(run_route(c, T, x, layers[l].Wr, idx, at<float>(ws, L.mass), at<float>(ws, L.gate), nullptr));
+        }
         MOESTEP_TRY(run_coreset(c, R, top_p, idx, at<float>(ws, L.mass), nsel, sel,
                                 at<uint8_t>(ws, L.survive), at<float>(ws, L.gaterr), layers[l].Wgu,
                                 last ? nullptr : layers[l + 1].Wr));
         MOESTEP_TRY(run_experts(c, R, x, &layers[l]));
-        MOESTEP_LAUNCH(5, launch_combine(1, act_dtype(dims->dtype), T, dims->H, k, at<float>(ws, L.y),
-                                         at<int32_t>(ws, L.slot_of), at<int32_t>(ws, L.slot_sh),
-                                         at<float>(ws, L.gaterr), dims->Is > 0, nullptr, hres, x,
-                                         last ? hid_trace : nullptr, nullptr, c.s));
+        if (!fused_head || last)
+            MOESTEP_LAUNCH(5, launch_combine(1, act_dtype(dims->dtype), T, dims->H, k, at<float>(ws, L.y),
+                                             at<int32_t>(ws, L.slot_of), at<int32_t>(ws, L.slot_sh),
+                                             at<float>(ws, L.gaterr), dims->Is > 0, nullptr, hres, x,
+                                             last ? hid_trace : nullptr, nullptr, c.s));
     }
     MOESTEP_TRY(run_lm_commit(c, R, x, Wlm, logit_scale, threshold, tokens, masked, choice, conf, accept, n_committed,
                               nullptr));
@@ -830,7 +868,7 @@ int block_decode_loop(const moestep_dims* dims, int R, int n_layers, const moest
     key_add(key, logit_scale);
     key_add(key, threshold);
     key_add(key, max_rounds);
-    key_add(key, g_route_plan);
+    key_add(key, g_layer_head);
     key_add(key, g_timeout_ns);
     std::lock_guard<std::mutex> lock(g_loop_mu);
     if (g_loop.exec == nullptr || g_loop.key != key) {
@@ -926,12 +964,15 @@ int moestep_prof_read(int kernel_id, int* launches, double* total_ms) {
     return MOESTEP_OK;
 }
 
-// Test hook: limit of every bounded wait in the tensor-core kernels (ns).
-int moestep_set_route_fusion(int on) {
-    g_route_plan = on != 0;
+int moestep_set_route_fusion(int mode) {
+    if (mode < 0 || mode > 2) return MOESTEP_EINVAL;
+    g_layer_head = mode;
     return MOESTEP_OK;
 }
 
+int moestep_route_fusion(void) { return g_layer_head; }
+
+// Test hook: limit of every bounded wait in the tensor-core kernels (ns).
 int moestep_set_wait_timeout_ns(unsigned long long ns) {
     g_timeout_ns = ns;
     return MOESTEP_OK;

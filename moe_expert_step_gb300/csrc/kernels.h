@@ -127,6 +127,27 @@ struct RoutePlanArgs {
     int* done;                      // expert-launch counters to zero
     int n_done;
 };
+// The previous layer's combine + RMSNorm and the router (logits, softmax, top-k) in
+// one cluster launch over 8-token tiles (bf16 activations).
+struct RouteCombineArgs {
+    int mode;                       // 1: h += experts' outputs, x = RMSNorm(h); 2: h = h_in, x = RMSNorm(h)
+    const float* y;
+    const int32_t* slot_of;
+    const int32_t* slot_sh;
+    const float* gate_rr_prev;
+    int has_shared;
+    const float* h_in;
+    float* hres;
+    __nv_bfloat16* x;
+    const __nv_bfloat16* Wr;
+    int T, H, E, k;
+    float* logits;                  // optional [T][E]
+    int32_t* idx;
+    float* mass;
+    float* gate;
+};
+int route_combine_eligible(int act_dtype, int T, int H, int E, int k);
+cudaError_t launch_route_combine(const RouteCombineArgs& a, cudaStream_t s);
 int route_plan_eligible(int R, int dtype, int T, int H, int E, int k);
 size_t route_plan_smem_bytes(int T, int H, int E, int k);
 cudaError_t launch_route_plan(const RoutePlanArgs& a, cudaStream_t s);

@@ -883,6 +883,107 @@ __global__ void __launch_bounds__(kRouteTcThreads, 1)
         topk_one_token(zs + tt * E, E, k, t0 + tt, idx, mass, gate);
 }
 
+// The previous layer's combine + RMSNorm and the tensor-core router in one
+// cluster launch (bf16 activations, E % 32 == 0, E <= 256, H % 512 == 0): grid
+// (E / 32, ceil(T / 8)), one cluster of E / 32 CTAs per 8-token tile.  CTA c of
+// a cluster runs the combine of tokens c, c + CL, ... of the tile (the combine
+// kernel's arithmetic, so both write bit-identical rows), the cluster barrier
+// makes the tile's x rows visible to the cluster, then CTA c computes the
+// logits of experts 32c .. 32c + 31 for the tile as route_tc_kernel does and
+// sends each logit over distributed shared memory to the CTA that takes the
+// token's softmax and top-k (token j of the tile: CTA j mod CL).
+struct RouteCombineSmem {
+    static constexpr int kPart = (kRouteTcThreads / 32) * 32 * 4;  // K partial sums [16 warps][32][4]
+    __host__ __device__ static int tokens_per_cta(int CL) { return (8 + CL - 1) / CL; }
+    __host__ __device__ static size_t bytes(int CL, int E) {
+        return sizeof(float) * (kPart + static_cast<size_t>(tokens_per_cta(CL)) * E) +
+               sizeof(int) * 2 * 33 + sizeof(float) * (2 * 33 + 2 * 9);
+    }
+};
+
+__global__ void __launch_bounds__(kRouteTcThreads, 1) route_combine_kernel(RouteCombineArgs a) {
+    extern __shared__ __align__(16) uint8_t rc_smem[];
+    cg::cluster_group cluster = cg::this_cluster();
+    const int CL = static_cast<int>(cluster.num_blocks());
+    const int rank = static_cast<int>(cluster.block_rank());
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, tig = lane & 3;
+    const int eh = warp & 1, q = warp >> 1;
+    const int T = a.T, H = a.H, E = a.E, k = a.k;
+    const int t0 = blockIdx.y * 8;
+    const int e0 = rank * kRouteTcExperts;
+    const int kspan = H >> 3;
+    const int TPC = RouteCombineSmem::tokens_per_cta(CL);
+    const int grp = threadIdx.x >> 8;  // combine: two groups of 256 threads
+    float* part = reinterpret_cast<float*>(rc_smem);
+    float* zs = part + RouteCombineSmem::kPart;  // [TPC][E] logits of this CTA's tokens
+    int* c_slot = reinterpret_cast<int*>(zs + static_cast<size_t>(TPC) * E) + 33 * grp;
+    float* c_g = reinterpret_cast<float*>(reinterpret_cast<int*>(zs + static_cast<size_t>(TPC) * E) + 66) + 33 * grp;
+    float* c_red = reinterpret_cast<float*>(reinterpret_cast<int*>(zs + static_cast<size_t>(TPC) * E) + 66) + 66 +
+                   9 * grp;
+    {  // router weights are never written: hint this CTA's rows before waiting
+        const char* w = reinterpret_cast<const char*>(a.Wr + static_cast<size_t>(e0) * H);
+        const int lines = kRouteTcExperts * H * 2 / 128;
+        for (int l = threadIdx.x; l < lines; l += kRouteTcThreads)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(w + 128ll * l));
+    }
+    pdl_trigger();
+    pdl_wait();
+    // 1. combine of this CTA's tokens of the tile
+    for (int j0 = 0; j0 < 8; j0 += 2 * CL) {
+        const int j = j0 + rank + CL * grp;
+        const int t = (j < 8 && t0 + j < T) ? t0 + j : -1;
+        if (a.mode == 1)
+            combine_row<bf16, 1>(t, H, k, a.y, a.slot_of, a.slot_sh, a.gate_rr_prev, a.has_shared, nullptr, a.hres,
+                                 a.x, nullptr, nullptr, c_slot, c_g, c_red);
+        else
+            combine_row<bf16, 2>(t, H, k, nullptr, nullptr, nullptr, nullptr, 0, a.h_in, a.hres, a.x, nullptr,
+                                 nullptr, c_slot, c_g, c_red);
+    }
+    cluster.sync();  // the tile's x rows are in global memory
+    // 2. logits of experts e0 .. e0 + 31 for the tile (route_tc_kernel's fragments)
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+    const bf16* w0 = a.Wr + static_cast<size_t>(e0 + eh * 16 + g) * H;
+    const bf16* w1 = w0 + static_cast<size_t>(8) * H;
+    const bool ok = t0 + g < T;
+    const bf16* xr = a.x + static_cast<size_t>(ok ? t0 + g : 0) * H;
+#pragma unroll 2
+    for (int h0 = q * kspan; h0 < (q + 1) * kspan; h0 += 64) {
+        const int hb = h0 + 16 * tig;
+        const uint4 a00 = __ldg(reinterpret_cast<const uint4*>(w0 + hb));
+        const uint4 a01 = __ldg(reinterpret_cast<const uint4*>(w0 + hb + 8));
+        const uint4 a10 = __ldg(reinterpret_cast<const uint4*>(w1 + hb));
+        const uint4 a11 = __ldg(reinterpret_cast<const uint4*>(w1 + hb + 8));
+        const uint4 b0 = ok ? __ldcg(reinterpret_cast<const uint4*>(xr + hb)) : make_uint4(0, 0, 0, 0);
+        const uint4 b1 = ok ? __ldcg(reinterpret_cast<const uint4*>(xr + hb + 8)) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj)
+            mma_16816(d, word8(a00, a01, 2 * jj), word8(a10, a11, 2 * jj), word8(a00, a01, 2 * jj + 1),
+                      word8(a10, a11, 2 * jj + 1), word8(b0, b1, 2 * jj), word8(b0, b1, 2 * jj + 1));
+    }
+    *reinterpret_cast<float4*>(part + (warp * 32 + lane) * 4) = make_float4(d[0], d[1], d[2], d[3]);
+    __syncthreads();
+    // 3. the eight K splits added in K order; each logit to the CTA that takes its token
+    for (int i = threadIdx.x; i < 2 * 128; i += kRouteTcThreads) {
+        const int h = i >> 7, ln = (i >> 2) & 31, r = i & 3;
+        float v = 0.f;
+#pragma unroll
+        for (int qq = 0; qq < 8; ++qq) v += part[((qq * 2 + h) * 32 + ln) * 4 + r];
+        const int e = e0 + h * 16 + (ln >> 2) + (r >= 2 ? 8 : 0);
+        const int j = 2 * (ln & 3) + (r & 1);
+        if (t0 + j < T) {
+            if (a.logits != nullptr) a.logits[static_cast<size_t>(t0 + j) * E + e] = v;
+            cluster.map_shared_rank(zs, j % CL)[(j / CL) * E + e] = v;
+        }
+    }
+    cluster.sync();  // every logit of this CTA's tokens has arrived
+    // 4. softmax and top-k, one warp per token
+    for (int jj = warp; jj < TPC; jj += kRouteTcThreads / 32) {
+        const int j = rank + CL * jj;
+        if (j < 8 && t0 + j < T) topk_one_token(zs + static_cast<size_t>(jj) * E, E, k, t0 + j, a.idx, a.mass, a.gate);
+    }
+}
+
 struct PlanLayout {
     int LD;             // staged row length (elements): H + 8, so the 8 rows of an MMA tile hit distinct banks
     size_t region;      // staged rows / K-split partial sums / coreset scratch (aliased in turn)
@@ -1173,6 +1274,34 @@ cudaError_t launch_gather(int dtype, const void* x, int H, const int32_t* slot_t
                           row_vec, slot_tok, plan, static_cast<uint4*>(xp), done, n_done);
     return launch_pdl(gather_kernel<false>, dim3(max_slots), dim3(256), 0, s, static_cast<const uint4*>(x), row_vec,
                       slot_tok, plan, static_cast<uint4*>(xp), done, n_done);
+}
+
+int route_combine_eligible(int act_dtype, int T, int H, int E, int k) {
+    if (act_dtype != MOESTEP_BF16 || T < 1 || T > 256 || k < 1 || k > 32) return 0;
+    return (E % kRouteTcExperts == 0 && E <= 8 * kRouteTcExperts && H % 512 == 0) ? 1 : 0;
+}
+
+cudaError_t launch_route_combine(const RouteCombineArgs& a, cudaStream_t s) {
+    const int CL = a.E / kRouteTcExperts;
+    const size_t smem = RouteCombineSmem::bytes(CL, a.E);
+    static int done[64] = {};
+    cudaError_t e = ensure_smem(route_combine_kernel, smem, done);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(CL, (a.T + 7) / 8);
+    cfg.blockDim = dim3(kRouteTcThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CL;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = g_launch_pdl ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, route_combine_kernel, a);
 }
 
 int route_plan_eligible(int R, int dtype, int T, int H, int E, int k) {

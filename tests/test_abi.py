@@ -150,4 +150,9 @@ def test_loop_and_fusion_arguments(L):
     rc = L.block_decode_loop(ctypes.byref(d), 1, 1, arr, fake, fake, fake, 5, fake, 1.0, 0.95, 8, fake, fake, fake,
                              fake, ws_bytes - 256, None)
     assert rc == ms.EWORKSPACE
-    assert L.moestep_set_route_fusion(1) == ms.OK and L.moestep_set_route_fusion(0) == ms.OK
+    prev = L.moestep_route_fusion()
+    assert prev == ms.FUSED_COMBINE_HEAD                       # the default
+    for mode in (ms.CLUSTER_HEAD, ms.SEPARATE_HEAD, ms.FUSED_COMBINE_HEAD):
+        assert L.moestep_set_route_fusion(mode) == ms.OK and L.moestep_route_fusion() == mode
+    assert L.moestep_set_route_fusion(3) == ms.EINVAL and L.moestep_set_route_fusion(-1) == ms.EINVAL
+    assert L.moestep_route_fusion() == ms.FUSED_COMBINE_HEAD

@@ -97,12 +97,15 @@ def test_tiny_model_full_loop(top_p, scale):
         assert rounds < cfg.P                              # the threshold branch fires
 
 
-@pytest.fixture(params=[False, True], ids=["separate", "fused"])
+@pytest.fixture(params=[ms.SEPARATE_HEAD, ms.CLUSTER_HEAD, ms.FUSED_COMBINE_HEAD],
+                ids=["separate", "cluster", "combine-in-router"])
 def fusion(request):
-    """Both single-request paths of block_decode_step: separate launches, one cluster launch."""
+    """Every single-request path of block_decode_step between expert launches: separate
+    launches, one cluster launch, the combine inside the router launch."""
+    prev = ms.route_fusion()
     ms.set_route_fusion(request.param)
     yield request.param
-    ms.set_route_fusion(False)
+    ms.set_route_fusion(prev)
 
 
 @pytest.mark.parametrize("corr", [0.0, 0.9])
@@ -197,24 +200,30 @@ def test_stack_full_step(stack, fusion):
     np.testing.assert_allclose(np.sqrt((hid ** 2).mean(1)), 1.0, rtol=2e-2)
 
 
-def test_route_fusion_matches_separate_launches(stack):
-    """The one-launch router/coreset/gather of a single request and the separate
-    launches take the same decisions on every layer of the stack; the residual
-    stream they produce differs only by the router's summation order."""
+def run_stack_modes(stack, modes):
     cfg, layers, Wlm_d, Wlm = stack
     h0 = W.host_h0(cfg, 1)
     masked0 = W.masked_subset(cfg, 1)
     out = []
+    prev = ms.route_fusion()
     try:
-        for fused in (True, False):
-            ms.set_route_fusion(fused)
+        for mode in modes:
+            ms.set_route_fusion(mode)
             st = Step(cfg, 1, cfg.n_layers)
-            st.run([clayer(l) for l in layers], Wlm_d, 0.9, t(h0), t(np.zeros(cfg.P, np.int32)),
-                   t(masked0.astype(np.uint8)))
-            out.append((np_(st.idx), np_(st.n_sel), np_(st.h_out), np_(st.hidden)))
+            tok = t(np.zeros(cfg.P, np.int32))
+            st.run([clayer(l) for l in layers], Wlm_d, 0.9, t(h0), tok, t(masked0.astype(np.uint8)))
+            out.append((np_(st.idx), np_(st.n_sel), np_(st.h_out), np_(st.hidden), np_(tok), np_(st.conf)))
     finally:
-        ms.set_route_fusion(False)
-    (i1, n1, h1, x1), (i2, n2, h2, x2) = out
+        ms.set_route_fusion(prev)
+    return h0, out
+
+
+def test_route_fusion_matches_separate_launches(stack):
+    """The one-launch router/coreset/gather of a single request and the separate
+    launches take the same decisions on every layer of the stack; the residual
+    stream they produce differs only by the router's summation order."""
+    cfg = stack[0]
+    h0, ((i1, n1, h1, x1, _, _), (i2, n2, h2, x2, _, _)) = run_stack_modes(stack, [ms.CLUSTER_HEAD, ms.SEPARATE_HEAD])
     # layer 0: identical inputs; both match the oracle's picks (order inside near-tied
     # runs of logits is a rounding decision of each kernel's summation order)
     x0 = oracle.round_bf16(oracle.rmsnorm(h0.astype(np.float64)))
@@ -228,3 +237,12 @@ def test_route_fusion_matches_separate_launches(stack):
         assert max_rel(h1, h2) <= BF16_TOL and max_rel(x1, x2) <= BF16_TOL
     else:   # a near-tie flipped deep in the stack: the layers before it still agree
         assert agree[: agree.index(False)] == [True] * agree.index(False)
+
+
+def test_combine_in_router_is_bit_identical(stack):
+    """The combine fused into the router's cluster launch does the separate combine and
+    router kernels' arithmetic in the same order: all 40 layers' routing, the residual
+    stream, the LM-head input and the commit are bit for bit the same."""
+    _, (a, b) = run_stack_modes(stack, [ms.FUSED_COMBINE_HEAD, ms.SEPARATE_HEAD])
+    for u, v in zip(a, b):
+        np.testing.assert_array_equal(u, v)
