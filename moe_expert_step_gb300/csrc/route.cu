@@ -306,9 +306,10 @@ constexpr int kCandCache = 2048;  // candidates of one request kept in shared me
 // The block coreset and work plan, executed by one 1024-thread CTA for request
 // r of nreq.  Phase 1: the coreset of request r.  Phase 2 (done by the last
 // request's CTA to finish, or directly when nreq == 1): the grouped-by-expert
-// work plan over the union of all requests' kept experts.  `masks` (E *
-// ceil(T/32) words) and `sc` are shared-memory scratch.  Used by the coreset kernel
-// (one CTA per request) and by the single-block router.
+// work plan over the union of all requests' kept experts.  `masks` (each
+// expert's token bitmask, word-major: word w of every expert side by side,
+// ceil(T/32) x E words) and `sc` are shared-memory scratch.  Used by the
+// coreset kernel (one CTA per request) and by the single-block router.
 struct CoresetScratch {  // shared memory of one coreset CTA
     long long A[1024];
     long long cum[1024];
