@@ -336,7 +336,8 @@ __host__ __device__ inline size_t coreset_masks_bytes(int E, int T) {
 __host__ __device__ inline int coreset_stage_slots(int E, int T, int k) {
     const size_t slots = static_cast<size_t>(T) * (k + 1);
     const size_t bytes = sizeof(CoresetScratch) + coreset_masks_bytes(E, T) + slots * 8;
-    return (slots <= kSlotStage && bytes <= 227 * 1024) ? static_cast<int>(slots) : 0;
+    // 1 KiB left for the kernel's static shared memory
+    return (slots <= kSlotStage && bytes <= 226 * 1024) ? static_cast<int>(slots) : 0;
 }
 
 // stage: shared memory for coreset_stage_slots(E, T, k) slots (2 ints each), or NULL
