@@ -42,7 +42,9 @@ EXPORTS = [
 class MoeStepError(RuntimeError):
     def __init__(self, code: int, what: str):
         self.code = code
-        super().__init__(f"{what}: {error_string(code)} ({code})")
+        # the library's text for the code, once it is loaded (loading it may be what failed)
+        text = error_string(code) if _LIB is not None else "library not loaded"
+        super().__init__(f"{what}: {text} ({code})")
 
 
 class Dims(ctypes.Structure):

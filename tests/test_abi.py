@@ -156,3 +156,14 @@ def test_loop_and_fusion_arguments(L):
         assert L.moestep_set_route_fusion(mode) == ms.OK and L.moestep_route_fusion() == mode
     assert L.moestep_set_route_fusion(3) == ms.EINVAL and L.moestep_set_route_fusion(-1) == ms.EINVAL
     assert L.moestep_route_fusion() == ms.FUSED_COMBINE_HEAD
+
+
+def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
+    """No fallback: with the shared library missing, the first call raises."""
+    from moe_expert_step_gb300 import _build
+    monkeypatch.setattr(ms, "_LIB", None)
+    monkeypatch.setattr(_build, "LIB", str(tmp_path / "libmoestep_missing.so"))
+    with pytest.raises(ms.MoeStepError):
+        ms.lib()
+    with pytest.raises(ms.MoeStepError):
+        ms.set_route_fusion(ms.FUSED_COMBINE_HEAD)
