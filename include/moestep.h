@@ -137,14 +137,21 @@ int moe_block_route(const moestep_dims* dims, int T, const void* x, const void* 
  * allocator, a fixed embedded budget) and that therefore cannot call
  * cudaMalloc or hand over a scratch buffer.
  * Scratch (router logits when `logits` is NULL, and the completion counters)
- * lives in one fixed array inside the library, 520 KiB per device, held by
- * every GPU that loads the library until the process exits.  Limits:
+ * lives in one fixed array inside the library, 520 KiB per CUDA context (one
+ * per device for the runtime's primary contexts), held by every GPU that loads
+ * the library until the process exits.  Limits:
  * T * E <= 131072 and T <= 8192; larger calls return MOESTEP_EUNSUPPORTED.
- * Arguments as in moe_block_route.  The first call on a device looks up the
- * array's device address (make that call before any stream capture).  The
+ * Arguments as in moe_block_route; x, Wr, the outputs and `stream` belong to
+ * the calling thread's current CUDA context.  The array has one copy per
+ * context, so its device address is looked up (cudaGetSymbolAddress) on the
+ * first call in each context: the primary context of a device, a context the
+ * caller created and made current, or a primary context re-created after
+ * cudaDeviceReset.  Make that first call before any stream capture.  The
  * call allocates nothing and clears the counters it needs on `stream`; all
- * calls share the one array, so calls whose executions overlap on the GPU
- * (other streams, other threads) race and must be serialised by the caller. */
+ * calls in one context share the one array, so calls whose executions overlap
+ * on the GPU (other streams, other threads) race and must be serialised by the
+ * caller.  Failures return MOESTEP_ECUDA with the cudaError_t in
+ * moestep_last_cuda_error(). */
 int moe_block_route_noalloc(const moestep_dims* dims, int T, const void* x, const void* Wr, int32_t* idx,
                             float* mass, float* gate, float* logits, void* stream);
 

@@ -518,6 +518,8 @@ bool thr_ok(float t) { return t > 0.f && t <= 1.f; }
 
 int validate_dims(const moestep_dims* d) { return check_dims(d); }
 int device_ok(int* sms) { return device_check(sms); }
+void set_last_cuda(int err) { g_last_cuda = err; }
+void count_launch() { g_launches.fetch_add(1); }
 
 void prof_begin(int kid, cudaStream_t s) {
     if (kid < 0 || kid >= MOESTEP_PROF_KERNELS || !((g_prof.mask >> kid) & 1)) return;

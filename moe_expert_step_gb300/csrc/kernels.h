@@ -192,6 +192,10 @@ int device_ok(int* sms);                   // current device is sm_103; *sms = i
 // ------------------------------------------------------------------ profiling hooks (api.cu)
 void prof_begin(int kid, cudaStream_t s);
 void prof_end(int kid, cudaStream_t s);
+// Bookkeeping shared by every entry point: the cudaError_t that moestep_last_cuda_error()
+// reports (this host thread), and the count that moestep_launch_count() reports.
+void set_last_cuda(int err);
+void count_launch();
 
 // Round loop: sets the while-node condition h to (any masked && rounds < max_rounds);
 // add = 1 increments *rounds first, add = 0 sets it to 0.

@@ -8,6 +8,8 @@
 // lives in one fixed-size array in this file, which every GPU that loads the
 // library holds until the process exits.  The caller still passes x, Wr and
 // the outputs.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -25,25 +27,78 @@ struct RouteScratch {
     int counters[kMaxGroups];
 };
 
-// One copy per device.  In host code this name is only a stand-in: host code
-// uses the device address looked up below, never the symbol itself.
+// One copy per CUDA context.  In host code this name is only a stand-in: host
+// code uses the device address looked up below, never the symbol itself.
 static __device__ __align__(256) RouteScratch g_route_scratch;
 
+// The array's device address belongs to the CUDA context that loaded this
+// module, not to the device number: a context the caller makes current
+// itself, or the primary context re-created after cudaDeviceReset, holds its
+// own copy at another address.  So the address is cached per context, under
+// the context's process-unique id (cuCtxGetId; ids are never reused, unlike
+// context handles), and looked up again for a context not seen before.
+struct CachedAddress {
+    unsigned long long ctx_id;
+    RouteScratch* addr;
+};
+constexpr int kCacheSlots = 64;
 std::mutex g_mu;
-RouteScratch* g_addr[64] = {};  // device address of g_route_scratch, per device
+CachedAddress g_cache[kCacheSlots] = {};
+int g_cache_used = 0, g_cache_next = 0;
 
-// Looks up the array's device address on the current device (once per device).
-int scratch_address(RouteScratch** out) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return MOESTEP_ECUDA;
-    if (dev < 0 || dev >= 64) return MOESTEP_EDEVICE;
-    std::lock_guard<std::mutex> lk(g_mu);
-    if (g_addr[dev] == nullptr) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || p == nullptr) return MOESTEP_ECUDA;
-        g_addr[dev] = static_cast<RouteScratch*>(p);
+PFN_cuCtxGetId_v12000 g_ctx_id = nullptr;
+std::once_flag g_ctx_id_once;
+
+// Id of the calling thread's current context; false if there is none (or the
+// driver call is unavailable).
+bool current_context_id(unsigned long long* id) {
+    std::call_once(g_ctx_id_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(fn);
+    });
+    return g_ctx_id != nullptr && g_ctx_id(nullptr, id) == CUDA_SUCCESS;
+}
+
+int lookup(RouteScratch** out) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_route_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+        moestep::set_last_cuda(static_cast<int>(e != cudaSuccess ? e : cudaErrorInvalidSymbol));
+        return MOESTEP_ECUDA;
     }
-    *out = g_addr[dev];
+    *out = static_cast<RouteScratch*>(p);
+    return MOESTEP_OK;
+}
+
+// The array's device address in the current context (looked up once per context).
+int scratch_address(RouteScratch** out) {
+    unsigned long long id = 0;
+    if (!current_context_id(&id)) {
+        // no current context yet: the symbol lookup makes the current device's
+        // primary context current, then its id can be read
+        RouteScratch* a = nullptr;
+        const int rc = lookup(&a);
+        if (rc != MOESTEP_OK) return rc;
+        if (!current_context_id(&id)) {
+            moestep::set_last_cuda(static_cast<int>(cudaErrorDeviceUninitialized));
+            return MOESTEP_ECUDA;
+        }
+    }
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (int i = 0; i < g_cache_used; ++i)
+        if (g_cache[i].ctx_id == id) {
+            *out = g_cache[i].addr;
+            return MOESTEP_OK;
+        }
+    RouteScratch* a = nullptr;
+    const int rc = lookup(&a);
+    if (rc != MOESTEP_OK) return rc;
+    const int slot = g_cache_used < kCacheSlots ? g_cache_used++ : (g_cache_next++ % kCacheSlots);
+    g_cache[slot] = CachedAddress{id, a};
+    *out = a;
     return MOESTEP_OK;
 }
 
@@ -62,10 +117,20 @@ extern "C" int moe_block_route_noalloc(const moestep_dims* dims, int T, const vo
     if ((rc = scratch_address(&s)) != MOESTEP_OK) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     // the completion counters must start at zero; the logits are fully written before they are read
-    if (cudaMemsetAsync(s->counters, 0, sizeof(int) * groups, st) != cudaSuccess) return MOESTEP_ECUDA;
-    float* lg = logits ? logits : s->logits;
-    if (moestep::launch_route(dims->dtype == MOESTEP_FP8 ? MOESTEP_BF16 : dims->dtype, x, Wr, T, dims->H, dims->E, dims->k, lg, idx, mass, gate, s->counters,
-                              nullptr, st) != cudaSuccess)
+    cudaError_t e = cudaMemsetAsync(s->counters, 0, sizeof(int) * groups, st);
+    if (e != cudaSuccess) {
+        moestep::set_last_cuda(static_cast<int>(e));
         return MOESTEP_ECUDA;
+    }
+    float* lg = logits ? logits : s->logits;
+    moestep::prof_begin(0, st);  // kernel id 0 (route), as for moe_block_route
+    e = moestep::launch_route(dims->dtype == MOESTEP_FP8 ? MOESTEP_BF16 : dims->dtype, x, Wr, T, dims->H, dims->E,
+                              dims->k, lg, idx, mass, gate, s->counters, nullptr, st);
+    moestep::prof_end(0, st);
+    if (e != cudaSuccess) {
+        moestep::set_last_cuda(static_cast<int>(e));
+        return MOESTEP_ECUDA;
+    }
+    moestep::count_launch();
     return MOESTEP_OK;
 }

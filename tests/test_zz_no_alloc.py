@@ -48,7 +48,9 @@ def test_noalloc_router_matches_workspace_router(cfg, T):
         ref = _outputs(T, cfg.k)
         ms.moe_block_route(d, x, Wr, *ref, ws)
         got = _outputs(T, cfg.k)
+        c0 = ms.launch_count()
         ms.moe_block_route_noalloc(d, x, Wr, *got)
+        assert ms.launch_count() == c0 + 1    # counted like the workspace router's launch
         torch.cuda.synchronize()
         np.testing.assert_array_equal(got[0].cpu().numpy(), ref[0].cpu().numpy())
         for g, r in zip(got[1:], ref[1:]):
