@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-loop", action="store_true", help="skip the whole-block round-loop measurement")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the batched-requests sweep (R = 1, 4, 16)")
+    ap.add_argument("--sweep", type=str, default="1,4,16", help="requests per step of the batched sweep")
     ap.add_argument("--correlation", type=float, default=0.0,
                     help="workload variant: tokens of a block share a hidden component (0 = independent)")
     ap.add_argument("--block", type=int, default=None, help="workload variant: block size P (default 32)")
@@ -52,11 +54,9 @@ def parse():
                     help="logit scale of the round-loop measurement (1 = every round is a fallback)")
     ap.add_argument("--prof-all", action="store_true", help="time every kernel in the roofline pass")
     ap.add_argument("--no-graph", action="store_true", help="time direct launches instead of CUDA-graph replays")
-    ap.add_argument("--route-fusion", action="store_true",
-                    help="one request: one cluster launch between expert launches (same as --layer-head 1)")
-    ap.add_argument("--layer-head", type=int, choices=(0, 1, 2), default=None,
-                    help="between expert launches: 0 separate combine/router/coreset/gather launches, 1 one "
-                         "cluster launch (one request), 2 combine inside the router launch (library default)")
+    ap.add_argument("--layer-head", type=int, choices=(0, 2), default=None,
+                    help="between expert launches: 0 separate combine/router/coreset/gather launches, "
+                         "2 combine inside the router launch (library default)")
     return ap.parse_args()
 
 
@@ -215,8 +215,8 @@ def run_gpu(args, dist: Dist):
     accept = torch.zeros(T, dtype=torch.uint8, device="cuda")
     n_comm = torch.zeros(R, dtype=torch.int32, device="cuda")
     ws = ms.workspace(d, R)
-    if args.route_fusion or args.layer_head is not None:
-        ms.set_route_fusion(1 if args.route_fusion else args.layer_head)
+    if args.layer_head is not None:
+        ms.set_route_fusion(args.layer_head)
     torch.cuda.synchronize()
     t_setup = time.time() - t_setup
 
@@ -338,6 +338,9 @@ def run_gpu(args, dist: Dist):
         round_loop = measure_round_loop(ms, W, cfg, d, R, layers, Wlm, top_p, ws, args.loop_scale, dist, THR)
     if ms.read_device_error(ws) != ms.OK:
         raise RuntimeError("device error word set during the benchmark")
+    sweep = None
+    if not args.no_sweep and R == 1:
+        sweep = measure_sweep(ms, W, cfg, d, layers, Wlm, [int(v) for v in args.sweep.split(",")], args, dist, THR)
 
     ms_step = ms_total / args.steps
     value = dist.world * args.steps * R / (ms_total / 1e3)   # one step advances R blocks
@@ -370,7 +373,8 @@ def run_gpu(args, dist: Dist):
         "warmup": max(3, args.warmup), "ms_per_step": round(ms_step, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 experts, bf16 rest" if cfg.dtype == "fp8" else "bf16",
         "data": "synthetic",
-        "config": {**workload_desc(cfg, R, args), "layer_head": layer_head_desc(cfg, R)},
+        "config": workload_desc(cfg, R, args),
+        "layer_head": layer_head_desc(cfg, R),
         "expert_weight_hbm": {
             "bytes_per_step": step_bytes, "expert_bytes_per_step": eb["expert_weights"],
             "experts_kept_per_layer": {"mean": round(statistics.mean(unions), 2), "min": min(unions),
@@ -390,10 +394,100 @@ def run_gpu(args, dist: Dist):
         "kernel_ms_per_step": {k: round(v[1] / steps_prof, 4) for k, v in prof.items() if v[0]},
         "clocks": clk, "gpu_launches": launches, "e2e": e2e,
         "round_loop": round_loop,
+        "sweep": sweep,
         "graph": not args.no_graph,
         "setup_s": round(t_setup, 1),
     }
     return line, cfg
+
+
+def measure_sweep(ms, W, cfg, d, layers, Wlm, Rs, args, dist, thr) -> dict:
+    """The same 40-layer step for R concurrent requests (R blocks of P tokens, one coreset per
+    request, experts grouped over the union of the requests' kept experts), each timed like the
+    headline: K CUDA-graph replays between CUDA events, then a pass with events around every
+    expert launch for that kernel's fraction of the HBM peak."""
+    import numpy as np
+    import torch
+
+    peak = load_peaks().get("hbm_gbs")
+    stream = torch.cuda.current_stream()
+    out = {"what": "block_decode_step over R requests x 32-token blocks, 40 layers, per-request coreset top_p "
+                   f"{TOP_P}; K = {args.steps} graph replays per R, inputs resident in HBM",
+           "points": []}
+    for R in Rs:
+        T = R * cfg.P
+        dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+        h0 = dev(W.host_h0(cfg, R))
+        tokens0 = torch.zeros(T, dtype=torch.int32, device="cuda")
+        masked0 = dev(W.masked_subset(cfg, R).astype(np.uint8))
+        top_p = torch.full((R,), TOP_P, dtype=torch.float32, device="cuda")
+        tokens, masked = tokens0.clone(), masked0.clone()
+        choice = torch.zeros(T, dtype=torch.int32, device="cuda")
+        conf = torch.zeros(T, dtype=torch.float32, device="cuda")
+        accept = torch.zeros(T, dtype=torch.uint8, device="cuda")
+        ncomm = torch.zeros(R, dtype=torch.int32, device="cuda")
+        ws = ms.workspace(d, R)
+
+        def step(**kw):
+            tokens.copy_(tokens0)
+            masked.copy_(masked0)
+            ms.block_decode_step(d, R, layers, Wlm, top_p, thr, h0, tokens, masked, choice, conf, accept, ncomm, ws,
+                                 **kw)
+
+        n_sel = torch.zeros((cfg.n_layers, R), dtype=torch.int32, device="cuda")
+        sel = torch.zeros((cfg.n_layers, R, cfg.E), dtype=torch.int32, device="cuda")
+        step(trace_n_sel=n_sel, trace_sel=sel)
+        torch.cuda.synchronize()
+        ns, sl = n_sel.cpu().numpy(), sel.cpu().numpy()
+        unions = [len(set().union(*[set(sl[l, r, :ns[l, r]].tolist()) for r in range(R)]))
+                  for l in range(cfg.n_layers)]
+        for _ in range(max(3, args.warmup)):
+            step()
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step()
+        stream.wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        for _ in range(3):
+            graph.replay()
+        dist.barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms_step = dist.max(e0.elapsed_time(e1)) / args.steps
+        ms.prof_enable(["expert_ffn"])
+        for _ in range(args.steps):
+            step()
+        torch.cuda.synchronize()
+        ff_n, ff_ms = ms.prof_read()["expert_ffn"]
+        ms.prof_enable([])
+        if ms.read_device_error(ws) != ms.OK:
+            raise RuntimeError(f"device error word set in the sweep (R = {R})")
+        eb = expert_bytes(cfg, unions)
+        step_bytes = eb["expert_weights"] + eb["router"] + eb["lm_head"]
+        ff_bytes = eb["expert_weights"] / cfg.n_layers + T * (cfg.k + 1) * (cfg.H * 2 + 4 * max(cfg.I, cfg.Is) + cfg.H * 4)
+        ff_gbs = ff_bytes / (ff_ms / max(1, ff_n) / 1e3) / 1e9
+        step_gbs = step_bytes / (ms_step / 1e3) / 1e9
+        out["points"].append({
+            "requests": R, "block_tokens": T, "block_steps_per_s": round(dist.world * R * 1e3 / ms_step, 2),
+            "ms_per_step": round(ms_step, 4), "experts_kept_per_layer_mean": round(float(np.mean(unions)), 2),
+            # routed tokens per kept expert (at most T k / |S|): the grouped GEMM's N, i.e. the flops per
+            # weight byte on the tensor pipe
+            "token_slots_per_kept_expert_at_most": round(T * cfg.k / float(np.mean(unions)), 2),
+            "gbs_whole_step": round(step_gbs, 1),
+            "frac_of_peak_whole_step": round(step_gbs / peak, 4) if peak else None,
+            "expert_kernel_avg_ms": round(ff_ms / max(1, ff_n), 5),
+            "frac_of_peak_expert_kernel": round(ff_gbs / peak, 4) if peak else None})
+        del graph, ws
+        torch.cuda.synchronize()
+    return out
 
 
 def measure_round_loop(ms, W, cfg, d, R, layers, Wlm, top_p, ws, scale, dist, thr, blocks=3):
@@ -488,34 +582,32 @@ def layer_head_desc(cfg, R: int) -> str:
     import moe_expert_step_gb300 as ms
 
     mode = ms.route_fusion()
-    if mode == 1 and R == 1 and cfg.P <= 32:
-        return "one cluster launch: combine + RMSNorm, router, top-k, coreset, plan, gather"
     if mode == 2 and R * cfg.P <= 256 and cfg.E % 32 == 0 and cfg.E <= 256 and cfg.H % 512 == 0:
         return "combine + RMSNorm inside the router's cluster launch; coreset; gather"
     return "separate launches: combine + RMSNorm, router, coreset, gather"
 
 
 def load_traffic(experts_per_launch: float):
-    """DRAM bytes per expert-FFN launch: the ncu capture's bytes per expert (profiles/) scaled to
-    the experts of one launch here; None if the kernel sources changed since that capture."""
-    p = os.path.join(ROOT, "profiles", "tc_gemm_clover_layer.md")
+    """DRAM bytes per expert-FFN launch: the ncu capture's bytes per expert (profiles/traffic.json,
+    one Clover layer) scaled to the experts of one launch here; None if the kernel sources
+    changed since that capture."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
-    vals = {}
-    for line in open(p):
-        if ":" in line and line.split(":")[0].strip() in ("experts_traffic_bytes_per_expert", "kernel_sources_sha"):
-            k, v = line.split(":", 1)
-            vals[k.strip()] = v.strip()
-    if vals.get("kernel_sources_sha") != kernel_sources_sha() or "experts_traffic_bytes_per_expert" not in vals:
+    rec = json.load(open(p)).get("tc_gemm_experts_bf16", {})
+    if rec.get("kernel_sources_sha") != kernel_sources_sha() or "dram_bytes_per_expert" not in rec:
         return None
-    return int(float(vals["experts_traffic_bytes_per_expert"]) * experts_per_launch)
+    return int(float(rec["dram_bytes_per_expert"]) * experts_per_launch)
 
 
 # ------------------------------------------------------------------------------------------ oracle (CPU)
-class OracleSample:
-    """The fp64 oracle on a bounded sample of the step: layer 0 of the stack over the whole
-    block (route, coreset, experts, residual, norm) and the LM head + commit.  Expert
-    weights the sample touches are generated before timing starts."""
+class OracleStep:
+    """The fp64 oracle's whole block step, timed for real: oracle.block_decode_step over all
+    40 layers (router, coreset, routed + shared experts, residual, RMSNorm per layer), the LM
+    head and the LowConfidence commit, on the benchmark's block.  Every layer uses layer 0's
+    weights: generating the stack's 64 GB of distinct weights on the host is far outside a
+    sample budget, while the per-layer arithmetic and shapes are those of the stack.  All of
+    layer 0's experts and the LM head are generated (float64) before timing starts."""
 
     def __init__(self, cfg, R: int):
         import numpy as np
@@ -526,67 +618,52 @@ class OracleSample:
         self.h0 = W.host_h0(cfg, R).astype(np.float64)
         self.masked = W.masked_subset(cfg, R)
         hl = W.HostLayer(cfg, 0)
-        x = oracle.round_bf16(oracle.rmsnorm(self.h0))
-        idx, mass, _, _ = oracle.route(x, hl.Wr, cfg.k)
-        cs = oracle.coreset_select(idx, mass, TOP_P, cfg.P)
-        used = sorted({int(e) for e in idx[cs.survive]})
-        self.cache = {e: hl.expert(e) for e in used}
+        experts = [hl.expert(e) for e in range(cfg.E)]
         sh = hl.shared()
-        self.layer = oracle.MoELayer(Wr=hl.Wr, expert=lambda e: self.cache[e], shared=lambda: sh)
+        self.layer = oracle.MoELayer(Wr=hl.Wr, expert=lambda e: experts[e], shared=lambda: sh)
         self.Wlm = W.host_lm_head(cfg)
 
-    def run(self) -> tuple[float, float]:
+    def run(self) -> float:
+        """Seconds of one full step."""
         import numpy as np
 
         import oracle
         c = self.cfg
         t0 = time.perf_counter()
-        x = oracle.round_bf16(oracle.rmsnorm(self.h0))
-        idx, mass, _, _ = oracle.route(x, self.layer.Wr, c.k)
-        cs = oracle.coreset_select(idx, mass, TOP_P, c.P)
-        h = self.h0 + oracle.moe_ffn(x, self.layer, idx, cs.gate_rr)
-        t_layer = time.perf_counter() - t0
-        t0 = time.perf_counter()
-        hidden = oracle.round_bf16(oracle.rmsnorm(h))
-        conf, choice = oracle.confidence_and_choice(oracle.lm_logits(hidden, self.Wlm))
-        oracle.lowconfidence_commit(conf, choice, np.zeros(len(conf), np.int32), self.masked, THRESHOLD, c.P)
-        t_head = time.perf_counter() - t0
-        return t_layer, t_head
-
-    def step_seconds(self, t_layer: float, t_head: float) -> float:
-        return self.cfg.n_layers * t_layer + t_head
+        oracle.block_decode_step(self.h0, [self.layer] * c.n_layers, self.Wlm, TOP_P, c.k, c.P, THRESHOLD,
+                                 np.zeros(len(self.masked), np.int32), self.masked, bf16=True)
+        return time.perf_counter() - t0
 
     def sample_desc(self) -> str:
-        return (f"layer 0 of {self.cfg.n_layers} over the full block (route, coreset, {len(self.cache)} routed "
-                f"experts + shared, residual, RMSNorm) plus the V={self.cfg.V} LM head and commit; step time = "
-                f"{self.cfg.n_layers} x layer + head")
+        c = self.cfg
+        return (f"the oracle's full block step (oracle.block_decode_step: {c.n_layers} layers of router, coreset, "
+                f"routed + shared SwiGLU experts, residual and RMSNorm over {self.R} x {c.P} tokens, then the "
+                f"V={c.V} LM head and the commit), every layer with layer 0's weights (the 64 GB of distinct "
+                f"weights are not generated on the host); weights generated before timing; numpy float64")
 
 
 def cpu_baseline(cfg, R: int, reps: int = 3) -> dict:
-    s = OracleSample(cfg, R)
-    times = [s.run() for _ in range(reps)]
-    tl = statistics.median(t[0] for t in times)
-    th = statistics.median(t[1] for t in times)
-    return {"value": round(R / s.step_seconds(tl, th), 5), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-            "sample": s.sample_desc() + f"; median of {reps} repetitions",
-            "layer_s": round(tl, 3), "head_s": round(th, 3)}
+    s = OracleStep(cfg, R)
+    secs = [s.run() for _ in range(reps)]
+    return {"value": round(R / statistics.median(secs), 5), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": s.sample_desc() + f"; median of {reps} timed steps",
+            "step_s": round(statistics.median(secs), 3)}
 
 
 def run_reference(args, dist: Dist):
     cfg = workload(args.config)
     R = args.requests
-    s = OracleSample(cfg, R)
+    s = OracleStep(cfg, R)
     for _ in range(args.warmup):
         s.run()
-    secs = [s.step_seconds(*s.run()) for _ in range(args.steps)]
-    total = sum(secs)
+    total = sum(s.run() for _ in range(args.steps))
     value = args.steps * R / total   # one step advances R blocks
     base = {"value": round(value, 5), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-            "sample": s.sample_desc() + "; every step one sample"}
+            "sample": s.sample_desc() + "; every step timed in full"}
     return {"impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": UNIT, "n_gpus": dist.world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * total / args.steps, 2),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": workload_desc(cfg, R), "cpu_baseline": base,
+            "data": "synthetic", "config": workload_desc(cfg, R, args), "cpu_baseline": base,
             "e2e": {"value": round(value, 5), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 

@@ -104,12 +104,17 @@ typedef struct {
     const float* Ssd;
 } moestep_layer;
 
-/* Optional per-layer records written by block_decode_step (any field may be NULL). */
+/* Optional per-layer records written by block_decode_step (any field may be NULL;
+ * x and h must be 16-byte aligned). */
 typedef struct {
     int32_t* n_sel;  /* [n_layers][R]     experts kept by each request's coreset */
     int32_t* idx;    /* [n_layers][T][k]  router top-k */
     float* hidden;   /* [T][H]            fp32 LM-head input (final RMSNorm output) */
     int32_t* sel;    /* [n_layers][R][E]  kept experts in ranking order (first n_sel entries) */
+    void* x;         /* [n_layers][T][H]  each layer's MoE input RMSNorm(h_l) (bf16, or fp32 in
+                      *                   MOESTEP_F32 models), exactly as its router and experts read it */
+    float* h;        /* [n_layers][T][H]  fp32 residual stream h_l entering each layer (h_0 = h_in;
+                      *                   the layer's MoE output is h_{l+1} - h_l, h_L is h_out) */
 } moestep_trace;
 
 /* Bytes of workspace needed by every entry point below for R requests
@@ -266,8 +271,8 @@ long long moestep_launch_count(void);
  * with events (0 turns timing off; enabling clears earlier records);
  * moestep_prof_read() synchronises and returns, per kernel id, the number of
  * timed launches and their summed duration in ms.  Kernel ids: 0 route
- * (with the fused layer heads of moestep_set_route_fusion: the cluster
- * launch that holds the router),
+ * (with moestep_set_route_fusion(2): the cluster launch that holds the
+ * router),
  * 1 coreset, 2 gather, 3 expert FFN (bf16: gate/up + SwiGLU + down in one
  * launch; fp32: gate/up), 4 fp32 expert down, 5 combine/norm, 6 LM head,
  * 7 commit, 8 other.  Not thread-safe. */
@@ -286,17 +291,13 @@ int moestep_set_wait_timeout_ns(unsigned long long ns);
  * layer's combine and RMSNorm, router, top-k, coreset, work plan and token
  * gather):
  *   0  separate launches: combine, router, coreset, gather;
- *   1  one cluster launch for all of them, for a single request: bf16 models
- *      with R == 1, P <= 32, E a multiple of 128 up to 512 and H a multiple of
- *      64 * 32 / (E / 128) up to 4096;
  *   2  (the default) the combine and RMSNorm inside the router's launch (a
  *      cluster of E / 32 CTAs per 8 tokens), then coreset and gather: bf16
  *      activations, at most 256 block tokens, E a multiple of 32 up to 256 and
  *      H a multiple of 512.
- * Shapes a mode does not cover take the separate launches.  Modes 0 and 2
- * compute bit-identical results; mode 1 differs from them only in the
- * summation order of the router logits.  Returns MOESTEP_EINVAL for another
- * mode.  Process-wide; not thread-safe. */
+ * Shapes mode 2 does not cover take the separate launches.  Both modes
+ * compute bit-identical results.  Returns MOESTEP_EINVAL for another mode.
+ * Process-wide; not thread-safe. */
 int moestep_set_route_fusion(int mode);
 /* The mode set by moestep_set_route_fusion. */
 int moestep_route_fusion(void);

@@ -57,7 +57,7 @@ class Layer(ctypes.Structure):
 
 class Trace(ctypes.Structure):
     _fields_ = [("n_sel", ctypes.c_void_p), ("idx", ctypes.c_void_p), ("hidden", ctypes.c_void_p),
-                ("sel", ctypes.c_void_p)]
+                ("sel", ctypes.c_void_p), ("x", ctypes.c_void_p), ("h", ctypes.c_void_p)]
 
 
 _LIB = None
@@ -223,9 +223,11 @@ def block_embed(d: ModelDims, R: int, tokens, masked, emb, pos, mask_id: int, h,
 
 def block_decode_step(d: ModelDims, R: int, layers, Wlm, top_p, threshold, h_in, tokens, masked, choice, conf,
                       accept, n_committed, ws, h_out=None, logit_scale=1.0, trace_n_sel=None, trace_idx=None,
-                      trace_hidden=None, trace_sel=None, stream=None) -> None:
+                      trace_hidden=None, trace_sel=None, trace_x=None, trace_h=None, stream=None) -> None:
+    """One denoising round; the optional trace_* tensors receive the per-layer records of
+    moestep_trace (trace_x: each layer's MoE input, trace_h: the residual entering it)."""
     arr = (Layer * max(1, len(layers)))(*layers)
-    tr = Trace(_p(trace_n_sel), _p(trace_idx), _p(trace_hidden), _p(trace_sel))
+    tr = Trace(_p(trace_n_sel), _p(trace_idx), _p(trace_hidden), _p(trace_sel), _p(trace_x), _p(trace_h))
     _check(lib().block_decode_step(ctypes.byref(d.c()), R, len(layers), arr, _p(Wlm), _p(top_p), float(logit_scale),
                                    float(threshold), _p(h_in), _p(h_out), _p(tokens), _p(masked), _p(choice),
                                    _p(conf), _p(accept), _p(n_committed), ctypes.byref(tr), _p(ws), ws.numel(),
@@ -249,14 +251,13 @@ def read_device_error(ws, stream=None) -> int:
     return w.value
 
 
-SEPARATE_HEAD, CLUSTER_HEAD, FUSED_COMBINE_HEAD = 0, 1, 2
+SEPARATE_HEAD, FUSED_COMBINE_HEAD = 0, 2
 
 
 def set_route_fusion(mode) -> None:
-    """What block_decode_step runs between expert launches: SEPARATE_HEAD (0, also False)
-    the combine / router / coreset / gather launches; CLUSTER_HEAD (1, also True) one cluster
-    launch for all of them (one request); FUSED_COMBINE_HEAD (2, the default) the combine
-    inside the router's launch."""
+    """What block_decode_step runs between expert launches: SEPARATE_HEAD (0) the combine /
+    router / coreset / gather launches; FUSED_COMBINE_HEAD (2, the default) the combine inside
+    the router's launch (bit-identical results)."""
     _check(lib().moestep_set_route_fusion(int(mode)), "moestep_set_route_fusion")
 
 

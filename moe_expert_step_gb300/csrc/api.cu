@@ -24,8 +24,8 @@ namespace {
 thread_local int g_last_cuda = 0;
 unsigned long long g_timeout_ns = 2000000000ull;  // bounded waits inside the tcgen05 kernels
 // What runs between two expert launches of block_decode_step: 0 separate combine /
-// router / coreset / gather launches; 1 one cluster launch for all of them (one
-// request); 2 the combine fused into the router's cluster launch
+// router / coreset / gather launches; 2 the combine fused into the router's
+// cluster launch
 int g_layer_head = 2;
 
 #define MOESTEP_CK(expr)                             \
@@ -321,39 +321,6 @@ int run_coreset(const Ctx& c, int R, const float* top_p, const int32_t* idx, con
         a.pf_next_bytes = 2ll * c.d->E * c.d->H;
     }
     MOESTEP_LAUNCH(1, launch_coreset(a, c.s));
-    return MOESTEP_OK;
-}
-
-// one request: the previous layer's combine (or the input norm), router, top-k,
-// coreset, plan and gather in one cluster launch
-int run_route_plan(const Ctx& c, int mode, const float* h_in, const void* Wr, const void* Wr_next, const float* top_p,
-                   int32_t* idx, int32_t* n_sel, int32_t* sel) {
-    const moestep_dims* d = c.d;
-    const Layout& L = c.L;
-    RoutePlanArgs a{};
-    a.mode = mode;
-    a.y = at<float>(c.ws, L.y);
-    a.slot_of = at<int32_t>(c.ws, L.slot_of);
-    a.slot_sh = at<int32_t>(c.ws, L.slot_sh);
-    a.gate_rr_prev = at<float>(c.ws, L.gaterr);
-    a.has_shared = d->Is > 0;
-    a.h_in = h_in;
-    a.hres = at<float>(c.ws, L.hres);
-    a.x = at<__nv_bfloat16>(c.ws, L.x);
-    a.Wr = static_cast<const __nv_bfloat16*>(Wr);
-    a.wr_next = static_cast<const __nv_bfloat16*>(Wr_next);
-    a.T = L.T;
-    a.H = d->H;
-    a.E = d->E;
-    a.idx = idx;
-    a.mass = at<float>(c.ws, L.mass);
-    a.gate = at<float>(c.ws, L.gate);
-    a.cs = coreset_args(c, 1, top_p, idx, a.mass, n_sel, sel, at<uint8_t>(c.ws, L.survive), at<float>(c.ws, L.gaterr));
-    a.xp = at<uint4>(c.ws, L.xp);
-    a.row_vec = d->H / 8;
-    a.done = at<int>(c.ws, L.done);
-    a.n_done = L.max_chunks;
-    MOESTEP_LAUNCH(0, launch_route_plan(a, c.s));
     return MOESTEP_OK;
 }
 
@@ -787,6 +754,7 @@ int block_decode_step(const moestep_dims* dims, int R, int n_layers, const moest
     if (!aligned16(h_in) || !aligned16(Wlm) || (h_out && !aligned16(h_out))) return MOESTEP_EALIGN;
     for (int l = 0; l < n_layers; ++l) MOESTEP_TRY(layer_ok(dims, &layers[l]));
     if (trace && trace->hidden && !aligned16(trace->hidden)) return MOESTEP_EALIGN;
+    if (trace && ((trace->x && !aligned16(trace->x)) || (trace->h && !aligned16(trace->h)))) return MOESTEP_EALIGN;
     MOESTEP_TRY(check_ws(dims, R, ws, ws_bytes));
     int sms = 0;
     MOESTEP_TRY(device_check(&sms));
@@ -797,36 +765,30 @@ int block_decode_step(const moestep_dims* dims, int R, int n_layers, const moest
     void* x = at<void>(ws, L.x);
     MOESTEP_CK(cudaMemsetAsync(at<char>(ws, L.counters), 0, L.counters_bytes, c.s));
     float* hid_trace = trace ? trace->hidden : nullptr;
-    const bool one_block = g_layer_head == 1 && n_layers > 0 &&
-                           route_plan_eligible(R, dims->dtype, T, dims->H, dims->E, k);
-    const bool fused_head = !one_block && g_layer_head == 2 && n_layers > 0 &&
+    const bool fused_head = g_layer_head == 2 && n_layers > 0 &&
                             route_combine_eligible(act_dtype(dims->dtype), T, dims->H, dims->E, k);
-    if (!one_block && !fused_head)
+    if (!fused_head)
         MOESTEP_LAUNCH(5, launch_combine(2, act_dtype(dims->dtype), T, dims->H, k, nullptr, nullptr, nullptr, nullptr, 0, h_in,
                                          hres, x, n_layers == 0 ? hid_trace : nullptr, nullptr, c.s));
+    const size_t act_row = static_cast<size_t>(dims->H) * (dims->dtype == MOESTEP_F32 ? 4 : 2);
     for (int l = 0; l < n_layers; ++l) {
         int32_t* idx = (trace && trace->idx) ? trace->idx + static_cast<size_t>(l) * T * k : at<int32_t>(ws, L.idx);
         int32_t* nsel = (trace && trace->n_sel) ? trace->n_sel + static_cast<size_t>(l) * R : at<int32_t>(ws, L.nsel);
         int32_t* sel = (trace && trace->sel) ? trace->sel + static_cast<size_t>(l) * R * dims->E : at<int32_t>(ws, L.sel);
         const bool last = l == n_layers - 1;
-        if (one_block) {
-            // the combine of layer l-1 (or the input norm) runs inside the layer-l launch
-            MOESTEP_TRY(run_route_plan(c, l == 0 ? 2 : 1, h_in, layers[l].Wr, last ? nullptr : layers[l + 1].Wr, top_p,
-                                       idx, nsel, sel));
-            MOESTEP_TRY(run_experts(c, R, x, &layers[l], true));
-            if (last)
-                MOESTEP_LAUNCH(5, launch_combine(1, act_dtype(dims->dtype), T, dims->H, k, at<float>(ws, L.y),
-                                                 at<int32_t>(ws, L.slot_of), at<int32_t>(ws, L.slot_sh),
-                                                 at<float>(ws, L.gaterr), dims->Is > 0, nullptr, hres, x, hid_trace,
-                                                 nullptr, c.s));
-            continue;
-        }
         if (fused_head) {
             // the combine of layer l-1 (or the input norm) runs inside the layer-l router launch
             MOESTEP_TRY(run_route_combine(c, l == 0 ? 2 : 1, h_in, layers[l].Wr, idx));
         } else {
             MOESTEP_TRY(run_route(c, T, x, layers[l].Wr, idx, at<float>(ws, L.mass), at<float>(ws, L.gate), nullptr));
         }
+        // layer l's input and residual stream are complete once its router has run
+        if (trace && trace->x)
+            MOESTEP_CK(cudaMemcpyAsync(static_cast<char*>(trace->x) + l * T * act_row, x, T * act_row,
+                                       cudaMemcpyDeviceToDevice, c.s));
+        if (trace && trace->h)
+            MOESTEP_CK(cudaMemcpyAsync(trace->h + static_cast<size_t>(l) * T * dims->H, hres,
+                                       sizeof(float) * T * dims->H, cudaMemcpyDeviceToDevice, c.s));
         MOESTEP_TRY(run_coreset(c, R, top_p, idx, at<float>(ws, L.mass), nsel, sel,
                                 at<uint8_t>(ws, L.survive), at<float>(ws, L.gaterr), layers[l].Wgu,
                                 last ? nullptr : layers[l + 1].Wr));
@@ -967,7 +929,7 @@ int moestep_prof_read(int kernel_id, int* launches, double* total_ms) {
 }
 
 int moestep_set_route_fusion(int mode) {
-    if (mode < 0 || mode > 2) return MOESTEP_EINVAL;
+    if (mode != 0 && mode != 2) return MOESTEP_EINVAL;
     g_layer_head = mode;
     return MOESTEP_OK;
 }

@@ -103,30 +103,6 @@ cudaError_t launch_topk_from_logits(const float* logits, int T, int E, int k, in
 constexpr int kCoresetPrefetchExperts = 32;
 cudaError_t launch_coreset(const CoresetArgs& a, cudaStream_t s);
 int coreset_smem_bytes(int E, int T);
-// One request (T <= 32, bf16): the previous layer's combine + RMSNorm, router,
-// top-k, coreset, plan and gather in one cluster launch.
-struct RoutePlanArgs {
-    int mode;                       // 1: h += experts' outputs (y, slot_of, slot_sh, gate_rr_prev); 2: h = h_in
-    const float* y;
-    const int32_t* slot_of;
-    const int32_t* slot_sh;
-    const float* gate_rr_prev;
-    int has_shared;
-    const float* h_in;
-    float* hres;                    // [T][H] fp32 residual stream (updated)
-    __nv_bfloat16* x;               // [T][H] RMSNorm(h) (written)
-    const __nv_bfloat16* Wr;        // [E][H]
-    const __nv_bfloat16* wr_next;   // next layer's router weights, hinted into L2 (NULL: none)
-    int T, H, E;
-    int32_t* idx;                   // router outputs
-    float* mass;
-    float* gate;
-    CoresetArgs cs;                 // coreset and plan (cs.idx / cs.mass are replaced by shared copies)
-    uint4* xp;                      // gathered rows
-    int row_vec;
-    int* done;                      // expert-launch counters to zero
-    int n_done;
-};
 // The previous layer's combine + RMSNorm and the router (logits, softmax, top-k) in
 // one cluster launch over 8-token tiles (bf16 activations).
 struct RouteCombineArgs {
@@ -148,9 +124,6 @@ struct RouteCombineArgs {
 };
 int route_combine_eligible(int act_dtype, int T, int H, int E, int k);
 cudaError_t launch_route_combine(const RouteCombineArgs& a, cudaStream_t s);
-int route_plan_eligible(int R, int dtype, int T, int H, int E, int k);
-size_t route_plan_smem_bytes(int T, int H, int E, int k);
-cudaError_t launch_route_plan(const RoutePlanArgs& a, cudaStream_t s);
 
 // xp[slot] = x[slot_tok[slot]] for the plan's slots; zeroes done[0..n_done)
 // (the fused expert launch's counters; NULL: none)

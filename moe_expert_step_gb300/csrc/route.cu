@@ -309,7 +309,7 @@ constexpr int kCandCache = 2048;  // candidates of one request kept in shared me
 // work plan over the union of all requests' kept experts.  `masks` (each
 // expert's token bitmask, word-major: word w of every expert side by side,
 // ceil(T/32) x E words) and `sc` are shared-memory scratch.  Used by the
-// coreset kernel (one CTA per request) and by the single-block router.
+// coreset kernel (one CTA per request).
 struct CoresetScratch {  // shared memory of one coreset CTA
     long long A[1024];
     long long cum[1024];
@@ -736,26 +736,8 @@ __global__ void __launch_bounds__(kCoresetThreads) coreset_kernel(CoresetArgs a)
                  *reinterpret_cast<CoresetScratch*>(coreset_smem), stage, nstage);
 }
 
-// ---------------------------------------------------------------------------- single-block layer head
-// One request (T <= 32 tokens), everything between two expert launches in ONE
-// launch of a cluster of kPlanCluster CTAs with no global atomics:
-//  1. combine: the previous layer's expert outputs into the residual stream and
-//     RMSNorm -> x (or, first layer, the norm of the input), the same
-//     arithmetic as the combine kernel; CTA c takes tokens c, c+8, ...;
-//  2. every CTA stages the block's x rows in shared memory;
-//  3. router logits of the CTA's experts [c*E/8, (c+1)*E/8) for every token on
-//     tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate; a warp takes a
-//     16-expert tile over 1/kq of H, the kq partial sums added in a fixed order)
-//     and each logit stored in the shared memory of the CTA that takes the
-//     token's top-k (distributed shared memory);
-//  4. top-k per token (one warp each), copies to CTA 0;
-//  5. coreset and work plan in CTA 0 (the coreset kernel's code);
-//  6. every CTA copies its share of token rows into the gathered activations.
-// L2 hints bring this CTA's router rows in before the previous kernel ends and
-// the next layer's router rows in for the next launch.
+// ---------------------------------------------------------------------------- tensor-core router
 namespace cg = cooperative_groups;
-constexpr int kPlanCluster = 8;
-constexpr int kPlanThreads = 1024;
 
 __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                           uint32_t b0, uint32_t b1) {
@@ -777,9 +759,10 @@ __device__ __forceinline__ uint32_t word8(const uint4& lo, const uint4& hi, int 
 // E / 32), 512 threads.  A CTA computes the logits of 32 experts for 8*NT tokens
 // with mma.sync m16n8k16 (bf16 in, fp32 accumulation): warp w takes the 16-expert
 // half w & 1 and the K eighth w >> 1, reads its weight rows and token rows straight
-// from global memory (16-byte loads, the K permutation of the layer-head kernel
-// above), and the eight K partial sums of every logit are added in K order through
-// shared memory.  The last CTA of a token tile (self-resetting counter) runs the
+// from global memory (16-byte loads; each thread's four K positions per MMA are
+// four consecutive elements, the same permutation for both operands, so its
+// fragments are plain 16-byte loads), and the eight K partial sums of every logit
+// are added in K order through shared memory.  The last CTA of a token tile (self-resetting counter) runs the
 // softmax and top-k of the tile's tokens.
 constexpr int kRouteTcThreads = 512;
 constexpr int kRouteTcExperts = 32;
@@ -986,195 +969,6 @@ __global__ void __launch_bounds__(kRouteTcThreads, 1) route_combine_kernel(Route
     }
 }
 
-struct PlanLayout {
-    int LD;             // staged row length (elements): H + 8, so the 8 rows of an MMA tile hit distinct banks
-    size_t region;      // staged rows / K-split partial sums / coreset scratch (aliased in turn)
-    size_t zs, sidx, smass, masks, cslot, cg, cred, total;
-};
-
-__host__ __device__ inline PlanLayout plan_layout(int T, int H, int E, int k) {
-    PlanLayout L;
-    const int ntt = (T + 7) / 8;
-    const int tpc = (T + kPlanCluster - 1) / kPlanCluster;
-    L.LD = H + 8;
-    size_t region = static_cast<size_t>(ntt) * 8 * L.LD * 2;
-    const size_t part = static_cast<size_t>(32) * 4 * 32 * 4 * sizeof(float);
-    if (part > region) region = part;
-    if (sizeof(CoresetScratch) > region) region = sizeof(CoresetScratch);
-    L.region = (region + 15) / 16 * 16;
-    L.zs = L.region;
-    L.sidx = L.zs + sizeof(float) * tpc * E;
-    L.smass = L.sidx + sizeof(int32_t) * T * k;
-    L.masks = L.smass + sizeof(float) * T * k;
-    L.cslot = L.masks + sizeof(uint32_t) * E * ((T + 31) / 32);
-    L.cg = L.cslot + sizeof(int) * 4 * 33;
-    L.cred = L.cg + sizeof(float) * 4 * 33;
-    L.total = L.cred + sizeof(float) * 4 * 9;
-    return L;
-}
-
-__global__ void __launch_bounds__(kPlanThreads, 1) route_plan_kernel(RoutePlanArgs a) {
-    extern __shared__ __align__(16) uint8_t rp_smem[];
-    cg::cluster_group cluster = cg::this_cluster();
-    const int rank = static_cast<int>(cluster.block_rank());
-    const int CL = kPlanCluster;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = lane >> 2, tig = lane & 3;
-    const int T = a.T, H = a.H, E = a.E, k = a.cs.k;
-    const int EPC = E / CL;                        // experts of this CTA
-    const int ett = EPC / 16, kq = 32 / ett;       // expert tiles, K splits (host: ett divides 32)
-    const int kspan = H / kq;                      // multiple of 128 (host)
-    const int ntt = (T + 7) / 8, TPC = (T + CL - 1) / CL;
-    const PlanLayout L = plan_layout(T, H, E, k);
-    bf16* xs = reinterpret_cast<bf16*>(rp_smem);
-    float* part = reinterpret_cast<float*>(rp_smem);
-    float* zs = reinterpret_cast<float*>(rp_smem + L.zs);
-    int32_t* sidx = reinterpret_cast<int32_t*>(rp_smem + L.sidx);
-    float* smass = reinterpret_cast<float*>(rp_smem + L.smass);
-    uint32_t* masks = reinterpret_cast<uint32_t*>(rp_smem + L.masks);
-    const int grp = threadIdx.x >> 8;  // combine: 4 groups of 256 threads, one token each
-    int* c_slot = reinterpret_cast<int*>(rp_smem + L.cslot) + 33 * grp;
-    float* c_g = reinterpret_cast<float*>(rp_smem + L.cg) + 33 * grp;
-    float* c_red = reinterpret_cast<float*>(rp_smem + L.cred) + 9 * grp;
-    {  // router weights are never written: hint this CTA's rows before waiting
-        const char* w = reinterpret_cast<const char*>(a.Wr + static_cast<size_t>(rank) * EPC * H);
-        const int lines = EPC * H * 2 / 128;
-        for (int l = threadIdx.x; l < lines; l += kPlanThreads) asm volatile("prefetch.global.L2 [%0];" ::"l"(w + 128ll * l));
-    }
-    pdl_trigger();
-    pdl_wait();
-    // 1. combine
-    {
-        const int t = rank + CL * grp;
-        const int tt = (grp < TPC && t < T) ? t : -1;
-        if (a.mode == 1)
-            combine_row<bf16, 1>(tt, H, k, a.y, a.slot_of, a.slot_sh, a.gate_rr_prev, a.has_shared, nullptr, a.hres,
-                                 a.x, nullptr, nullptr, c_slot, c_g, c_red);
-        else
-            combine_row<bf16, 2>(tt, H, k, nullptr, nullptr, nullptr, nullptr, 0, a.h_in, a.hres, a.x, nullptr,
-                                 nullptr, c_slot, c_g, c_red);
-    }
-    cluster.sync();  // every token's x row is in global memory (and every CTA has started)
-    // 2. stage x: row t at t*LD, rows T .. 8*ntt-1 zero
-    {
-        const int vpr = H / 8;
-        const int nvec = ntt * 8 * vpr;
-        const uint4* xg = reinterpret_cast<const uint4*>(a.x);
-        for (int i0 = threadIdx.x; i0 < nvec; i0 += 8 * kPlanThreads) {
-            uint4 v[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int i = i0 + u * kPlanThreads;
-                const int row = i / vpr;
-                v[u] = (i < nvec && row < T) ? __ldcg(xg + i) : make_uint4(0, 0, 0, 0);
-            }
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int i = i0 + u * kPlanThreads;
-                if (i < nvec) {
-                    const int row = i / vpr, c = i - row * vpr;
-                    *reinterpret_cast<uint4*>(xs + static_cast<size_t>(row) * L.LD + c * 8) = v[u];
-                }
-            }
-        }
-    }
-    __syncthreads();
-    // 3. logits.  Thread (g, tig)'s 4 K positions of MMA j in a 64-wide chunk are
-    // elements 16*tig + 4j .. +3 (one permutation of K for A and B, so the sums are
-    // unchanged) and its fragments are plain 16-byte loads.
-    {
-        const int et = warp / kq, q = warp % kq;
-        float d[4][4];
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-            for (int r = 0; r < 4; ++r) d[nt][r] = 0.f;
-        const bf16* w0 = a.Wr + static_cast<size_t>(rank * EPC + et * 16 + g) * H;
-        const bf16* w1 = w0 + static_cast<size_t>(8) * H;
-        for (int h0 = q * kspan; h0 < (q + 1) * kspan; h0 += 64) {
-            const int hb = h0 + 16 * tig;
-            const uint4 a00 = __ldg(reinterpret_cast<const uint4*>(w0 + hb));
-            const uint4 a01 = __ldg(reinterpret_cast<const uint4*>(w0 + hb + 8));
-            const uint4 a10 = __ldg(reinterpret_cast<const uint4*>(w1 + hb));
-            const uint4 a11 = __ldg(reinterpret_cast<const uint4*>(w1 + hb + 8));
-#pragma unroll
-            for (int nt = 0; nt < 4; ++nt) {
-                if (nt < ntt) {
-                    const bf16* xr = xs + static_cast<size_t>(nt * 8 + g) * L.LD + hb;
-                    const uint4 b0 = *reinterpret_cast<const uint4*>(xr);
-                    const uint4 b1 = *reinterpret_cast<const uint4*>(xr + 8);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        mma_16816(d[nt], word8(a00, a01, 2 * j), word8(a10, a11, 2 * j), word8(a00, a01, 2 * j + 1),
-                                  word8(a10, a11, 2 * j + 1), word8(b0, b1, 2 * j), word8(b0, b1, 2 * j + 1));
-                }
-            }
-        }
-        __syncthreads();  // the staged rows are dead: the partial sums take their place
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
-            if (nt < ntt)
-#pragma unroll
-                for (int r = 0; r < 4; ++r) part[((warp * 4 + nt) * 32 + lane) * 4 + r] = d[nt][r];
-    }
-    __syncthreads();
-    // 4. add the K splits in split order (element r of lane ln is expert g + 8*(r>=2)
-    // and token 2*tig + (r&1) of the tile) and store the logit with the CTA that
-    // takes the token's top-k
-    for (int i = threadIdx.x; i < ett * ntt * 128; i += kPlanThreads) {
-        const int tile = i >> 7, ln = (i >> 2) & 31, r = i & 3;
-        const int et = tile / ntt, nt = tile % ntt;
-        float v = 0.f;
-        for (int q = 0; q < kq; ++q) v += part[(((et * kq + q) * 4 + nt) * 32 + ln) * 4 + r];
-        const int el = et * 16 + (ln >> 2) + (r >= 2 ? 8 : 0);
-        const int t = nt * 8 + 2 * (ln & 3) + (r & 1);
-        if (t < T) cluster.map_shared_rank(zs, t % CL)[(t / CL) * E + rank * EPC + el] = v;
-    }
-    if (a.wr_next != nullptr) {  // the next layer's router rows, for the next launch
-        const char* w = reinterpret_cast<const char*>(a.wr_next + static_cast<size_t>(rank) * EPC * H);
-        const int lines = EPC * H * 2 / 128;
-        for (int l = threadIdx.x; l < lines; l += kPlanThreads) asm volatile("prefetch.global.L2 [%0];" ::"l"(w + 128ll * l));
-    }
-    cluster.sync();  // every token's logits are with the CTA that takes its top-k
-    {
-        const int t = rank + CL * warp;
-        if (warp < TPC && t < T)
-            topk_one_token(zs + warp * E, E, k, t, a.idx, a.mass, a.gate, cluster.map_shared_rank(sidx, 0),
-                           cluster.map_shared_rank(smass, 0));
-    }
-    cluster.sync();  // CTA 0 holds every token's experts and routing mass
-    if (rank == 0) {
-        CoresetArgs cs = a.cs;
-        cs.idx = sidx;
-        cs.mass = smass;
-        coreset_body(cs, 0, 1, masks, *reinterpret_cast<CoresetScratch*>(rp_smem));
-        for (int i = threadIdx.x; i < a.n_done; i += kPlanThreads) a.done[i] = 0;
-        __threadfence();
-    }
-    cluster.sync();  // the plan is written
-    // 6. gathered rows: one warp per slot row, 8 16-byte vectors in flight per lane
-    const int n_slots = __ldcg(&a.cs.plan[2]);
-    const uint4* xg = reinterpret_cast<const uint4*>(a.x);
-    for (int sl = rank * (kPlanThreads / 32) + warp; sl < n_slots; sl += CL * (kPlanThreads / 32)) {
-        const int t = __ldcg(&a.cs.slot_tok[sl]);
-        const uint4* src = xg + static_cast<size_t>(t) * a.row_vec;
-        uint4* dst = a.xp + static_cast<size_t>(sl) * a.row_vec;
-        for (int c0 = 0; c0 < a.row_vec; c0 += 256) {
-            uint4 v[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int c = c0 + u * 32 + lane;
-                if (c < a.row_vec) v[u] = __ldcg(src + c);
-            }
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int c = c0 + u * 32 + lane;
-                if (c < a.row_vec) dst[c] = v[u];
-            }
-        }
-    }
-}
-
 // 8 bf16 -> 8 f16 (round to nearest even; exact unless below f16's normal range)
 __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
     uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -1304,39 +1098,6 @@ cudaError_t launch_route_combine(const RouteCombineArgs& a, cudaStream_t s) {
     cfg.attrs = attr;
     cfg.numAttrs = g_launch_pdl ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, route_combine_kernel, a);
-}
-
-int route_plan_eligible(int R, int dtype, int T, int H, int E, int k) {
-    if (R != 1 || dtype != MOESTEP_BF16 || T < 1 || T > 32 || k > 32 || H > 4096) return 0;
-    if (E % (16 * kPlanCluster) != 0 || E > 512) return 0;
-    const int ett = E / kPlanCluster / 16;
-    if (32 % ett != 0) return 0;
-    if (H % (64 * (32 / ett)) != 0) return 0;
-    return plan_layout(T, H, E, k).total <= 227 * 1024 ? 1 : 0;
-}
-
-size_t route_plan_smem_bytes(int T, int H, int E, int k) { return plan_layout(T, H, E, k).total; }
-
-cudaError_t launch_route_plan(const RoutePlanArgs& a, cudaStream_t s) {
-    const size_t smem = route_plan_smem_bytes(a.T, a.H, a.E, a.cs.k);
-    static int done[64] = {};
-    cudaError_t e = ensure_smem(route_plan_kernel, smem, done);
-    if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(kPlanCluster);
-    cfg.blockDim = dim3(kPlanThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kPlanCluster;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = g_launch_pdl ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, route_plan_kernel, a);
 }
 
 }  // namespace moestep

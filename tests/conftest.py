@@ -19,3 +19,19 @@ def cuda_ok():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     return True
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Report the top-k pick pairs that GPU tests saw in the opposite order to the oracle's
+    (their fp64 logit gap against the fp32 error window that allowed the swap)."""
+    try:
+        from tests.helpers import SWAP_LOG
+    except ImportError:
+        return
+    if SWAP_LOG:
+        gaps = sorted(SWAP_LOG, key=lambda gw: -gw[0])
+        terminalreporter.write_line(f"top-k order swaps: {len(gaps)}; largest fp64 gap {gaps[0][0]:.3e} "
+                                    f"(window {gaps[0][1]:.3e}); largest gap/window "
+                                    f"{max(g / w for g, w in gaps):.3f}")
+    else:
+        terminalreporter.write_line("top-k order swaps: none")

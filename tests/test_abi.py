@@ -152,9 +152,10 @@ def test_loop_and_fusion_arguments(L):
     assert rc == ms.EWORKSPACE
     prev = L.moestep_route_fusion()
     assert prev == ms.FUSED_COMBINE_HEAD                       # the default
-    for mode in (ms.CLUSTER_HEAD, ms.SEPARATE_HEAD, ms.FUSED_COMBINE_HEAD):
+    for mode in (ms.SEPARATE_HEAD, ms.FUSED_COMBINE_HEAD):
         assert L.moestep_set_route_fusion(mode) == ms.OK and L.moestep_route_fusion() == mode
-    assert L.moestep_set_route_fusion(3) == ms.EINVAL and L.moestep_set_route_fusion(-1) == ms.EINVAL
+    for bad in (1, 3, -1):
+        assert L.moestep_set_route_fusion(bad) == ms.EINVAL
     assert L.moestep_route_fusion() == ms.FUSED_COMBINE_HEAD
 
 

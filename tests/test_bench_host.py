@@ -94,4 +94,4 @@ def test_bench_arguments_parse(argv, monkeypatch):
     import bench
     monkeypatch.setattr(sys, "argv", ["bench.py"] + argv)
     a = bench.parse()
-    assert a.steps == 3 and a.warmup == 3 and a.layer_head is None and not a.route_fusion
+    assert a.steps == 3 and a.warmup == 3 and a.layer_head is None

@@ -117,19 +117,23 @@ def host_rounds(cfg, layers, Wlm_d, emb_d, pos_d, top_p, tokens0, masked0, R=1, 
     return np_(tokens), rounds
 
 
-def test_clover_loop_equals_host_driven_rounds():
+@pytest.mark.parametrize("R", [1, 4])
+def test_clover_loop_equals_host_driven_rounds(R):
+    """R = 4: four blocks decoded together, each with its own coreset and its own rounds
+    (the loop runs until every request's block is resolved)."""
     cfg = replace(W.LAYER, name="clover_2layer", n_layers=2)
     layers = [clayer(W.device_layer(cfg, l)) for l in range(cfg.n_layers)]
     Wlm_d = W.device_lm_head(cfg)
     # synthetic embedding: N(0, 1) bf16 tables from the generator
     emb_d = W.to_device(W.host_activations(cfg, "emb", cfg.V), "bf16")
     pos_d = W.to_device(W.host_activations(cfg, "pos", cfg.P), "bf16")
-    masked0 = W.masked_subset(cfg, 1)
-    tokens0 = np.where(masked0, 0, np.arange(cfg.P) + 7)
-    h_tok, h_rounds = host_rounds(cfg, layers, Wlm_d, emb_d, pos_d, 0.9, tokens0, masked0, scale=24.0)
-    ws = ms.workspace(dims_of(cfg), 1)
+    masked0 = W.masked_subset(cfg, R)
+    tokens0 = np.where(masked0, 0, np.arange(R * cfg.P) % cfg.P + 7)
+    h_tok, h_rounds = host_rounds(cfg, layers, Wlm_d, emb_d, pos_d, 0.9, tokens0, masked0, R=R, scale=24.0)
+    ws = ms.workspace(dims_of(cfg), R)
     for _ in range(2):                       # the second call reuses the cached graph
-        tok, msk, rounds = run_loop(cfg, layers, Wlm_d, emb_d, pos_d, 0.9, tokens0, masked0, scale=24.0, ws=ws)
+        tok, msk, rounds = run_loop(cfg, layers, Wlm_d, emb_d, pos_d, 0.9, tokens0, masked0, scale=24.0, R=R,
+                                    ws=ws)
         assert rounds == h_rounds and not msk.any()
         np.testing.assert_array_equal(tok, h_tok)
     np.testing.assert_array_equal(tok[~masked0], tokens0[~masked0])     # committed tokens never change

@@ -12,7 +12,8 @@ import moe_expert_step_gb300 as ms
 import oracle
 import synth
 from synth import workloads as W
-from tests.helpers import aligned, coreset_margin, match_topk, max_rel, np_, t, topk_margins
+from tests.helpers import (aligned, coreset_margin, dot_error_bound, match_topk, max_rel, np_, router_kind, t,
+                           topk_margin_ok)
 
 pytestmark = pytest.mark.gpu
 
@@ -72,10 +73,10 @@ def test_route_matches_oracle(cfg_name, T):
     xo = synth.as_f64(xa, cfg.dtype)
     oi, om, og, oz = oracle.route(xo, ol.Wr, cfg.k)
     assert max_rel(logits, oz) < 1e-5
-    margins = topk_margins(oz, cfg.k)
-    ok = margins > 1e-4
-    assert ok.mean() > 0.9
-    perm = match_topk(idx[ok], oi[ok], oz[ok], cfg.k)
+    eps = dot_error_bound(xo, ol.Wr, router_kind(cfg.H, cfg.E, cfg.dtype))
+    ok = topk_margin_ok(oz, eps, cfg.k)
+    assert ok.mean() > 0.99
+    perm = match_topk(idx[ok], oi[ok], oz[ok], cfg.k, eps[ok])
     assert max_rel(aligned(mass[ok], perm), om[ok]) < 1e-4 and max_rel(aligned(gate[ok], perm), og[ok]) < 1e-4
     assert max_rel(mass, om) < 1e-4 and max_rel(gate, og) < 1e-4
 
@@ -171,9 +172,11 @@ def test_route_then_coreset_c2(tp):
     xa = W.host_activations(cfg, "x_layer", 32)
     idx, mass, gate, logits = route_gpu(d, W.to_device(xa, "bf16"), lay["Wr"])
     n_sel, sel, survive, gate_rr, err = coreset_gpu(d, 1, [tp], idx, mass)
-    oi, om, _, oz = oracle.route(synth.as_f64(xa, "bf16"), W.HostLayer(cfg, 0).Wr, cfg.k)
-    assert (topk_margins(oz, cfg.k) > 1e-4).all()
-    perm = match_topk(idx, oi, oz, cfg.k)
+    xo, Wr = synth.as_f64(xa, "bf16"), W.HostLayer(cfg, 0).Wr
+    oi, om, _, oz = oracle.route(xo, Wr, cfg.k)
+    eps = dot_error_bound(xo, Wr, "tc")
+    assert topk_margin_ok(oz, eps, cfg.k).all()
+    perm = match_topk(idx, oi, oz, cfg.k, eps)
     cs = oracle.coreset_select(oi, om, tp, 32)
     assert coreset_margin(cs) > 1e-5
     assert list(sel[0, :n_sel[0]]) == cs.sel[0]
