@@ -286,7 +286,6 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
 
 // ---------------------------------------------------------------------------- coreset
 constexpr int kCoresetThreads = 1024;
-constexpr int kHelperThreads = 256;  // helper CTAs of a layer whose coreset ran in the router launch
 
 // Inclusive prefix sum over one value per thread of a block of whole warps (up to
 // 1024 threads).  warp_tot (32 entries) ends with the running totals per warp; its
@@ -1142,13 +1141,8 @@ cudaError_t launch_coreset(const CoresetArgs& a, cudaStream_t s) {
     static int done[64] = {};
     cudaError_t e = ensure_smem(coreset_kernel, smem, done);
     if (e != cudaSuccess) return e;
-    if (a.helpers_only) {
-        // 256 threads and only the expert bitmask in shared memory, so a helper fits on an SM
-        // beside a CTA of the expert launch, which can then start (barriers, tensor memory)
-        // while the helpers still gather
-        const size_t hs = static_cast<size_t>((a.E + 31) / 32) * 4;
-        return launch_pdl(coreset_kernel, dim3(a.pf_ctas), dim3(kHelperThreads), hs, s, a);
-    }
+    if (a.helpers_only)
+        return launch_pdl(coreset_kernel, dim3(a.pf_ctas), dim3(kCoresetThreads), smem, s, a);
     const int helpers = (a.pf_base != nullptr && a.pf_experts > 0) ? a.pf_ctas : 0;
     return launch_pdl(coreset_kernel, dim3(a.R + helpers), dim3(kCoresetThreads), smem, s, a);
 }
