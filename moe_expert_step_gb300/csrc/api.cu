@@ -80,9 +80,7 @@ Layout make_layout(const moestep_dims& d, int R) {
         return at;
     };
     L.hdr = take(256);  // int[0]: error word, int[8..15]: where a wait timed out, int[32..34]: expert work plan
-    // router groups, coreset plan, commit per request, the router launch's coreset: CTAs per
-    // request, CTAs of the launch and the plan flag (zeroed at the start of every call)
-    L.counters_bytes = sizeof(int) * (L.route_groups + 1 + R + R + 2);
+    L.counters_bytes = sizeof(int) * (L.route_groups + 1 + R);  // router groups, coreset, commit per request
     L.counters = take(L.counters_bytes);
     L.logits = take(sizeof(float) * T * d.E);
     L.idx = take(sizeof(int32_t) * T * d.k);
@@ -326,15 +324,8 @@ int run_coreset(const Ctx& c, int R, const float* top_p, const int32_t* idx, con
     return MOESTEP_OK;
 }
 
-// the router launch's coreset counters (after the commit counters; zeroed with the others)
-int* req_done_ctr(const Ctx& c, int R) { return at<int>(c.ws, c.L.counters) + c.L.route_groups + 1 + R; }
-int* route_done_ctr(const Ctx& c, int R) { return req_done_ctr(c, R) + R; }
-int* plan_flag_ctr(const Ctx& c, int R) { return route_done_ctr(c, R) + 1; }
-
-// the previous layer's combine (mode 1) or the input norm (mode 2), then the router; with
-// cs, also layer `layer`'s coreset and plan in the same launch
-int run_route_combine(const Ctx& c, int mode, const float* h_in, const void* Wr, int32_t* idx,
-                      const CoresetArgs* cs = nullptr, int layer = 0) {
+// the previous layer's combine (mode 1) or the input norm (mode 2), then the router
+int run_route_combine(const Ctx& c, int mode, const float* h_in, const void* Wr, int32_t* idx) {
     const moestep_dims* d = c.d;
     const Layout& L = c.L;
     RouteCombineArgs a{};
@@ -356,49 +347,7 @@ int run_route_combine(const Ctx& c, int mode, const float* h_in, const void* Wr,
     a.idx = idx;
     a.mass = at<float>(c.ws, L.mass);
     a.gate = at<float>(c.ws, L.gate);
-    if (cs != nullptr) {
-        a.with_coreset = 1;
-        a.cs = *cs;
-        a.req_done = req_done_ctr(c, cs->R);
-        a.route_done = route_done_ctr(c, cs->R);
-        a.plan_flag = plan_flag_ctr(c, cs->R);
-        a.plan_value = layer + 1;
-        a.ctas_per_req = d->E / 32 * (d->P / 8);
-    }
     MOESTEP_LAUNCH(0, launch_route_combine(a, c.s));
-    return MOESTEP_OK;
-}
-
-// Helper launch of a layer whose coreset ran in the router launch: L2 hints once every top-k
-// is written, then the token gather once the plan is (flags, bounded waits).
-int run_helpers(const Ctx& c, int R, const int32_t* idx, const void* x, const void* Wgu, const void* Wr_next,
-                int layer) {
-    const moestep_dims* d = c.d;
-    const Layout& L = c.L;
-    CoresetArgs a = coreset_args(c, R, nullptr, idx, nullptr, nullptr, nullptr, nullptr, nullptr);
-    a.helpers_only = 1;
-    a.pf_base = static_cast<const char*>(Wgu);
-    a.pf_stride = 2ll * d->I * d->H * (d->dtype == MOESTEP_FP8 ? 1 : 2);
-    a.pf_experts = kCoresetPrefetchExperts;
-    // one helper per SM that the router launch leaves free, so every helper can be resident at once
-    // (a helper that started late, on the SM of the router CTA that ran the coreset, would hold up
-    // the launch's completion and with it the expert launch)
-    const int route_ctas = d->E / 32 * ((L.T + 7) / 8);
-    a.pf_ctas = c.sms - route_ctas > 16 ? c.sms - route_ctas : 16;
-    a.pf_next = static_cast<const char*>(Wr_next);
-    a.pf_next_bytes = 2ll * d->E * d->H;
-    a.route_done = route_done_ctr(c, R);
-    a.route_target = (layer + 1) * (d->E / 32) * ((L.T + 7) / 8);
-    a.plan_flag = plan_flag_ctr(c, R);
-    a.plan_value = layer + 1;
-    a.gx = static_cast<const uint4*>(x);
-    a.gxp = at<uint4>(c.ws, L.xp);
-    a.row_vec = d->H * 2 / 16;
-    a.to_f16 = d->dtype == MOESTEP_FP8;
-    a.done = at<int>(c.ws, L.done);
-    a.n_done = L.max_chunks;
-    a.timeout_ns = g_timeout_ns;
-    MOESTEP_LAUNCH(1, launch_coreset(a, c.s));
     return MOESTEP_OK;
 }
 
@@ -818,8 +767,6 @@ int block_decode_step(const moestep_dims* dims, int R, int n_layers, const moest
     float* hid_trace = trace ? trace->hidden : nullptr;
     const bool fused_head = g_layer_head == 2 && n_layers > 0 &&
                             route_combine_eligible(act_dtype(dims->dtype), T, dims->H, dims->E, k);
-    const bool fused_cs = fused_head && dims->dtype != MOESTEP_F32 && sms > 0 &&
-                          route_combine_coreset_eligible(act_dtype(dims->dtype), R, dims->P, dims->H, dims->E, k);
     if (!fused_head)
         MOESTEP_LAUNCH(5, launch_combine(2, act_dtype(dims->dtype), T, dims->H, k, nullptr, nullptr, nullptr, nullptr, 0, h_in,
                                          hres, x, n_layers == 0 ? hid_trace : nullptr, nullptr, c.s));
@@ -829,13 +776,7 @@ int block_decode_step(const moestep_dims* dims, int R, int n_layers, const moest
         int32_t* nsel = (trace && trace->n_sel) ? trace->n_sel + static_cast<size_t>(l) * R : at<int32_t>(ws, L.nsel);
         int32_t* sel = (trace && trace->sel) ? trace->sel + static_cast<size_t>(l) * R * dims->E : at<int32_t>(ws, L.sel);
         const bool last = l == n_layers - 1;
-        if (fused_cs) {
-            // the combine of layer l-1 (or the input norm), the router and layer l's coreset and
-            // plan in one launch; the helper launch hints weights into L2 and gathers the rows
-            CoresetArgs cs = coreset_args(c, R, top_p, idx, at<float>(ws, L.mass), nsel, sel,
-                                          at<uint8_t>(ws, L.survive), at<float>(ws, L.gaterr));
-            MOESTEP_TRY(run_route_combine(c, l == 0 ? 2 : 1, h_in, layers[l].Wr, idx, &cs, l));
-        } else if (fused_head) {
+        if (fused_head) {
             // the combine of layer l-1 (or the input norm) runs inside the layer-l router launch
             MOESTEP_TRY(run_route_combine(c, l == 0 ? 2 : 1, h_in, layers[l].Wr, idx));
         } else {
@@ -848,15 +789,10 @@ int block_decode_step(const moestep_dims* dims, int R, int n_layers, const moest
         if (trace && trace->h)
             MOESTEP_CK(cudaMemcpyAsync(trace->h + static_cast<size_t>(l) * T * dims->H, hres,
                                        sizeof(float) * T * dims->H, cudaMemcpyDeviceToDevice, c.s));
-        if (fused_cs) {
-            MOESTEP_TRY(run_helpers(c, R, idx, x, layers[l].Wgu, last ? nullptr : layers[l + 1].Wr, l));
-            MOESTEP_TRY(run_experts(c, R, x, &layers[l], true));
-        } else {
-            MOESTEP_TRY(run_coreset(c, R, top_p, idx, at<float>(ws, L.mass), nsel, sel,
-                                    at<uint8_t>(ws, L.survive), at<float>(ws, L.gaterr), layers[l].Wgu,
-                                    last ? nullptr : layers[l + 1].Wr));
-            MOESTEP_TRY(run_experts(c, R, x, &layers[l]));
-        }
+        MOESTEP_TRY(run_coreset(c, R, top_p, idx, at<float>(ws, L.mass), nsel, sel,
+                                at<uint8_t>(ws, L.survive), at<float>(ws, L.gaterr), layers[l].Wgu,
+                                last ? nullptr : layers[l + 1].Wr));
+        MOESTEP_TRY(run_experts(c, R, x, &layers[l]));
         if (!fused_head || last)
             MOESTEP_LAUNCH(5, launch_combine(1, act_dtype(dims->dtype), T, dims->H, k, at<float>(ws, L.y),
                                              at<int32_t>(ws, L.slot_of), at<int32_t>(ws, L.slot_sh),

@@ -93,24 +93,6 @@ struct CoresetArgs {
     int pf_ctas;
     const char* pf_next;      // also hinted by those CTAs: pf_next_bytes from here (the next layer's router)
     long long pf_next_bytes;
-    // helpers only (the coreset itself runs in the router launch, see RouteCombineArgs): every CTA
-    // of the launch is a helper; it waits (bounded, no programmatic-launch wait) until
-    // *route_done >= route_target (every router CTA wrote its top-k), hints as above, waits until
-    // *plan_flag >= plan_value (the plan is written), then copies the plan's token rows
-    // gxp[slot] = gx[slot_tok[slot]] (row_vec 16-byte vectors a row; to_f16: bf16 rows stored as
-    // f16) and CTA 0 zeroes done[0 .. n_done)
-    int helpers_only;
-    const int* route_done;
-    int route_target;
-    const int* plan_flag;
-    int plan_value;
-    const uint4* gx;
-    uint4* gxp;
-    int row_vec;
-    int to_f16;
-    int* done;
-    int n_done;
-    unsigned long long timeout_ns;
 };
 
 cudaError_t launch_route(int dtype, const void* x, const void* Wr, int T, int H, int E, int k, float* logits,
@@ -139,21 +121,8 @@ struct RouteCombineArgs {
     int32_t* idx;
     float* mass;
     float* gate;
-    // optional coreset in the same launch (with_coreset): every CTA counts its top-k done in
-    // *route_done and in req_done[request]; the last CTA of a request (ctas_per_req of them, P % 8
-    // == 0) runs the request's coreset (cs; the last request's CTA also the plan), and the CTA that
-    // wrote the plan release-stores plan_value into *plan_flag
-    int with_coreset;
-    CoresetArgs cs;
-    int* route_done;
-    int* req_done;
-    int ctas_per_req;
-    int* plan_flag;
-    int plan_value;
 };
 int route_combine_eligible(int act_dtype, int T, int H, int E, int k);
-// the coreset can join the router launch: route_combine_eligible and whole 8-token tiles per request
-int route_combine_coreset_eligible(int act_dtype, int R, int P, int H, int E, int k);
 cudaError_t launch_route_combine(const RouteCombineArgs& a, cudaStream_t s);
 
 // xp[slot] = x[slot_tok[slot]] for the plan's slots; zeroes done[0..n_done)

@@ -272,27 +272,13 @@ __global__ void __launch_bounds__(256) topk_from_logits_kernel(const float* __re
     topk_one_token(s, E, k, t, idx, mass, gate);
 }
 
-// 8 bf16 -> 8 f16 (round to nearest even; exact unless below f16's normal range)
-__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
-    uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
-        const __half2 h = __floats2half2_rn(f.x, f.y);
-        w[i] = *reinterpret_cast<const uint32_t*>(&h);
-    }
-    return make_uint4(w[0], w[1], w[2], w[3]);
-}
-
 // ---------------------------------------------------------------------------- coreset
 constexpr int kCoresetThreads = 1024;
 
-// Inclusive prefix sum over one value per thread of a block of whole warps (up to
-// 1024 threads).  warp_tot (32 entries) ends with the running totals per warp; its
-// last entry, warp_tot[31], is the block total whatever the block size.
+// Inclusive prefix sum over one value per thread of a 1024-thread block.
 template <typename V>
 __device__ V block_inclusive_scan(V v, V* warp_tot) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const V n = __shfl_up_sync(0xffffffffu, v, o);
@@ -301,7 +287,7 @@ __device__ V block_inclusive_scan(V v, V* warp_tot) {
     if (lane == 31) warp_tot[warp] = v;
     __syncthreads();
     if (warp == 0) {
-        V w = lane < nw ? warp_tot[lane] : V(0);
+        V w = warp_tot[lane];
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const V n = __shfl_up_sync(0xffffffffu, w, o);
@@ -354,10 +340,8 @@ __host__ __device__ inline int coreset_stage_slots(int E, int T, int k) {
     return (slots <= kSlotStage && bytes <= 226 * 1024) ? static_cast<int>(slots) : 0;
 }
 
-// stage: shared memory for coreset_stage_slots(E, T, k) slots (2 ints each), or NULL.
-// Any block of whole warps with at least E and at least 32 threads; returns true in the
-// CTA that wrote the work plan (the last request's, or the only one).
-__device__ bool coreset_body(const CoresetArgs& a, int r, int nreq, uint32_t* masks, CoresetScratch& sc,
+// stage: shared memory for coreset_stage_slots(E, T, k) slots (2 ints each), or NULL
+__device__ void coreset_body(const CoresetArgs& a, int r, int nreq, uint32_t* masks, CoresetScratch& sc,
                              int* stage = nullptr, int nstage = 0) {
     long long* A = sc.A;
     long long* cum = sc.cum;
@@ -390,9 +374,8 @@ __device__ bool coreset_body(const CoresetArgs& a, int r, int nreq, uint32_t* ma
         for (int i = tid; i < E * TWl; i += blockDim.x) masks[i] = 0u;
     __syncthreads();
     for (int c = tid; c < nc; c += blockDim.x) {
-        // L2 loads: in the router launch these were just written by the request's other CTAs
-        const int e = __ldcg(&a.idx[base + c]);
-        const float ms = __ldcg(&a.mass[base + c]);
+        const int e = a.idx[base + c];
+        const float ms = a.mass[base + c];
         if (cached) {
             cidx[c] = e;
             cmass[c] = ms;
@@ -428,7 +411,7 @@ __device__ bool coreset_body(const CoresetArgs& a, int r, int nreq, uint32_t* ma
     // on the full aggregate and the id.  All sums are >= 0.
     {
         int parts = 1;
-        while (parts < 32 && parts * 2 * nC <= static_cast<int>(blockDim.x)) parts *= 2;
+        while (parts < 32 && parts * 2 * nC <= kCoresetThreads) parts *= 2;
         const int p = tid / parts, part = tid % parts;
         const bool mine_ok = p < nC;
         const uint32_t mh = mine_ok ? sc.khi[p] : 0u;
@@ -512,8 +495,8 @@ __device__ bool coreset_body(const CoresetArgs& a, int r, int nreq, uint32_t* ma
                 for (int q = 0; q < 8; ++q) {
                     const int c = c0 + j0 + q;
                     const bool in = j0 + q < k;
-                    ev[q] = in ? (cached ? cidx[c] : __ldcg(&a.idx[base + c])) : -1;
-                    mv[q] = in ? (cached ? cmass[c] : __ldcg(&a.mass[base + c])) : 0.f;
+                    ev[q] = in ? (cached ? cidx[c] : a.idx[base + c]) : -1;
+                    mv[q] = in ? (cached ? cmass[c] : a.mass[base + c]) : 0.f;
                 }
     #pragma unroll
                 for (int q = 0; q < 8; ++q)
@@ -526,8 +509,8 @@ __device__ bool coreset_body(const CoresetArgs& a, int r, int nreq, uint32_t* ma
                 for (int q = 0; q < 8; ++q) {
                     const int c = c0 + j0 + q;
                     const bool in = j0 + q < k;
-                    ev[q] = in ? (cached ? cidx[c] : __ldcg(&a.idx[base + c])) : -1;
-                    mv[q] = in ? (cached ? cmass[c] : __ldcg(&a.mass[base + c])) : 0.f;
+                    ev[q] = in ? (cached ? cidx[c] : a.idx[base + c]) : -1;
+                    mv[q] = in ? (cached ? cmass[c] : a.mass[base + c]) : 0.f;
                 }
     #pragma unroll
                 for (int q = 0; q < 8; ++q) {
@@ -552,7 +535,7 @@ __device__ bool coreset_body(const CoresetArgs& a, int r, int nreq, uint32_t* ma
             if (s_last) *a.counter = 0;
         }
         __syncthreads();
-        if (!s_last) return false;
+        if (!s_last) return;
         __threadfence();
     } else {
         if (!local) __threadfence();
@@ -619,7 +602,7 @@ __device__ bool coreset_body(const CoresetArgs& a, int r, int nreq, uint32_t* ma
         for (int i = 0; i < my_nch; ++i)
             a.chunks[chunk_base + i] = make_int4(tid, slot_base + i * a.nch, min(a.nch, my_cnt - i * a.nch), 0);
     }
-    if (tid == static_cast<int>(blockDim.x) - 1) {
+    if (tid == kCoresetThreads - 1) {
         s_nr = slot_end;
         s_nrc = chunk_end;
     }
@@ -680,7 +663,6 @@ __device__ bool coreset_body(const CoresetArgs& a, int r, int nreq, uint32_t* ma
             a.slot_exp[i] = stage[nstage + i];
         }
     }
-    return true;
 }
 
 // L2 hints by the extra CTAs of the coreset launch: the union of the experts the
@@ -688,8 +670,7 @@ __device__ bool coreset_body(const CoresetArgs& a, int r, int nreq, uint32_t* ma
 // expert launch takes the kept experts in id order, so these are the first it
 // streams; most candidates are kept).  Hints only: nothing is written.
 constexpr int kMaxPrefetchExperts = 64;
-// first: index of the first hinting CTA of the launch
-__device__ void coreset_prefetch(const CoresetArgs& a, uint32_t* bits, int first) {
+__device__ void coreset_prefetch(const CoresetArgs& a, uint32_t* bits) {
     __shared__ int s_pe[kMaxPrefetchExperts];
     __shared__ int s_npe;
     const int tid = threadIdx.x;
@@ -698,7 +679,7 @@ __device__ void coreset_prefetch(const CoresetArgs& a, uint32_t* bits, int first
     for (int i = tid; i < nw; i += blockDim.x) bits[i] = 0u;
     __syncthreads();
     for (int c = tid; c < a.T * a.k; c += blockDim.x) {
-        const int e = __ldcg(&a.idx[c]);  // written by a kernel that may still be running
+        const int e = __ldg(&a.idx[c]);
         if (e >= 0 && e < E) atomicOr(&bits[e >> 5], 1u << (e & 31));
     }
     __syncthreads();
@@ -725,8 +706,8 @@ __device__ void coreset_prefetch(const CoresetArgs& a, uint32_t* bits, int first
     __syncthreads();
     const long long lines_per = a.pf_stride >> 7;
     const long long total = lines_per * s_npe;
-    const long long stride = static_cast<long long>(gridDim.x - first) * blockDim.x;
-    const long long g = static_cast<long long>(blockIdx.x - first) * blockDim.x + tid;
+    const long long stride = static_cast<long long>(gridDim.x - a.R) * blockDim.x;
+    const long long g = static_cast<long long>(blockIdx.x - a.R) * blockDim.x + tid;
     for (long long l = g; l < total; l += stride) {
         const int j = static_cast<int>(l / lines_per);
         const char* p = a.pf_base + static_cast<long long>(s_pe[j]) * a.pf_stride + ((l - j * lines_per) << 7);
@@ -737,55 +718,13 @@ __device__ void coreset_prefetch(const CoresetArgs& a, uint32_t* bits, int first
             asm volatile("prefetch.global.L2 [%0];" ::"l"(a.pf_next + (l << 7)));
 }
 
-// Helper CTAs of a layer whose coreset runs in the router launch (a.helpers_only): the
-// router launch may still be running, so instead of the programmatic-launch wait they
-// wait (bounded) on its flags: first until every router CTA has written its top-k, then
-// hint the first candidate experts' weights into L2; then until the work plan is written,
-// then copy the plan's token rows into the gathered activations.  A wait that runs out
-// sets the error word and the CTA returns.
-__device__ void coreset_helpers(const CoresetArgs& a, uint32_t* bits) {
-    __shared__ int s_ok;
-    const int tid = threadIdx.x;
-    if (tid == 0) {
-        s_ok = wait_at_least(a.route_done, a.route_target, a.timeout_ns);
-        if (!s_ok) record_error(a.err, kErrTimeoutFlag);
-    }
-    __syncthreads();
-    if (!s_ok) return;
-    __threadfence();
-    if (a.pf_base != nullptr && a.pf_experts > 0) coreset_prefetch(a, bits, 0);
-    if (tid == 0) {
-        s_ok = wait_at_least(a.plan_flag, a.plan_value, a.timeout_ns);
-        if (!s_ok) record_error(a.err, kErrTimeoutFlag);
-    }
-    __syncthreads();
-    if (!s_ok) return;
-    __threadfence();
-    if (blockIdx.x == 0 && a.done != nullptr)
-        for (int i = tid; i < a.n_done; i += blockDim.x) a.done[i] = 0;
-    const long long n = static_cast<long long>(__ldcg(&a.plan[2])) * a.row_vec;
-    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + tid; i < n; i += stride) {
-        const int slot = static_cast<int>(i / a.row_vec);
-        const int v = static_cast<int>(i - static_cast<long long>(slot) * a.row_vec);
-        const int t = __ldcg(&a.slot_tok[slot]);
-        const uint4 w = __ldcg(&a.gx[static_cast<size_t>(t) * a.row_vec + v]);
-        a.gxp[i] = a.to_f16 ? bf16x8_to_f16x8(w) : w;
-    }
-}
-
-// grid R (+ pf_ctas hint CTAs), 1024 threads: one CTA per request (see coreset_body);
-// or, with a.helpers_only, pf_ctas helper CTAs (see coreset_helpers).
+// grid R (+ pf_ctas hint CTAs), 1024 threads: one CTA per request (see coreset_body).
 __global__ void __launch_bounds__(kCoresetThreads) coreset_kernel(CoresetArgs a) {
     extern __shared__ __align__(16) uint8_t coreset_smem[];  // scratch, masks [ceil(T/32)][E], slot staging
     pdl_trigger();
-    if (a.helpers_only) {
-        coreset_helpers(a, reinterpret_cast<uint32_t*>(coreset_smem));
-        return;
-    }
     pdl_wait();
     if (static_cast<int>(blockIdx.x) >= a.R) {
-        coreset_prefetch(a, reinterpret_cast<uint32_t*>(coreset_smem), a.R);
+        coreset_prefetch(a, reinterpret_cast<uint32_t*>(coreset_smem));
         return;
     }
     // slot staging only pays when several requests share the plan step
@@ -938,20 +877,12 @@ __global__ void __launch_bounds__(kRouteTcThreads, 1)
 // logits of experts 32c .. 32c + 31 for the tile as route_tc_kernel does and
 // sends each logit over distributed shared memory to the CTA that takes the
 // token's softmax and top-k (token j of the tile: CTA j mod CL).
-// With the coreset in the launch, the last CTA of a request reuses its shared memory
-// (dead after its top-k) for the coreset's scratch, masks and plan staging.
 struct RouteCombineSmem {
     static constexpr int kPart = (kRouteTcThreads / 32) * 32 * 4;  // K partial sums [16 warps][32][4]
     __host__ __device__ static int tokens_per_cta(int CL) { return (8 + CL - 1) / CL; }
     __host__ __device__ static size_t bytes(int CL, int E) {
         return sizeof(float) * (kPart + static_cast<size_t>(tokens_per_cta(CL)) * E) +
                sizeof(int) * 2 * 33 + sizeof(float) * (2 * 33 + 2 * 9);
-    }
-    __host__ __device__ static int stage_slots(int R, int E, int T, int k) {
-        return R > 1 ? coreset_stage_slots(E, T, k) : 0;
-    }
-    __host__ __device__ static size_t coreset_bytes(int R, int E, int T, int k) {
-        return sizeof(CoresetScratch) + coreset_masks_bytes(E, T) + static_cast<size_t>(stage_slots(R, E, T, k)) * 8;
     }
 };
 
@@ -1036,32 +967,18 @@ __global__ void __launch_bounds__(kRouteTcThreads, 1) route_combine_kernel(Route
         const int j = rank + CL * jj;
         if (j < 8 && t0 + j < T) topk_one_token(zs + static_cast<size_t>(jj) * E, E, k, t0 + j, a.idx, a.mass, a.gate);
     }
-    if (!a.with_coreset) return;
-    // 5. count this CTA's top-k done; the last CTA of the tile's request runs its coreset (and,
-    //    for the last request, the work plan) in this CTA's shared memory
-    __shared__ int s_last_req;
-    __threadfence();
-    __syncthreads();
-    const int req = t0 / a.cs.P;
-    if (threadIdx.x == 0) {
-        atomicAdd(a.route_done, 1);
-        const int prev = atomicAdd(&a.req_done[req], 1);
-        s_last_req = prev == a.ctas_per_req - 1;
-        if (s_last_req) a.req_done[req] = 0;  // every other CTA of the request has counted
+}
+
+// 8 bf16 -> 8 f16 (round to nearest even; exact unless below f16's normal range)
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
+    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+        const __half2 h = __floats2half2_rn(f.x, f.y);
+        w[i] = *reinterpret_cast<const uint32_t*>(&h);
     }
-    __syncthreads();
-    if (!s_last_req) return;
-    __threadfence();
-    const int nstage = RouteCombineSmem::stage_slots(a.cs.R, E, T, k);
-    int* stage = nstage > 0 ? reinterpret_cast<int*>(rc_smem + sizeof(CoresetScratch) + coreset_masks_bytes(E, T))
-                            : nullptr;
-    const bool wrote_plan = coreset_body(a.cs, req, a.cs.R, reinterpret_cast<uint32_t*>(rc_smem + sizeof(CoresetScratch)),
-                                         *reinterpret_cast<CoresetScratch*>(rc_smem), stage, nstage);
-    if (wrote_plan) {
-        __threadfence();
-        __syncthreads();
-        if (threadIdx.x == 0) release_store_gpu(a.plan_flag, a.plan_value);
-    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 // One CTA per slot: xp[slot] = x[slot_tok[slot]] (TO_F16: bf16 rows stored as f16,
@@ -1141,8 +1058,6 @@ cudaError_t launch_coreset(const CoresetArgs& a, cudaStream_t s) {
     static int done[64] = {};
     cudaError_t e = ensure_smem(coreset_kernel, smem, done);
     if (e != cudaSuccess) return e;
-    if (a.helpers_only)
-        return launch_pdl(coreset_kernel, dim3(a.pf_ctas), dim3(kCoresetThreads), smem, s, a);
     const int helpers = (a.pf_base != nullptr && a.pf_experts > 0) ? a.pf_ctas : 0;
     return launch_pdl(coreset_kernel, dim3(a.R + helpers), dim3(kCoresetThreads), smem, s, a);
 }
@@ -1162,18 +1077,9 @@ int route_combine_eligible(int act_dtype, int T, int H, int E, int k) {
     return (E % kRouteTcExperts == 0 && E <= 8 * kRouteTcExperts && H % 512 == 0) ? 1 : 0;
 }
 
-int route_combine_coreset_eligible(int act_dtype, int R, int P, int H, int E, int k) {
-    if (!route_combine_eligible(act_dtype, R * P, H, E, k) || P % 8 != 0 || P * k > kCandCache) return 0;
-    return RouteCombineSmem::coreset_bytes(R, E, R * P, k) <= 220 * 1024 ? 1 : 0;
-}
-
 cudaError_t launch_route_combine(const RouteCombineArgs& a, cudaStream_t s) {
     const int CL = a.E / kRouteTcExperts;
-    size_t smem = RouteCombineSmem::bytes(CL, a.E);
-    if (a.with_coreset) {
-        const size_t cb = RouteCombineSmem::coreset_bytes(a.cs.R, a.E, a.T, a.k);
-        smem = smem > cb ? smem : cb;
-    }
+    const size_t smem = RouteCombineSmem::bytes(CL, a.E);
     static int done[64] = {};
     cudaError_t e = ensure_smem(route_combine_kernel, smem, done);
     if (e != cudaSuccess) return e;
