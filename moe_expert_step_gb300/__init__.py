@@ -153,8 +153,12 @@ class ModelDims:
 
 
 def layer(Wr, Wgu, Wd, Wsgu=None, Wsd=None, Sgu=None, Sd=None, Ssgu=None, Ssd=None) -> Layer:
-    """Device pointers of one layer; the four row-scale tensors only with FP8 expert weights."""
-    return Layer(_p(Wr), _p(Wgu), _p(Wd), _p(Wsgu), _p(Wsd), _p(Sgu), _p(Sd), _p(Ssgu), _p(Ssd))
+    """Device pointers of one layer; the four row-scale tensors only with FP8 expert weights.
+    The returned struct holds references to the tensors, so their memory stays allocated for
+    as long as the struct is alive."""
+    lay = Layer(_p(Wr), _p(Wgu), _p(Wd), _p(Wsgu), _p(Wsd), _p(Sgu), _p(Sd), _p(Ssgu), _p(Ssd))
+    lay._tensors = (Wr, Wgu, Wd, Wsgu, Wsd, Sgu, Sd, Ssgu, Ssd)
+    return lay
 
 
 def workspace_size(d: ModelDims, R: int) -> int:

@@ -168,3 +168,22 @@ def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
         ms.lib()
     with pytest.raises(ms.MoeStepError):
         ms.set_route_fusion(ms.FUSED_COMBINE_HEAD)
+
+
+def test_layer_struct_keeps_its_tensors_alive():
+    """ms.layer() returns raw pointers for the C ABI; the struct also holds the tensors, so a
+    caller that keeps only the struct (e.g. [ms.layer(**device_layer(...)) for ...]) cannot
+    leave the library reading freed memory."""
+    import gc
+    import weakref
+
+    import torch
+    w = torch.zeros(8)
+    ref = weakref.ref(w)
+    lay = ms.layer(w, w, w)
+    del w
+    gc.collect()
+    assert ref() is not None and lay.Wr == ref().data_ptr()
+    del lay
+    gc.collect()
+    assert ref() is None
