@@ -45,16 +45,23 @@ __device__ __forceinline__ float4 roundtrip4<bf16>(float4 v) {
                        __bfloat162float(__float2bfloat16_rn(v.z)), __bfloat162float(__float2bfloat16_rn(v.w)));
 }
 
+// Optional extra consumer of the normalised row: called as sink(c, n) for each group
+// of four columns c .. c+3 (n: the fp32 values that were rounded into x).
+struct NoSink {
+    __device__ __forceinline__ void operator()(int, float4) const {}
+};
+
 // One token per group of 256 threads (t < 0: the group only joins the barriers;
 // every thread of the block calls it).  MODE 0: out = sum_j gate_rr*y[slot_j] +
 // y[shared slot].  MODE 1: h += that; x = RMSNorm(h).  MODE 2: h = h_in; x =
 // RMSNorm(h).  The routed terms are added in candidate order j = 0..k-1, then the
 // shared one.  s_slot / s_g (33 each) and red (9) are the group's scratch.
-template <typename T, int MODE>
+template <typename T, int MODE, typename Sink = NoSink>
 __device__ void combine_row(int t, int H, int k, const float* __restrict__ y, const int32_t* __restrict__ slot_of,
                             const int32_t* __restrict__ slot_sh, const float* __restrict__ gate_rr, int has_shared,
                             const float* __restrict__ h_in, float* __restrict__ h, T* __restrict__ x,
-                            float* __restrict__ x_f32, float* __restrict__ out, int* s_slot, float* s_g, float* red) {
+                            float* __restrict__ x_f32, float* __restrict__ out, int* s_slot, float* s_g, float* red,
+                            Sink sink = Sink()) {
     const int gt = threadIdx.x & 255;
     const bool on = t >= 0;
     if (MODE != 2) {
@@ -128,6 +135,7 @@ __device__ void combine_row(int t, int H, int k, const float* __restrict__ y, co
         }
         const float4 n = make_float4(v.x * inv, v.y * inv, v.z * inv, v.w * inv);
         store4<T>(x + row + c, n);
+        sink(c, n);
         if (x_f32 != nullptr) *reinterpret_cast<float4*>(x_f32 + row + c) = roundtrip4<T>(n);
     }
 }

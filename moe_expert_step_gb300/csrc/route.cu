@@ -655,6 +655,8 @@ __device__ void coreset_body(const CoresetArgs& a, int r, int nreq, uint32_t* ma
         a.plan[1] = nsc;
         a.plan[2] = NR + (a.has_shared ? T : 0);
     }
+    if (a.done != nullptr)  // the expert launch's per-chunk counters start at zero
+        for (int i = tid; i < a.n_done; i += blockDim.x) a.done[i] = 0;
     if (stage != nullptr) {  // the staged slots, in order
         __syncthreads();
         const int ns = NR + (a.has_shared ? T : 0);
@@ -869,20 +871,51 @@ __global__ void __launch_bounds__(kRouteTcThreads, 1)
 }
 
 // The previous layer's combine + RMSNorm and the tensor-core router in one
-// cluster launch (bf16 activations, E % 32 == 0, E <= 256, H % 512 == 0): grid
-// (E / 32, ceil(T / 8)), one cluster of E / 32 CTAs per 8-token tile.  CTA c of
-// a cluster runs the combine of tokens c, c + CL, ... of the tile (the combine
-// kernel's arithmetic, so both write bit-identical rows), the cluster barrier
-// makes the tile's x rows visible to the cluster, then CTA c computes the
-// logits of experts 32c .. 32c + 31 for the tile as route_tc_kernel does and
-// sends each logit over distributed shared memory to the CTA that takes the
-// token's softmax and top-k (token j of the tile: CTA j mod CL).
+// cluster launch (bf16 activations, E % 32 == 0, E <= 256, H % 512 == 0, H <= 2560):
+// grid (E / 32, ceil(T / 8)), one cluster of E / 32 CTAs per 8-token tile.
+// Before waiting for the previous kernel, CTA c copies the router rows of its
+// experts 32c .. 32c + 31 into shared memory (cp.async; the weights are never
+// written).  It then runs the combine of tokens c, c + CL, ... of the tile (the
+// combine kernel's arithmetic, so both write bit-identical rows) and copies each
+// normalised row into the shared memory of every CTA of the cluster (distributed
+// shared memory); after the cluster barrier it computes the logits of its 32
+// experts for the tile from shared memory with route_tc_kernel's fragments and
+// K order, and sends each logit to the CTA that takes the token's softmax and
+// top-k (token j of the tile: CTA j mod CL).
 struct RouteCombineSmem {
     static constexpr int kPart = (kRouteTcThreads / 32) * 32 * 4;  // K partial sums [16 warps][32][4]
+    // staged rows: H + 8 elements, so the 8 rows an MMA fragment reads start in distinct banks
+    __host__ __device__ static int ld(int H) { return H + 8; }
     __host__ __device__ static int tokens_per_cta(int CL) { return (8 + CL - 1) / CL; }
-    __host__ __device__ static size_t bytes(int CL, int E) {
-        return sizeof(float) * (kPart + static_cast<size_t>(tokens_per_cta(CL)) * E) +
+    __host__ __device__ static size_t w_off() { return 0; }
+    __host__ __device__ static size_t x_off(int H) { return static_cast<size_t>(kRouteTcExperts) * ld(H) * 2; }
+    __host__ __device__ static size_t part_off(int H) { return x_off(H) + static_cast<size_t>(8) * ld(H) * 2; }
+    __host__ __device__ static size_t bytes(int CL, int E, int H) {
+        return part_off(H) + sizeof(float) * (kPart + static_cast<size_t>(tokens_per_cta(CL)) * E) +
                sizeof(int) * 2 * 33 + sizeof(float) * (2 * 33 + 2 * 9);
+    }
+};
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+    const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+}
+
+// Writes each normalised 4-column group of token row j of the tile into the staged x
+// tile of every CTA of the cluster.
+struct ClusterRowSink {
+    bf16* xs;  // this CTA's staged tile [8][ld]
+    int row_off;
+    int CL;
+    __device__ __forceinline__ void operator()(int c, float4 n) const {
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(n.x, n.y);
+        const __nv_bfloat162 hi = __floats2bfloat162_rn(n.z, n.w);
+        uint2 u;
+        u.x = *reinterpret_cast<const uint32_t*>(&lo);
+        u.y = *reinterpret_cast<const uint32_t*>(&hi);
+        cg::cluster_group cluster = cg::this_cluster();
+        for (int r = 0; r < CL; ++r)
+            *reinterpret_cast<uint2*>(cluster.map_shared_rank(xs, r) + row_off + c) = u;
     }
 };
 
@@ -895,52 +928,63 @@ __global__ void __launch_bounds__(kRouteTcThreads, 1) route_combine_kernel(Route
     const int g = lane >> 2, tig = lane & 3;
     const int eh = warp & 1, q = warp >> 1;
     const int T = a.T, H = a.H, E = a.E, k = a.k;
+    const int LD = RouteCombineSmem::ld(H);
     const int t0 = blockIdx.y * 8;
     const int e0 = rank * kRouteTcExperts;
     const int kspan = H >> 3;
     const int TPC = RouteCombineSmem::tokens_per_cta(CL);
     const int grp = threadIdx.x >> 8;  // combine: two groups of 256 threads
-    float* part = reinterpret_cast<float*>(rc_smem);
+    bf16* ws = reinterpret_cast<bf16*>(rc_smem + RouteCombineSmem::w_off());   // [32][LD] router rows
+    bf16* xs = reinterpret_cast<bf16*>(rc_smem + RouteCombineSmem::x_off(H));  // [8][LD] the tile's x rows
+    float* part = reinterpret_cast<float*>(rc_smem + RouteCombineSmem::part_off(H));
     float* zs = part + RouteCombineSmem::kPart;  // [TPC][E] logits of this CTA's tokens
     int* c_slot = reinterpret_cast<int*>(zs + static_cast<size_t>(TPC) * E) + 33 * grp;
     float* c_g = reinterpret_cast<float*>(reinterpret_cast<int*>(zs + static_cast<size_t>(TPC) * E) + 66) + 33 * grp;
     float* c_red = reinterpret_cast<float*>(reinterpret_cast<int*>(zs + static_cast<size_t>(TPC) * E) + 66) + 66 +
                    9 * grp;
-    {  // router weights are never written: hint this CTA's rows before waiting
-        const char* w = reinterpret_cast<const char*>(a.Wr + static_cast<size_t>(e0) * H);
-        const int lines = kRouteTcExperts * H * 2 / 128;
-        for (int l = threadIdx.x; l < lines; l += kRouteTcThreads)
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(w + 128ll * l));
+    {  // router weights are never written: stage this CTA's rows before waiting
+        const int vec = H >> 3;  // 16-byte pieces per row
+        const bf16* w = a.Wr + static_cast<size_t>(e0) * H;
+        for (int i = threadIdx.x; i < kRouteTcExperts * vec; i += kRouteTcThreads) {
+            const int r = i / vec, c = (i - r * vec) << 3;
+            cp_async16(ws + r * LD + c, w + static_cast<size_t>(r) * H + c);
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
     }
     pdl_trigger();
+    cluster.sync();  // every CTA of the cluster runs before any writes into another's shared memory
     pdl_wait();
-    // 1. combine of this CTA's tokens of the tile
+    // 1. combine of this CTA's tokens of the tile; each normalised row also goes to the
+    //    x tile of every CTA of the cluster (rows past the block's last token are zero)
     for (int j0 = 0; j0 < 8; j0 += 2 * CL) {
         const int j = j0 + rank + CL * grp;
         const int t = (j < 8 && t0 + j < T) ? t0 + j : -1;
+        const ClusterRowSink sink{xs, j * LD, CL};
         if (a.mode == 1)
             combine_row<bf16, 1>(t, H, k, a.y, a.slot_of, a.slot_sh, a.gate_rr_prev, a.has_shared, nullptr, a.hres,
-                                 a.x, nullptr, nullptr, c_slot, c_g, c_red);
+                                 a.x, nullptr, nullptr, c_slot, c_g, c_red, sink);
         else
             combine_row<bf16, 2>(t, H, k, nullptr, nullptr, nullptr, nullptr, 0, a.h_in, a.hres, a.x, nullptr,
-                                 nullptr, c_slot, c_g, c_red);
+                                 nullptr, c_slot, c_g, c_red, sink);
+        if (j < 8 && t < 0)
+            for (int c = (threadIdx.x & 255) * 4; c < H; c += 1024) sink(c, make_float4(0.f, 0.f, 0.f, 0.f));
     }
-    cluster.sync();  // the tile's x rows are in global memory
-    // 2. logits of experts e0 .. e0 + 31 for the tile (route_tc_kernel's fragments)
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    cluster.sync();  // the tile's x rows and this CTA's router rows are in shared memory
+    // 2. logits of experts e0 .. e0 + 31 for the tile (route_tc_kernel's fragments and K order)
     float d[4] = {0.f, 0.f, 0.f, 0.f};
-    const bf16* w0 = a.Wr + static_cast<size_t>(e0 + eh * 16 + g) * H;
-    const bf16* w1 = w0 + static_cast<size_t>(8) * H;
-    const bool ok = t0 + g < T;
-    const bf16* xr = a.x + static_cast<size_t>(ok ? t0 + g : 0) * H;
-#pragma unroll 2
+    const bf16* w0 = ws + (eh * 16 + g) * LD;
+    const bf16* w1 = w0 + 8 * LD;
+    const bf16* xr = xs + g * LD;
+#pragma unroll 4
     for (int h0 = q * kspan; h0 < (q + 1) * kspan; h0 += 64) {
         const int hb = h0 + 16 * tig;
-        const uint4 a00 = __ldg(reinterpret_cast<const uint4*>(w0 + hb));
-        const uint4 a01 = __ldg(reinterpret_cast<const uint4*>(w0 + hb + 8));
-        const uint4 a10 = __ldg(reinterpret_cast<const uint4*>(w1 + hb));
-        const uint4 a11 = __ldg(reinterpret_cast<const uint4*>(w1 + hb + 8));
-        const uint4 b0 = ok ? __ldcg(reinterpret_cast<const uint4*>(xr + hb)) : make_uint4(0, 0, 0, 0);
-        const uint4 b1 = ok ? __ldcg(reinterpret_cast<const uint4*>(xr + hb + 8)) : make_uint4(0, 0, 0, 0);
+        const uint4 a00 = *reinterpret_cast<const uint4*>(w0 + hb);
+        const uint4 a01 = *reinterpret_cast<const uint4*>(w0 + hb + 8);
+        const uint4 a10 = *reinterpret_cast<const uint4*>(w1 + hb);
+        const uint4 a11 = *reinterpret_cast<const uint4*>(w1 + hb + 8);
+        const uint4 b0 = *reinterpret_cast<const uint4*>(xr + hb);
+        const uint4 b1 = *reinterpret_cast<const uint4*>(xr + hb + 8);
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj)
             mma_16816(d, word8(a00, a01, 2 * jj), word8(a10, a11, 2 * jj), word8(a00, a01, 2 * jj + 1),
@@ -1074,12 +1118,13 @@ cudaError_t launch_gather(int dtype, const void* x, int H, const int32_t* slot_t
 
 int route_combine_eligible(int act_dtype, int T, int H, int E, int k) {
     if (act_dtype != MOESTEP_BF16 || T < 1 || T > 256 || k < 1 || k > 32) return 0;
-    return (E % kRouteTcExperts == 0 && E <= 8 * kRouteTcExperts && H % 512 == 0) ? 1 : 0;
+    if (E % kRouteTcExperts != 0 || E > 8 * kRouteTcExperts || H % 512 != 0) return 0;
+    return RouteCombineSmem::bytes(E / kRouteTcExperts, E, H) <= 225 * 1024 ? 1 : 0;
 }
 
 cudaError_t launch_route_combine(const RouteCombineArgs& a, cudaStream_t s) {
     const int CL = a.E / kRouteTcExperts;
-    const size_t smem = RouteCombineSmem::bytes(CL, a.E);
+    const size_t smem = RouteCombineSmem::bytes(CL, a.E, a.H);
     static int done[64] = {};
     cudaError_t e = ensure_smem(route_combine_kernel, smem, done);
     if (e != cudaSuccess) return e;
