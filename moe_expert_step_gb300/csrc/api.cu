@@ -80,7 +80,8 @@ Layout make_layout(const moestep_dims& d, int R) {
         return at;
     };
     L.hdr = take(256);  // int[0]: error word, int[8..15]: where a wait timed out, int[32..34]: expert work plan
-    L.counters_bytes = sizeof(int) * (L.route_groups + 1 + R);  // router groups, coreset, commit per request
+    // router groups, coreset, commit per request, plan flag (zeroed at the start of every call)
+    L.counters_bytes = sizeof(int) * (L.route_groups + 1 + R + 1);
     L.counters = take(L.counters_bytes);
     L.logits = take(sizeof(float) * T * d.E);
     L.idx = take(sizeof(int32_t) * T * d.k);
@@ -306,12 +307,24 @@ CoresetArgs coreset_args(const Ctx& c, int R, const float* top_p, const int32_t*
     return a;
 }
 
+// set by layer l's coreset once its plan is written (value l + 1); zeroed with the counters
+int* plan_flag(const Ctx& c, int R) { return at<int>(c.ws, c.L.counters) + c.L.route_groups + 1 + R; }
+
 // Wgu (may be NULL): the layer's gate/up weights, hinted into L2 for the first candidates
 // Wr_next (may be NULL): the next layer's router weights, hinted too
+// zero_done: the plan step also zeroes the expert launch's chunk counters (no gather launch follows)
 int run_coreset(const Ctx& c, int R, const float* top_p, const int32_t* idx, const float* mass, int32_t* n_sel,
                 int32_t* sel, uint8_t* survive, float* gate_rr, const void* Wgu = nullptr,
-                const void* Wr_next = nullptr) {
+                const void* Wr_next = nullptr, bool zero_done = false, int layer = -1) {
     CoresetArgs a = coreset_args(c, R, top_p, idx, mass, n_sel, sel, survive, gate_rr);
+    if (zero_done) {
+        a.done = at<int>(c.ws, c.L.done);
+        a.n_done = c.L.max_chunks;
+    }
+    if (layer >= 0) {
+        a.plan_flag = plan_flag(c, R);
+        a.plan_value = layer + 1;
+    }
     if (Wgu != nullptr && c.d->dtype != MOESTEP_F32 && c.sms > R) {
         a.pf_base = static_cast<const char*>(Wgu);
         a.pf_stride = 2ll * c.d->I * c.d->H * (c.d->dtype == MOESTEP_FP8 ? 1 : 2);
@@ -325,7 +338,7 @@ int run_coreset(const Ctx& c, int R, const float* top_p, const int32_t* idx, con
 }
 
 // the previous layer's combine (mode 1) or the input norm (mode 2), then the router
-int run_route_combine(const Ctx& c, int mode, const float* h_in, const void* Wr, int32_t* idx) {
+int run_route_combine(const Ctx& c, int mode, const float* h_in, const void* Wr, int32_t* idx, int layer = 0) {
     const moestep_dims* d = c.d;
     const Layout& L = c.L;
     RouteCombineArgs a{};
@@ -347,17 +360,25 @@ int run_route_combine(const Ctx& c, int mode, const float* h_in, const void* Wr,
     a.idx = idx;
     a.mass = at<float>(c.ws, L.mass);
     a.gate = at<float>(c.ws, L.gate);
+    a.plan_flag = plan_flag(c, L.T / d->P);
+    a.plan_value = layer;  // layer - 1's coreset stored layer
+    a.timeout_ns = g_timeout_ns;
     MOESTEP_LAUNCH(0, launch_route_combine(a, c.s));
     return MOESTEP_OK;
 }
 
 // gather + experts (fp32: FFMA; bf16: tcgen05 gate/up then down); leaves y
 // (per slot) in the workspace
+// in_launch_gather (bf16 experts): no gather launch; the expert launch copies its token rows
+// itself and the shared expert reads x directly (the coreset zeroed the chunk counters)
+bool in_launch_gather(const moestep_dims* d) { return d->dtype == MOESTEP_BF16; }
+
 int run_experts(const Ctx& c, int R, const void* x, const moestep_layer* layer, bool gathered = false) {
     const moestep_dims* d = c.d;
     const Layout& L = c.L;
     const int* plan = at<int>(c.ws, L.hdr) + 32;
     const bool tc = d->dtype != MOESTEP_F32;
+    const bool in_launch = gathered && in_launch_gather(d);
     if (!gathered)
         MOESTEP_LAUNCH(2, launch_gather(d->dtype, x, d->H, at<int32_t>(c.ws, L.slot_tok), plan, L.max_slots,
                                         at<void>(c.ws, L.xp), tc ? at<int>(c.ws, L.done) : nullptr, L.max_chunks,
@@ -390,6 +411,11 @@ int run_experts(const Ctx& c, int R, const void* x, const moestep_layer* layer, 
     }
     if ((rc = make_map(&m.b[0], at<void>(c.ws, L.xp), d->H, L.max_slots, 16))) return rc;
     if ((rc = make_map(&m.b[1], at<void>(c.ws, L.act), L.act_ld, L.max_slots, 16))) return rc;
+    if (in_launch) {
+        if ((rc = make_map(&m.b[2], x, d->H, L.T, 16))) return rc;
+    } else {
+        m.b[2] = m.b[0];
+    }
     GemmParams g{};
     g.plan = plan;
     g.chunks = at<int4>(c.ws, L.chunks);
@@ -418,6 +444,13 @@ int run_experts(const Ctx& c, int R, const void* x, const moestep_layer* layer, 
     g.sc[1] = sh ? layer->Ssgu : layer->Sgu;
     g.sc[2] = layer->Sd;
     g.sc[3] = sh ? layer->Ssd : layer->Sd;
+    if (in_launch) {
+        g.gx = static_cast<const uint4*>(x);
+        g.gxp = at<uint4>(c.ws, L.xp);
+        g.slot_tok = at<int32_t>(c.ws, L.slot_tok);
+        g.row_vec = d->H * 2 / 16;
+        g.n_tok = L.T;
+    }
     MOESTEP_LAUNCH(3, launch_tc_gemm(f8 ? kExpertsF8 : kExperts, L.nch, m, g, c.sms, c.s));
     return MOESTEP_OK;
 }
@@ -778,7 +811,7 @@ int block_decode_step(const moestep_dims* dims, int R, int n_layers, const moest
         const bool last = l == n_layers - 1;
         if (fused_head) {
             // the combine of layer l-1 (or the input norm) runs inside the layer-l router launch
-            MOESTEP_TRY(run_route_combine(c, l == 0 ? 2 : 1, h_in, layers[l].Wr, idx));
+            MOESTEP_TRY(run_route_combine(c, l == 0 ? 2 : 1, h_in, layers[l].Wr, idx, l));
         } else {
             MOESTEP_TRY(run_route(c, T, x, layers[l].Wr, idx, at<float>(ws, L.mass), at<float>(ws, L.gate), nullptr));
         }
@@ -789,10 +822,11 @@ int block_decode_step(const moestep_dims* dims, int R, int n_layers, const moest
         if (trace && trace->h)
             MOESTEP_CK(cudaMemcpyAsync(trace->h + static_cast<size_t>(l) * T * dims->H, hres,
                                        sizeof(float) * T * dims->H, cudaMemcpyDeviceToDevice, c.s));
+        const bool in_launch = in_launch_gather(dims);
         MOESTEP_TRY(run_coreset(c, R, top_p, idx, at<float>(ws, L.mass), nsel, sel,
                                 at<uint8_t>(ws, L.survive), at<float>(ws, L.gaterr), layers[l].Wgu,
-                                last ? nullptr : layers[l + 1].Wr));
-        MOESTEP_TRY(run_experts(c, R, x, &layers[l]));
+                                last ? nullptr : layers[l + 1].Wr, in_launch, l));
+        MOESTEP_TRY(run_experts(c, R, x, &layers[l], in_launch));
         if (!fused_head || last)
             MOESTEP_LAUNCH(5, launch_combine(1, act_dtype(dims->dtype), T, dims->H, k, at<float>(ws, L.y),
                                              at<int32_t>(ws, L.slot_of), at<int32_t>(ws, L.slot_sh),

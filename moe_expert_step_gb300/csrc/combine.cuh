@@ -56,15 +56,29 @@ struct NoSink {
 // y[shared slot].  MODE 1: h += that; x = RMSNorm(h).  MODE 2: h = h_in; x =
 // RMSNorm(h).  The routed terms are added in candidate order j = 0..k-1, then the
 // shared one.  s_slot / s_g (33 each) and red (9) are the group's scratch.
+// The token's slots and gates read into the group's scratch (MODE != 2); combine_row
+// does this itself unless its caller already did (slots_loaded).
+__device__ __forceinline__ void combine_load_slots(int t, int k, const int32_t* __restrict__ slot_of,
+                                                   const int32_t* __restrict__ slot_sh,
+                                                   const float* __restrict__ gate_rr, int has_shared, int* s_slot,
+                                                   float* s_g) {
+    const int gt = threadIdx.x & 255;
+    if (t >= 0 && gt < k) {
+        s_slot[gt] = __ldcg(&slot_of[t * k + gt]);
+        s_g[gt] = __ldcg(&gate_rr[t * k + gt]);
+    }
+    if (t >= 0 && gt == 32) s_slot[32] = has_shared ? __ldcg(&slot_sh[t]) : -1;
+}
+
 template <typename T, int MODE, typename Sink = NoSink>
 __device__ void combine_row(int t, int H, int k, const float* __restrict__ y, const int32_t* __restrict__ slot_of,
                             const int32_t* __restrict__ slot_sh, const float* __restrict__ gate_rr, int has_shared,
                             const float* __restrict__ h_in, float* __restrict__ h, T* __restrict__ x,
                             float* __restrict__ x_f32, float* __restrict__ out, int* s_slot, float* s_g, float* red,
-                            Sink sink = Sink()) {
+                            Sink sink = Sink(), bool slots_loaded = false) {
     const int gt = threadIdx.x & 255;
     const bool on = t >= 0;
-    if (MODE != 2) {
+    if (MODE != 2 && !slots_loaded) {
         if (on && gt < k) {
             s_slot[gt] = slot_of[t * k + gt];
             s_g[gt] = gate_rr[t * k + gt];

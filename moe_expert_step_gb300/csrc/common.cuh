@@ -65,6 +65,31 @@ __device__ __forceinline__ void record_error(int* err, int bits) {
     if (err) atomicOr(err, bits);
 }
 
+// Flags between kernels that run concurrently under programmatic dependent launch.
+__device__ __forceinline__ uint64_t gtimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ int acquire_load_gpu(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void release_store_gpu(int* p, int v) {
+    asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Bounded wait until *p >= v (acquire): false if limit_ns passed first.
+__device__ __forceinline__ bool wait_at_least(const int* p, int v, uint64_t limit_ns) {
+    if (acquire_load_gpu(p) >= v) return true;
+    const uint64_t t0 = gtimer_ns();
+    for (;;) {
+        __nanosleep(64);
+        if (acquire_load_gpu(p) >= v) return true;
+        if (gtimer_ns() - t0 >= limit_ns) return false;
+    }
+}
+
 // Merge of softmax partials (m = max logit, a = its lowest index, s = sum exp(l - m)).
 struct SoftmaxPartial {
     float m;

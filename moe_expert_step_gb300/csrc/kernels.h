@@ -23,7 +23,7 @@ enum GemmMode { kGateUp = 0, kDown = 1, kLmHead = 2, kExperts = 3, kExpertsF8 = 
 // SwiGLU output stored as f16.
 struct TensorMaps {
     CUtensorMap a[4];
-    CUtensorMap b[2];
+    CUtensorMap b[3];  // b[2] (kExperts with an in-launch gather): the block's token rows x [T][H]
 };
 
 struct GemmParams {
@@ -58,6 +58,15 @@ struct GemmParams {
     int* err;
     unsigned long long timeout_ns;
     const float* sc[4];    // kExpertsF8: row scales of the weights of a[0..3]
+    // kExperts, optional in-launch gather (gx != NULL): the epilogue warps first copy the token
+    // rows of their CTA's routed gate/up chunks, gxp[slot] = gx[slot_tok[slot]] (row_vec 16-byte
+    // vectors a row), before the producer loads them; shared-expert units read the token rows
+    // straight from x (maps.b[2]: slot NR + t is token t, NR = plan[2] - n_tok)
+    const uint4* gx;
+    uint4* gxp;
+    const int32_t* slot_tok;
+    int row_vec;
+    int n_tok;
 };
 
 cudaError_t launch_tc_gemm(int mode, int nch, const TensorMaps& maps, const GemmParams& p, int grid, cudaStream_t s);
@@ -84,6 +93,10 @@ struct CoresetArgs {
     int nch;
     int has_shared;
     int* err;
+    int* done;          // optional: the expert launch's chunk counters, zeroed once the plan is written
+    int n_done;
+    int* plan_flag;     // optional: release-stores plan_value here once the plan is written
+    int plan_value;
     // optional L2 hints: CTAs R .. R+pf_ctas-1 of the coreset launch hint the
     // weights (pf_stride bytes from pf_base + e * pf_stride) of the pf_experts
     // lowest-id experts that any token picked, while CTAs 0 .. R-1 run the coreset
@@ -121,6 +134,12 @@ struct RouteCombineArgs {
     int32_t* idx;
     float* mass;
     float* gate;
+    // mode 1, optional: once *plan_flag >= plan_value (the previous layer's coreset wrote its plan,
+    // so slot_of / slot_sh / gate_rr_prev are final) they are read before waiting for the
+    // previous kernel; without the flag, or if the bounded wait runs out, after it
+    const int* plan_flag;
+    int plan_value;
+    unsigned long long timeout_ns;
 };
 int route_combine_eligible(int act_dtype, int T, int H, int E, int k);
 cudaError_t launch_route_combine(const RouteCombineArgs& a, cudaStream_t s);

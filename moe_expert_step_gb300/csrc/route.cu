@@ -657,6 +657,11 @@ __device__ void coreset_body(const CoresetArgs& a, int r, int nreq, uint32_t* ma
     }
     if (a.done != nullptr)  // the expert launch's per-chunk counters start at zero
         for (int i = tid; i < a.n_done; i += blockDim.x) a.done[i] = 0;
+    if (a.plan_flag != nullptr) {  // the next router launch may read the plan's slots and gates
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) release_store_gpu(a.plan_flag, a.plan_value);
+    }
     if (stage != nullptr) {  // the staged slots, in order
         __syncthreads();
         const int ns = NR + (a.has_shared ? T : 0);
@@ -952,6 +957,20 @@ __global__ void __launch_bounds__(kRouteTcThreads, 1) route_combine_kernel(Route
         asm volatile("cp.async.commit_group;" ::: "memory");
     }
     pdl_trigger();
+    // One pass of the combine loop per group (E >= 128): its token's slots and gates, final once
+    // the previous layer's coreset set its flag, are read while the previous kernel still runs.
+    bool pre = false;
+    if (a.mode == 1 && a.plan_flag != nullptr && 2 * CL >= 8) {
+        __shared__ int s_pre;
+        if (threadIdx.x == 0) s_pre = wait_at_least(a.plan_flag, a.plan_value, a.timeout_ns);
+        __syncthreads();
+        pre = s_pre != 0;
+        if (pre) {
+            const int j = rank + CL * grp;
+            combine_load_slots((j < 8 && t0 + j < T) ? t0 + j : -1, k, a.slot_of, a.slot_sh, a.gate_rr_prev,
+                               a.has_shared, c_slot, c_g);
+        }
+    }
     cluster.sync();  // every CTA of the cluster runs before any writes into another's shared memory
     pdl_wait();
     // 1. combine of this CTA's tokens of the tile; each normalised row also goes to the
@@ -962,7 +981,7 @@ __global__ void __launch_bounds__(kRouteTcThreads, 1) route_combine_kernel(Route
         const ClusterRowSink sink{xs, j * LD, CL};
         if (a.mode == 1)
             combine_row<bf16, 1>(t, H, k, a.y, a.slot_of, a.slot_sh, a.gate_rr_prev, a.has_shared, nullptr, a.hres,
-                                 a.x, nullptr, nullptr, c_slot, c_g, c_red, sink);
+                                 a.x, nullptr, nullptr, c_slot, c_g, c_red, sink, pre);
         else
             combine_row<bf16, 2>(t, H, k, nullptr, nullptr, nullptr, nullptr, 0, a.h_in, a.hres, a.x, nullptr,
                                  nullptr, c_slot, c_g, c_red, sink);
