@@ -96,7 +96,7 @@ Layout make_layout(const moestep_dims& d, int R) {
     L.slot_tok = take(sizeof(int32_t) * L.max_slots);
     L.slot_exp = take(sizeof(int32_t) * L.max_slots);
     L.chunks = take(sizeof(int4) * L.max_chunks);
-    L.done = take(sizeof(int) * L.max_chunks);
+    L.done = take(sizeof(int) * (L.max_chunks + 1));  // chunk counters, then the expert launch's unit counter
     L.xp = take(esz * L.max_slots * d.H);
     L.act = take(esz * L.max_slots * L.act_ld);
     L.y = take(sizeof(float) * L.max_slots * d.H);
@@ -312,15 +312,11 @@ int* plan_flag(const Ctx& c, int R) { return at<int>(c.ws, c.L.counters) + c.L.r
 
 // Wgu (may be NULL): the layer's gate/up weights, hinted into L2 for the first candidates
 // Wr_next (may be NULL): the next layer's router weights, hinted too
-// zero_done: the plan step also zeroes the expert launch's chunk counters (no gather launch follows)
+// layer (>= 0): the plan step release-stores layer + 1 into the plan flag
 int run_coreset(const Ctx& c, int R, const float* top_p, const int32_t* idx, const float* mass, int32_t* n_sel,
                 int32_t* sel, uint8_t* survive, float* gate_rr, const void* Wgu = nullptr,
-                const void* Wr_next = nullptr, bool zero_done = false, int layer = -1) {
+                const void* Wr_next = nullptr, int layer = -1) {
     CoresetArgs a = coreset_args(c, R, top_p, idx, mass, n_sel, sel, survive, gate_rr);
-    if (zero_done) {
-        a.done = at<int>(c.ws, c.L.done);
-        a.n_done = c.L.max_chunks;
-    }
     if (layer >= 0) {
         a.plan_flag = plan_flag(c, R);
         a.plan_value = layer + 1;
@@ -369,20 +365,14 @@ int run_route_combine(const Ctx& c, int mode, const float* h_in, const void* Wr,
 
 // gather + experts (fp32: FFMA; bf16: tcgen05 gate/up then down); leaves y
 // (per slot) in the workspace
-// in_launch_gather (bf16 experts): no gather launch; the expert launch copies its token rows
-// itself and the shared expert reads x directly (the coreset zeroed the chunk counters)
-bool in_launch_gather(const moestep_dims* d) { return d->dtype == MOESTEP_BF16; }
-
-int run_experts(const Ctx& c, int R, const void* x, const moestep_layer* layer, bool gathered = false) {
+int run_experts(const Ctx& c, int R, const void* x, const moestep_layer* layer) {
     const moestep_dims* d = c.d;
     const Layout& L = c.L;
     const int* plan = at<int>(c.ws, L.hdr) + 32;
     const bool tc = d->dtype != MOESTEP_F32;
-    const bool in_launch = gathered && in_launch_gather(d);
-    if (!gathered)
-        MOESTEP_LAUNCH(2, launch_gather(d->dtype, x, d->H, at<int32_t>(c.ws, L.slot_tok), plan, L.max_slots,
-                                        at<void>(c.ws, L.xp), tc ? at<int>(c.ws, L.done) : nullptr, L.max_chunks,
-                                        c.s));
+    MOESTEP_LAUNCH(2, launch_gather(d->dtype, x, d->H, at<int32_t>(c.ws, L.slot_tok), plan, L.max_slots,
+                                    at<void>(c.ws, L.xp), tc ? at<int>(c.ws, L.done) : nullptr, L.max_chunks + 1,
+                                    c.s));
     if (d->dtype == MOESTEP_F32) {
         MOESTEP_LAUNCH(3, launch_f32_gateup(d->H, d->E, d->I, d->Is, L.max_slots, at<float>(c.ws, L.xp),
                                             at<int32_t>(c.ws, L.slot_exp), plan, static_cast<const float*>(layer->Wgu),
@@ -411,11 +401,6 @@ int run_experts(const Ctx& c, int R, const void* x, const moestep_layer* layer, 
     }
     if ((rc = make_map(&m.b[0], at<void>(c.ws, L.xp), d->H, L.max_slots, 16))) return rc;
     if ((rc = make_map(&m.b[1], at<void>(c.ws, L.act), L.act_ld, L.max_slots, 16))) return rc;
-    if (in_launch) {
-        if ((rc = make_map(&m.b[2], x, d->H, L.T, 16))) return rc;
-    } else {
-        m.b[2] = m.b[0];
-    }
     GemmParams g{};
     g.plan = plan;
     g.chunks = at<int4>(c.ws, L.chunks);
@@ -440,17 +425,11 @@ int run_experts(const Ctx& c, int R, const void* x, const moestep_layer* layer, 
     g.out2 = at<void>(c.ws, L.y);
     g.out2_ld = d->H;
     g.done = at<int>(c.ws, L.done);
+    g.unit_ctr = at<int>(c.ws, L.done) + L.max_chunks;
     g.sc[0] = layer->Sgu;
     g.sc[1] = sh ? layer->Ssgu : layer->Sgu;
     g.sc[2] = layer->Sd;
     g.sc[3] = sh ? layer->Ssd : layer->Sd;
-    if (in_launch) {
-        g.gx = static_cast<const uint4*>(x);
-        g.gxp = at<uint4>(c.ws, L.xp);
-        g.slot_tok = at<int32_t>(c.ws, L.slot_tok);
-        g.row_vec = d->H * 2 / 16;
-        g.n_tok = L.T;
-    }
     MOESTEP_LAUNCH(3, launch_tc_gemm(f8 ? kExpertsF8 : kExperts, L.nch, m, g, c.sms, c.s));
     return MOESTEP_OK;
 }
@@ -822,11 +801,10 @@ int block_decode_step(const moestep_dims* dims, int R, int n_layers, const moest
         if (trace && trace->h)
             MOESTEP_CK(cudaMemcpyAsync(trace->h + static_cast<size_t>(l) * T * dims->H, hres,
                                        sizeof(float) * T * dims->H, cudaMemcpyDeviceToDevice, c.s));
-        const bool in_launch = in_launch_gather(dims);
         MOESTEP_TRY(run_coreset(c, R, top_p, idx, at<float>(ws, L.mass), nsel, sel,
                                 at<uint8_t>(ws, L.survive), at<float>(ws, L.gaterr), layers[l].Wgu,
-                                last ? nullptr : layers[l + 1].Wr, in_launch, l));
-        MOESTEP_TRY(run_experts(c, R, x, &layers[l], in_launch));
+                                last ? nullptr : layers[l + 1].Wr, l));
+        MOESTEP_TRY(run_experts(c, R, x, &layers[l]));
         if (!fused_head || last)
             MOESTEP_LAUNCH(5, launch_combine(1, act_dtype(dims->dtype), T, dims->H, k, at<float>(ws, L.y),
                                              at<int32_t>(ws, L.slot_of), at<int32_t>(ws, L.slot_sh),

@@ -190,6 +190,54 @@ __device__ __forceinline__ void record_timeout(int* err, int role, int u, int kb
     }
 }
 
+// Units of the bf16 expert launch are handed out at run time: the producer warp takes each
+// next unit index from a global counter (so CTAs that stream faster take more units and the
+// launch ends together) and publishes it in a ring of kUnitQ shared-memory entries that the
+// MMA warp and the four epilogue warps read in the same order.  Gate/up units have the lower
+// indices, so every gate/up unit is taken before any down unit, as with the static order.
+constexpr int kUnitQ = 8;
+struct UnitRing {
+    uint64_t* full;   // [kUnitQ] the producer wrote the entry (count 1)
+    uint64_t* empty;  // [kUnitQ] the MMA warp and the four epilogue warps read it (count 5)
+    int* idx;         // [kUnitQ] unit index, or -1: no more units
+};
+
+// Producer warp: the next unit (or -1), taken from *ctr by lane 0 and published in the ring;
+// false if the wait for a free entry gave up.
+__device__ __forceinline__ bool take_unit(const UnitRing& r, int* ctr, int n_units, int& qi, int& u,
+                                          volatile int* abort, uint64_t tmo) {
+    int good = 1, v = -1;
+    if ((threadIdx.x & 31) == 0) {
+        const int e = qi % kUnitQ;
+        good = tc::mbar_wait(&r.empty[e], ((qi / kUnitQ) & 1) ^ 1u, abort, tmo);
+        if (good) {
+            v = atomicAdd(ctr, 1);
+            if (v >= n_units) v = -1;
+            r.idx[e] = v;
+            tc::mbar_arrive(&r.full[e]);
+        }
+    }
+    ++qi;
+    u = __shfl_sync(0xffffffffu, v, 0);
+    return __shfl_sync(0xffffffffu, good, 0) != 0;
+}
+
+// MMA or epilogue warp: the next published unit (or -1); false if the wait gave up.
+__device__ __forceinline__ bool read_unit(const UnitRing& r, int& qi, int& u, volatile int* abort, uint64_t tmo) {
+    int good = 1, v = -1;
+    if ((threadIdx.x & 31) == 0) {
+        const int e = qi % kUnitQ;
+        good = tc::mbar_wait(&r.full[e], (qi / kUnitQ) & 1, abort, tmo);
+        if (good) {
+            v = r.idx[e];
+            tc::mbar_arrive(&r.empty[e]);
+        }
+    }
+    ++qi;
+    u = __shfl_sync(0xffffffffu, v, 0);
+    return __shfl_sync(0xffffffffu, good, 0) != 0;
+}
+
 template <int MODE, int NCH>
 __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ TensorMaps maps, const GemmParams p) {
@@ -213,8 +261,9 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
     uint64_t* conv = fin + 1;            // F8: the stage's weight tile is converted (count 1)
     uint64_t* full8 = conv + STAGES;     // F8: the slot's FP8 tile and token rows landed (TMA bytes)
     uint64_t* empty8 = full8 + S8;       // F8: the MMA is done with the slot (count 1)
-    uint64_t* gath = empty8 + S8;        // in-launch gather: the epilogue threads' rows are stored (count 128)
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(gath + 1);
+    constexpr bool DYN = MODE == kExperts;  // units handed out at run time (UnitRing)
+    const UnitRing ring{empty8 + S8, empty8 + S8 + kUnitQ, reinterpret_cast<int*>(empty8 + S8 + 2 * kUnitQ)};
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(ring.idx + kUnitQ);
     int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
     int* zero_flag = abort_flag + 1;
 
@@ -231,7 +280,11 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
             tc::mbar_init(&tempty[b], 128);
         }
         tc::mbar_init(fin, F8 ? 2 : 1);
-        tc::mbar_init(gath, 128);
+        if (DYN)
+            for (int q = 0; q < kUnitQ; ++q) {
+                tc::mbar_init(&ring.full[q], 1);
+                tc::mbar_init(&ring.empty[q], 5);
+            }
         if (F8) {
             for (int s = 0; s < STAGES; ++s) tc::mbar_init(&conv[s], 4);  // one arrival per warp of a group
             for (int s = 0; s < S8; ++s) {
@@ -250,7 +303,6 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
                 tc::prefetch_tmap(&maps.a[2]);
                 tc::prefetch_tmap(&maps.a[3]);
                 tc::prefetch_tmap(&maps.b[1]);
-                if (!F8 && p.gx != nullptr) tc::prefetch_tmap(&maps.b[2]);
             }
         }
     }
@@ -349,18 +401,22 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
-        // in-launch gather: routed gate/up token rows are loaded once the epilogue warps stored
-        // them; shared units take the token rows of x itself (slot NR + t is token t)
-        const bool gather = EXP && !F8 && p.gx != nullptr;
-        const int NR = gather ? p.plan[2] - p.n_tok : 0;
-        bool rows_ready = !gather;
-        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        int qi = 0;
+        for (int u = blockIdx.x; ok; u += gridDim.x) {
+            if (DYN) {
+                if (!take_unit(ring, p.unit_ctr, n_units, qi, u, abortv, tmo)) {
+                    ok = false;
+                    if (lane == 0) record_timeout(p.err, 7, u, -1, -1, 0, n_units, 0);
+                    break;
+                }
+                if (u < 0) break;
+            } else if (u >= n_units) {
+                break;
+            }
             const Unit w = decode_unit<MODE, NCH>(u, p, nrc, nsc);
             const int nb = (w.n + 15) >> 4;
             const CUtensorMap* mA = &maps.a[(w.dn && EXP ? 2 : 0) + (w.shared ? 1 : 0)];
-            const bool from_x = gather && !w.dn && w.shared;
-            const CUtensorMap* mB = &maps.b[w.dn && EXP ? 1 : (from_x ? 2 : 0)];
-            const int brow = from_x ? w.slot0 - NR : w.slot0;
+            const CUtensorMap* mB = &maps.b[w.dn && EXP ? 1 : 0];
             if (EXP && w.dn) {
                 // the SwiGLU rows of this chunk come from gate/up units of other CTAs
                 int good = 1;
@@ -391,16 +447,9 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
                             tc::tma_load_2d_hint(sa, mA, &full[stage], kb * 64, w.rowA0, pol);
                             tc::tma_load_2d_hint(sa + kABytes / 2, mA, &full[stage], kb * 64, w.rowA1, pol);
                         }
-                        if (!rows_ready && !w.dn && !w.shared) {
-                            // the weight tile is on its way; the token rows wait for the gather
-                            good = tc::mbar_wait(gath, 0, abortv, tmo);
-                            rows_ready = true;
-                            asm volatile("fence.proxy.async.global;" ::: "memory");
-                        }
-                        if (good)
-                            for (int b = 0; b < nb; ++b)
-                                tc::tma_load_2d(sa + kABytes + b * kBoxBBytes, mB, &full[stage], kb * 64,
-                                                brow + 16 * b);
+                        for (int b = 0; b < nb; ++b)
+                            tc::tma_load_2d(sa + kABytes + b * kBoxBBytes, mB, &full[stage], kb * 64,
+                                            w.slot0 + 16 * b);
                         issued |= 1u << stage;
                         issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
                     }
@@ -440,7 +489,17 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
         uint32_t ph8 = 0;
         bool ok = true;
         int it = 0;
-        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++it) {
+        int qi = 0;
+        for (int u = blockIdx.x; ok; u += gridDim.x, ++it) {
+            if (DYN) {
+                if (!read_unit(ring, qi, u, abortv, tmo)) {
+                    ok = false;
+                    break;
+                }
+                if (u < 0) break;
+            } else if (u >= n_units) {
+                break;
+            }
             const Unit w = decode_unit<MODE, NCH>(u, p, nrc, nsc);
             const int buf = it & 1;
             const uint32_t aph = (it >> 1) & 1;
@@ -505,26 +564,21 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
     } else if (warp < 6) {
         // ------------------------------------------------------------ epilogue (warps 2..5)
         const int sp = warp & 3;  // TMEM sub-partition this warp may access: lanes 32*sp .. 32*sp+31
-        if (EXP && !F8 && p.gx != nullptr) {
-            // in-launch gather: the token rows of this CTA's routed gate/up chunks (other CTAs
-            // that share a chunk store the same bytes), then one arrival per thread
-            const int et = threadIdx.x - 64;  // 0 .. 127
-            const int n_gu_routed = nrc * p.routed_tiles;
-            for (int u = blockIdx.x; u < n_gu_routed; u += gridDim.x) {
-                const int4 ch = p.chunks[u / p.routed_tiles];
-                const int nv = ch.z * p.row_vec;
-                for (int i = et; i < nv; i += 128) {
-                    const int r = i / p.row_vec, v = i - r * p.row_vec;
-                    const int t = __ldg(&p.slot_tok[ch.y + r]);
-                    p.gxp[static_cast<size_t>(ch.y + r) * p.row_vec + v] =
-                        __ldg(&p.gx[static_cast<size_t>(t) * p.row_vec + v]);
-                }
-            }
-            asm volatile("fence.proxy.async.global;" ::: "memory");
-            tc::mbar_arrive(gath);
-        }
         int it = 0;
-        for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++it) {
+        int qi = 0;
+        for (int u = blockIdx.x;; u += gridDim.x, ++it) {
+            if (DYN) {
+                if (!read_unit(ring, qi, u, abortv, tmo)) {
+                    if (lane == 0) {
+                        *abort_flag = 1;
+                        record_error(p.err, kErrTimeoutEpilogue);
+                    }
+                    break;
+                }
+                if (u < 0) break;
+            } else if (u >= n_units) {
+                break;
+            }
             const Unit w = decode_unit<MODE, NCH>(u, p, nrc, nsc);
             const int buf = it & 1;
             const uint32_t aph = (it >> 1) & 1;

@@ -23,7 +23,7 @@ enum GemmMode { kGateUp = 0, kDown = 1, kLmHead = 2, kExperts = 3, kExpertsF8 = 
 // SwiGLU output stored as f16.
 struct TensorMaps {
     CUtensorMap a[4];
-    CUtensorMap b[3];  // b[2] (kExperts with an in-launch gather): the block's token rows x [T][H]
+    CUtensorMap b[2];
 };
 
 struct GemmParams {
@@ -58,15 +58,7 @@ struct GemmParams {
     int* err;
     unsigned long long timeout_ns;
     const float* sc[4];    // kExpertsF8: row scales of the weights of a[0..3]
-    // kExperts, optional in-launch gather (gx != NULL): the epilogue warps first copy the token
-    // rows of their CTA's routed gate/up chunks, gxp[slot] = gx[slot_tok[slot]] (row_vec 16-byte
-    // vectors a row), before the producer loads them; shared-expert units read the token rows
-    // straight from x (maps.b[2]: slot NR + t is token t, NR = plan[2] - n_tok)
-    const uint4* gx;
-    uint4* gxp;
-    const int32_t* slot_tok;
-    int row_vec;
-    int n_tok;
+    int* unit_ctr;         // kExperts: next unit to hand out (zeroed with the chunk counters)
 };
 
 cudaError_t launch_tc_gemm(int mode, int nch, const TensorMaps& maps, const GemmParams& p, int grid, cudaStream_t s);
@@ -93,8 +85,6 @@ struct CoresetArgs {
     int nch;
     int has_shared;
     int* err;
-    int* done;          // optional: the expert launch's chunk counters, zeroed once the plan is written
-    int n_done;
     int* plan_flag;     // optional: release-stores plan_value here once the plan is written
     int plan_value;
     // optional L2 hints: CTAs R .. R+pf_ctas-1 of the coreset launch hint the

@@ -655,8 +655,6 @@ __device__ void coreset_body(const CoresetArgs& a, int r, int nreq, uint32_t* ma
         a.plan[1] = nsc;
         a.plan[2] = NR + (a.has_shared ? T : 0);
     }
-    if (a.done != nullptr)  // the expert launch's per-chunk counters start at zero
-        for (int i = tid; i < a.n_done; i += blockDim.x) a.done[i] = 0;
     if (a.plan_flag != nullptr) {  // the next router launch may read the plan's slots and gates
         __threadfence();
         __syncthreads();
