@@ -307,20 +307,15 @@ CoresetArgs coreset_args(const Ctx& c, int R, const float* top_p, const int32_t*
     return a;
 }
 
-// set by layer l's coreset once its plan is written (value l + 1); zeroed with the counters
+// set to l + 1 by layer l's gather launch once the coreset has completed; zeroed with the counters
 int* plan_flag(const Ctx& c, int R) { return at<int>(c.ws, c.L.counters) + c.L.route_groups + 1 + R; }
 
 // Wgu (may be NULL): the layer's gate/up weights, hinted into L2 for the first candidates
 // Wr_next (may be NULL): the next layer's router weights, hinted too
-// layer (>= 0): the plan step release-stores layer + 1 into the plan flag
 int run_coreset(const Ctx& c, int R, const float* top_p, const int32_t* idx, const float* mass, int32_t* n_sel,
                 int32_t* sel, uint8_t* survive, float* gate_rr, const void* Wgu = nullptr,
-                const void* Wr_next = nullptr, int layer = -1) {
+                const void* Wr_next = nullptr) {
     CoresetArgs a = coreset_args(c, R, top_p, idx, mass, n_sel, sel, survive, gate_rr);
-    if (layer >= 0) {
-        a.plan_flag = plan_flag(c, R);
-        a.plan_value = layer + 1;
-    }
     if (Wgu != nullptr && c.d->dtype != MOESTEP_F32 && c.sms > R) {
         a.pf_base = static_cast<const char*>(Wgu);
         a.pf_stride = 2ll * c.d->I * c.d->H * (c.d->dtype == MOESTEP_FP8 ? 1 : 2);
@@ -357,22 +352,23 @@ int run_route_combine(const Ctx& c, int mode, const float* h_in, const void* Wr,
     a.mass = at<float>(c.ws, L.mass);
     a.gate = at<float>(c.ws, L.gate);
     a.plan_flag = plan_flag(c, L.T / d->P);
-    a.plan_value = layer;  // layer - 1's coreset stored layer
+    a.plan_value = layer;  // layer - 1's gather stored layer
     a.timeout_ns = g_timeout_ns;
     MOESTEP_LAUNCH(0, launch_route_combine(a, c.s));
     return MOESTEP_OK;
 }
 
 // gather + experts (fp32: FFMA; bf16: tcgen05 gate/up then down); leaves y
-// (per slot) in the workspace
-int run_experts(const Ctx& c, int R, const void* x, const moestep_layer* layer) {
+// (per slot) in the workspace.  layer >= 0 (block_decode_step): the gather sets the plan flag
+// to layer + 1 for the next layer's router launch.
+int run_experts(const Ctx& c, int R, const void* x, const moestep_layer* layer, int layer_index = -1) {
     const moestep_dims* d = c.d;
     const Layout& L = c.L;
     const int* plan = at<int>(c.ws, L.hdr) + 32;
     const bool tc = d->dtype != MOESTEP_F32;
     MOESTEP_LAUNCH(2, launch_gather(d->dtype, x, d->H, at<int32_t>(c.ws, L.slot_tok), plan, L.max_slots,
                                     at<void>(c.ws, L.xp), tc ? at<int>(c.ws, L.done) : nullptr, L.max_chunks + 1,
-                                    c.s));
+                                    layer_index >= 0 ? plan_flag(c, R) : nullptr, layer_index + 1, c.s));
     if (d->dtype == MOESTEP_F32) {
         MOESTEP_LAUNCH(3, launch_f32_gateup(d->H, d->E, d->I, d->Is, L.max_slots, at<float>(c.ws, L.xp),
                                             at<int32_t>(c.ws, L.slot_exp), plan, static_cast<const float*>(layer->Wgu),
@@ -803,8 +799,8 @@ int block_decode_step(const moestep_dims* dims, int R, int n_layers, const moest
                                        sizeof(float) * T * dims->H, cudaMemcpyDeviceToDevice, c.s));
         MOESTEP_TRY(run_coreset(c, R, top_p, idx, at<float>(ws, L.mass), nsel, sel,
                                 at<uint8_t>(ws, L.survive), at<float>(ws, L.gaterr), layers[l].Wgu,
-                                last ? nullptr : layers[l + 1].Wr, l));
-        MOESTEP_TRY(run_experts(c, R, x, &layers[l]));
+                                last ? nullptr : layers[l + 1].Wr));
+        MOESTEP_TRY(run_experts(c, R, x, &layers[l], l));
         if (!fused_head || last)
             MOESTEP_LAUNCH(5, launch_combine(1, act_dtype(dims->dtype), T, dims->H, k, at<float>(ws, L.y),
                                              at<int32_t>(ws, L.slot_of), at<int32_t>(ws, L.slot_sh),

@@ -94,7 +94,12 @@ __device__ void combine_row(int t, int H, int k, const float* __restrict__ y, co
     for (int c = gt * 4; on && c < H; c += 1024, ++i) {
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         if (MODE != 2) {
-            // slots in groups of 8 loaded together, added in candidate order
+            // the shared expert's row is loaded with the first group of routed rows (all in
+            // flight together); routed rows in groups of 8, added in candidate order, then the
+            // shared one
+            const int ssl = s_slot[32];
+            const float4 vs = ssl >= 0 ? __ldg(reinterpret_cast<const float4*>(y + static_cast<size_t>(ssl) * H + c))
+                                       : make_float4(0.f, 0.f, 0.f, 0.f);
             for (int j0 = 0; j0 < k; j0 += 8) {
                 float4 v[8];
 #pragma unroll
@@ -114,12 +119,11 @@ __device__ void combine_row(int t, int H, int k, const float* __restrict__ y, co
                     }
                 }
             }
-            if (s_slot[32] >= 0) {
-                const float4 v = *reinterpret_cast<const float4*>(y + static_cast<size_t>(s_slot[32]) * H + c);
-                acc.x += v.x;
-                acc.y += v.y;
-                acc.z += v.z;
-                acc.w += v.w;
+            if (ssl >= 0) {
+                acc.x += vs.x;
+                acc.y += vs.y;
+                acc.z += vs.z;
+                acc.w += vs.w;
             }
         }
         if (MODE == 0) {

@@ -85,8 +85,6 @@ struct CoresetArgs {
     int nch;
     int has_shared;
     int* err;
-    int* plan_flag;     // optional: release-stores plan_value here once the plan is written
-    int plan_value;
     // optional L2 hints: CTAs R .. R+pf_ctas-1 of the coreset launch hint the
     // weights (pf_stride bytes from pf_base + e * pf_stride) of the pf_experts
     // lowest-id experts that any token picked, while CTAs 0 .. R-1 run the coreset
@@ -124,9 +122,9 @@ struct RouteCombineArgs {
     int32_t* idx;
     float* mass;
     float* gate;
-    // mode 1, optional: once *plan_flag >= plan_value (the previous layer's coreset wrote its plan,
-    // so slot_of / slot_sh / gate_rr_prev are final) they are read before waiting for the
-    // previous kernel; without the flag, or if the bounded wait runs out, after it
+    // mode 1, optional: once *plan_flag >= plan_value (set by the previous layer's gather launch:
+    // its coreset completed, so slot_of / slot_sh / gate_rr_prev are final) they are read before
+    // waiting for the previous kernel; without the flag, or if the bounded wait runs out, after it
     const int* plan_flag;
     int plan_value;
     unsigned long long timeout_ns;
@@ -135,9 +133,11 @@ int route_combine_eligible(int act_dtype, int T, int H, int E, int k);
 cudaError_t launch_route_combine(const RouteCombineArgs& a, cudaStream_t s);
 
 // xp[slot] = x[slot_tok[slot]] for the plan's slots; zeroes done[0..n_done)
-// (the fused expert launch's counters; NULL: none)
+// (the fused expert launch's counters; NULL: none); release-stores flag_value into *flag
+// (NULL: none) once the preceding coreset launch has completed
 cudaError_t launch_gather(int dtype, const void* x, int H, const int32_t* slot_tok, const int* plan,
-                          int max_slots, void* xp, int* done, int n_done, cudaStream_t s);
+                          int max_slots, void* xp, int* done, int n_done, int* flag, int flag_value,
+                          cudaStream_t s);
 
 // ------------------------------------------------------------------ combine / norm / embed
 // mode 0: out = routed + shared; mode 1: h += routed + shared, x = RMSNorm(h); mode 2: h = h_in, x = RMSNorm(h)

@@ -655,11 +655,6 @@ __device__ void coreset_body(const CoresetArgs& a, int r, int nreq, uint32_t* ma
         a.plan[1] = nsc;
         a.plan[2] = NR + (a.has_shared ? T : 0);
     }
-    if (a.plan_flag != nullptr) {  // the next router launch may read the plan's slots and gates
-        __threadfence();
-        __syncthreads();
-        if (tid == 0) release_store_gpu(a.plan_flag, a.plan_value);
-    }
     if (stage != nullptr) {  // the staged slots, in order
         __syncthreads();
         const int ns = NR + (a.has_shared ? T : 0);
@@ -1044,14 +1039,17 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
 
 // One CTA per slot: xp[slot] = x[slot_tok[slot]] (TO_F16: bf16 rows stored as f16,
 // the activation type of the FP8 expert launch); CTA 0 also zeroes the expert
-// launch's chunk counters.
+// launch's chunk counters and, if given, release-stores flag_value into *flag
+// (the coreset before it has completed: its plan, slots and gates are final).
 template <bool TO_F16>
 __global__ void __launch_bounds__(256) gather_kernel(const uint4* __restrict__ x, int row_vec,
                                                      const int32_t* __restrict__ slot_tok, const int* __restrict__ plan,
-                                                     uint4* __restrict__ xp, int* __restrict__ done, int n_done) {
+                                                     uint4* __restrict__ xp, int* __restrict__ done, int n_done,
+                                                     int* __restrict__ flag, int flag_value) {
     const int slot = blockIdx.x;
     pdl_trigger();
     pdl_wait();
+    if (flag != nullptr && blockIdx.x == 0 && threadIdx.x == 0) release_store_gpu(flag, flag_value);
     if (done != nullptr && blockIdx.x == 0)
         for (int i = threadIdx.x; i < n_done; i += blockDim.x) done[i] = 0;
     if (slot < plan[2]) {
@@ -1124,13 +1122,13 @@ cudaError_t launch_coreset(const CoresetArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_gather(int dtype, const void* x, int H, const int32_t* slot_tok, const int* plan, int max_slots,
-                          void* xp, int* done, int n_done, cudaStream_t s) {
+                          void* xp, int* done, int n_done, int* flag, int flag_value, cudaStream_t s) {
     const int row_vec = H * (dtype == MOESTEP_F32 ? 4 : 2) / 16;
     if (dtype == MOESTEP_FP8)
         return launch_pdl(gather_kernel<true>, dim3(max_slots), dim3(256), 0, s, static_cast<const uint4*>(x),
-                          row_vec, slot_tok, plan, static_cast<uint4*>(xp), done, n_done);
+                          row_vec, slot_tok, plan, static_cast<uint4*>(xp), done, n_done, flag, flag_value);
     return launch_pdl(gather_kernel<false>, dim3(max_slots), dim3(256), 0, s, static_cast<const uint4*>(x), row_vec,
-                      slot_tok, plan, static_cast<uint4*>(xp), done, n_done);
+                      slot_tok, plan, static_cast<uint4*>(xp), done, n_done, flag, flag_value);
 }
 
 int route_combine_eligible(int act_dtype, int T, int H, int E, int k) {
