@@ -71,12 +71,15 @@ __host__ __device__ constexpr int smem_bytes(int nch) { return num_stages(nch) *
 // FP8 weights: shared memory is one long ring of slots that the TMA warp fills far
 // ahead, each with one 128 x 128 E4M3 weight tile (a K block of 128) and its token
 // rows as two 64-wide B boxes (the MMA's B operand, read in place).  The converted f16
-// A operands live in tensor memory (kF8AStages stages of 64 columns from column
-// kF8AColumn), so the conversion adds no shared-memory traffic beyond reading the FP8
+// A operands live in tensor memory (f8_a_stages stages of 64 columns from column
+// f8_a_column), so the conversion adds no shared-memory traffic beyond reading the FP8
 // tile once; eight MMAs per K block share one wait and two commits.
 constexpr int kF8Tile = 16384;    // 128 rows x 128 E4M3 bytes
-constexpr int kF8AStages = 4;     // f16 A operands in TMEM
-constexpr int kF8AColumn = 256;   // their first TMEM column (accumulators use 0 .. 2 NCH - 1 <= 128)
+// f16 A operands in TMEM after the accumulators (two MMA warps x two buffers x NCH columns):
+// as many 64-column stages as the 512 columns leave, an even number (each converter group owns
+// every other stage)
+__host__ __device__ constexpr int f8_a_column(int nch) { return 4 * nch; }
+__host__ __device__ constexpr int f8_a_stages(int nch) { return ((512 - 4 * nch) / 64) & ~1; }
 __host__ __device__ constexpr int f8_slot_bytes(int nch) { return kF8Tile + 2 * nch * 128; }
 // Even, so that with two TMA warps taking alternate K blocks each slot is always filled by
 // the same warp: a warp then never reaches a slot's next use before it filled the current
@@ -85,7 +88,7 @@ __host__ __device__ constexpr int f8_slots(int nch) {
     return ((kSmemBudget - 1024) / f8_slot_bytes(nch) > 24 ? 24 : (kSmemBudget - 1024) / f8_slot_bytes(nch)) & ~1;
 }
 static_assert(f8_slots(32) % 2 == 0 && f8_slots(64) % 2 == 0 && f8_slots(64) >= 4, "FP8 slot ring");
-static_assert(kF8AStages % 2 == 0, "each converter group must own its A stages");
+static_assert(f8_a_stages(32) == 6 && f8_a_stages(64) == 4, "FP8 A stages in tensor memory");
 __host__ __device__ constexpr int smem_bytes_f8(int nch) { return f8_slots(nch) * f8_slot_bytes(nch) + 1024 + 1024; }
 
 struct Unit {
@@ -243,7 +246,7 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ TensorMaps maps, const GemmParams p) {
     constexpr bool EXP = MODE == kExperts || MODE == kExpertsF8;  // whole routed + shared FFN
     constexpr bool F8 = MODE == kExpertsF8;                       // FP8 weights, converted in shared memory
-    constexpr int STAGES = F8 ? kF8AStages : num_stages(NCH);  // F8: A stages in TMEM
+    constexpr int STAGES = F8 ? f8_a_stages(NCH) : num_stages(NCH);  // F8: A stages in TMEM
     constexpr int SB = F8 ? 0 : stage_bytes(NCH);
     constexpr int S8 = F8 ? f8_slots(NCH) : 0;            // F8: slots of FP8 tile + token rows
     constexpr int SL = f8_slot_bytes(NCH);
@@ -520,7 +523,7 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
                     }
                     tc::fence_after_sync();
                     if (F8) {
-                        const uint32_t at = tmem_base + static_cast<uint32_t>(kF8AColumn + 64 * stage);
+                        const uint32_t at = tmem_base + static_cast<uint32_t>(f8_a_column(NCH) + 64 * stage);
                         const uint32_t sb = tc::smem_addr(f8ring + slot * SL + kF8Tile + mh * NCH * 128);
                         uint64_t bd[4];  // this warp's 64-wide half of the K block, four K = 16 steps
 #pragma unroll
@@ -713,7 +716,7 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
         // slot's FP8 tile (128 bytes, 16-byte chunk j of row r at chunk j ^ (r & 7): the
         // TMA's 128-byte swizzle, so a warp's reads hit distinct banks) into 64 f16x2 words
         // (values times 2^-8, exactly) and stores them as TMEM lane 32q + i, columns
-        // kF8AColumn + 64 stage ..: A row i in lane i, elements 2c, 2c+1 in column c.
+        // f8_a_column(NCH) + 64 stage ..: A row i in lane i, elements 2c, 2c+1 in column c.
         const int q = warp & 3;
         const int grp = (warp - 6) >> 2;
         const int row = 32 * q + lane;
@@ -738,21 +741,18 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
                 }
                 tc::fence_after_sync();
                 const uint4* src = reinterpret_cast<const uint4*>(f8ring + slot * SL + 128 * row);
+                uint32_t h[64];  // the row's 128 codes as 64 f16x2 words, stored with one instruction
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t h[32];
+                for (int i = 0; i < 8; ++i) {
+                    const uint4 v = src[i ^ (row & 7)];
+                    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const uint4 v = src[(4 * half + i) ^ (row & 7)];
-                        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            h[8 * i + 2 * j] = tc::e4m3x2_to_f16x2_div256(wv[j], 0);
-                            h[8 * i + 2 * j + 1] = tc::e4m3x2_to_f16x2_div256(wv[j], 2);
-                        }
+                    for (int j = 0; j < 4; ++j) {
+                        h[8 * i + 2 * j] = tc::e4m3x2_to_f16x2_div256(wv[j], 0);
+                        h[8 * i + 2 * j + 1] = tc::e4m3x2_to_f16x2_div256(wv[j], 2);
                     }
-                    tc::tmem_st32(lane_base + static_cast<uint32_t>(kF8AColumn + 64 * stage + 32 * half), h);
                 }
+                tc::tmem_st64(lane_base + static_cast<uint32_t>(f8_a_column(NCH) + 64 * stage), h);
                 tc::fence_before_sync();
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(&conv[stage]);
