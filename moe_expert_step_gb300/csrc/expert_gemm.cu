@@ -31,9 +31,12 @@
 //                 LM head: per position and 32-row slice: (max, argmax, sum exp)
 //
 // FP8 E4M3 weights (kExpertsF8, 512 threads), K blocks of 128:
-//   warps 0, 15 TMA producers on alternate K blocks: a ring of shared-memory
-//               slots, each one 128 x 128-byte FP8 tile (128-byte swizzle) and
-//               its token rows as two 64-wide f16 B boxes.
+//   warp 0      TMA producer of the A ring: 128 x 128-byte FP8 weight tiles
+//               (128-byte swizzle), one per K block; a slot is free again as
+//               soon as its converters have read it into registers.
+//   warp 15     TMA producer of the B ring: each K block's token rows as two
+//               64-wide f16 B boxes; B slot i goes with TMEM A stage i and is
+//               free again with it, at the MMAs' commit.
 //   warps 6-13  converters, two groups of four on alternate K blocks: each
 //               warp turns the 32 tile rows of its TMEM lane quarter into f16
 //               (exact, values times 2^-8) and stores them with tcgen05.st
@@ -56,7 +59,7 @@ constexpr int kThreads = 192;
 constexpr int kThreadsF8 = 512;  // + eight converter warps (two groups of four), a second MMA warp and a
                                  // second TMA warp
 constexpr int kMmaWarp2 = 14;    // FP8: issues the second 64-wide half of each K block into its own accumulator
-constexpr int kTmaWarp2 = 15;    // FP8: loads the odd K blocks' slots
+constexpr int kTmaWarp2 = 15;    // FP8: loads the token rows (B ring); warp 0 loads the weight tiles
 constexpr uint64_t kTeardownNs = 1000000000ull;  // fixed limit for draining in-flight copies/MMAs
 constexpr int kABytes = 16384;            // 128 rows x 64 bf16
 constexpr int kBoxBBytes = 16 * 128;      // 16 rows x 64 bf16
@@ -68,28 +71,35 @@ __host__ __device__ constexpr int num_stages(int nch) {
 }
 __host__ __device__ constexpr int smem_bytes(int nch) { return num_stages(nch) * stage_bytes(nch) + 512 + 1024; }
 
-// FP8 weights: shared memory is one long ring of slots that the TMA warp fills far
-// ahead, each with one 128 x 128 E4M3 weight tile (a K block of 128) and its token
-// rows as two 64-wide B boxes (the MMA's B operand, read in place).  The converted f16
-// A operands live in tensor memory (f8_a_stages stages of 64 columns from column
-// f8_a_column), so the conversion adds no shared-memory traffic beyond reading the FP8
-// tile once; eight MMAs per K block share one wait and two commits.
+// FP8 weights: shared memory holds two rings that two TMA warps fill far ahead.  The
+// A ring holds 128 x 128 E4M3 weight tiles (a K block of 128); a tile's slot is
+// released as soon as its converters hold it in registers, so the weight stream does
+// not wait out the MMAs.  The converted f16 A operands live in tensor memory
+// (f8_a_stages stages of 64 columns from column f8_a_column), so the conversion adds no
+// shared-memory traffic beyond reading the FP8 tile once.  The B ring has one slot per
+// A stage with the K block's token rows as two 64-wide B boxes (the MMA's B operand,
+// read in place); a stage's converters arrive only once its token rows have landed, so
+// each MMA warp waits once and commits once per K block (four MMAs): the tensor pipe,
+// not the HBM stream, is what small token counts make scarce here.
 constexpr int kF8Tile = 16384;    // 128 rows x 128 E4M3 bytes
 // f16 A operands in TMEM after the accumulators (two MMA warps x two buffers x NCH columns):
 // as many 64-column stages as the 512 columns leave, an even number (each converter group owns
 // every other stage)
 __host__ __device__ constexpr int f8_a_column(int nch) { return 4 * nch; }
 __host__ __device__ constexpr int f8_a_stages(int nch) { return ((512 - 4 * nch) / 64) & ~1; }
-__host__ __device__ constexpr int f8_slot_bytes(int nch) { return kF8Tile + 2 * nch * 128; }
-// Even, so that with two TMA warps taking alternate K blocks each slot is always filled by
-// the same warp: a warp then never reaches a slot's next use before it filled the current
-// one, which the parity waits on the slot's barriers rely on (they tell two phases apart).
-__host__ __device__ constexpr int f8_slots(int nch) {
-    return ((kSmemBudget - 1024) / f8_slot_bytes(nch) > 24 ? 24 : (kSmemBudget - 1024) / f8_slot_bytes(nch)) & ~1;
+__host__ __device__ constexpr int f8_b_bytes(int nch) { return 2 * nch * 128; }  // one B slot
+__host__ __device__ constexpr int f8_b_slots(int nch) { return f8_a_stages(nch); }
+// The rest of shared memory, an even number of slots (so that each A slot is always read by the
+// same converter group).
+__host__ __device__ constexpr int f8_a_slots(int nch) {
+    return ((kSmemBudget - 1024 - f8_b_slots(nch) * f8_b_bytes(nch)) / kF8Tile) & ~1;
 }
-static_assert(f8_slots(32) % 2 == 0 && f8_slots(64) % 2 == 0 && f8_slots(64) >= 4, "FP8 slot ring");
+static_assert(f8_a_slots(32) == 10 && f8_a_slots(64) == 10, "FP8 weight-tile ring");
 static_assert(f8_a_stages(32) == 6 && f8_a_stages(64) == 4, "FP8 A stages in tensor memory");
-__host__ __device__ constexpr int smem_bytes_f8(int nch) { return f8_slots(nch) * f8_slot_bytes(nch) + 1024 + 1024; }
+__host__ __device__ constexpr int smem_bytes_f8(int nch) {
+    return f8_a_slots(nch) * kF8Tile + f8_b_slots(nch) * f8_b_bytes(nch) + 1024 + 1024;
+}
+static_assert(smem_bytes_f8(32) <= 232448 && smem_bytes_f8(64) <= 232448, "FP8 shared memory");
 
 struct Unit {
     int kb, rowA0, rowA1, slot0, n, mt, c;
@@ -193,15 +203,18 @@ __device__ __forceinline__ void record_timeout(int* err, int role, int u, int kb
     }
 }
 
-// Units of the bf16 expert launch are handed out at run time: the producer warp takes each
-// next unit index from a global counter (so CTAs that stream faster take more units and the
-// launch ends together) and publishes it in a ring of kUnitQ shared-memory entries that the
-// MMA warp and the four epilogue warps read in the same order.  Gate/up units have the lower
+// Units of the expert launches are handed out at run time: the (weight) producer warp takes
+// each next unit index from a global counter (so CTAs that stream faster take more units and
+// the launch ends together) and publishes it in a ring of kUnitQ shared-memory entries that
+// every other role's warps read in the same order (bf16: the MMA warp and the four epilogue
+// warps; FP8 also the token-row producer, the second MMA warp and the eight converters).  Gate/up units have the lower
 // indices, so every gate/up unit is taken before any down unit, as with the static order.
 constexpr int kUnitQ = 8;
+constexpr int kUnitReaders = 5;     // bf16: MMA + 4 epilogue warps
+constexpr int kUnitReadersF8 = 15;  // FP8: B producer, 2 MMA, 4 epilogue and 8 converter warps
 struct UnitRing {
     uint64_t* full;   // [kUnitQ] the producer wrote the entry (count 1)
-    uint64_t* empty;  // [kUnitQ] the MMA warp and the four epilogue warps read it (count 5)
+    uint64_t* empty;  // [kUnitQ] every reader warp read it (count kUnitReaders / kUnitReadersF8)
     int* idx;         // [kUnitQ] unit index, or -1: no more units
 };
 
@@ -248,24 +261,28 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
     constexpr bool F8 = MODE == kExpertsF8;                       // FP8 weights, converted in shared memory
     constexpr int STAGES = F8 ? f8_a_stages(NCH) : num_stages(NCH);  // F8: A stages in TMEM
     constexpr int SB = F8 ? 0 : stage_bytes(NCH);
-    constexpr int S8 = F8 ? f8_slots(NCH) : 0;            // F8: slots of FP8 tile + token rows
-    constexpr int SL = f8_slot_bytes(NCH);
+    constexpr int SA = F8 ? f8_a_slots(NCH) : 0;          // F8: weight-tile slots
+    constexpr int SBR = F8 ? f8_b_slots(NCH) : 0;         // F8: token-row slots
+    constexpr int BL = f8_b_bytes(NCH);
     constexpr uint32_t TMEM_COLS = F8 ? 512u : ((2 * NCH < 32) ? 32u : static_cast<uint32_t>(2 * NCH));
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* f8ring = smem + STAGES * SB;  // F8: S8 slots of SL bytes
-    uint64_t* bars = reinterpret_cast<uint64_t*>(f8ring + S8 * SL);
+    uint8_t* aring = smem + STAGES * SB;  // F8: SA weight tiles of kF8Tile bytes
+    uint8_t* bring = aring + SA * kF8Tile;  // F8: SBR token-row slots of BL bytes
+    uint64_t* bars = reinterpret_cast<uint64_t*>(bring + SBR * BL);
     uint64_t* full = bars;
     uint64_t* empty = bars + STAGES;
     uint64_t* tfull = bars + 2 * STAGES;
     uint64_t* tempty = tfull + 2;
     uint64_t* fin = tempty + 2;
     uint64_t* conv = fin + 1;            // F8: the stage's weight tile is converted (count 1)
-    uint64_t* full8 = conv + STAGES;     // F8: the slot's FP8 tile and token rows landed (TMA bytes)
-    uint64_t* empty8 = full8 + S8;       // F8: the MMA is done with the slot (count 1)
-    constexpr bool DYN = MODE == kExperts;  // units handed out at run time (UnitRing)
-    const UnitRing ring{empty8 + S8, empty8 + S8 + kUnitQ, reinterpret_cast<int*>(empty8 + S8 + 2 * kUnitQ)};
+    uint64_t* fullA = conv + STAGES;     // F8: the weight tile landed (TMA bytes)
+    uint64_t* emptyA = fullA + SA;       // F8: its four converter warps read it (count 4)
+    uint64_t* fullB = emptyA + SA;       // F8: the token rows landed (TMA bytes); freed with empty[]
+    uint64_t* rend = fullB + SBR;
+    constexpr bool DYN = EXP;  // units handed out at run time (UnitRing)
+    const UnitRing ring{rend, rend + kUnitQ, reinterpret_cast<int*>(rend + 2 * kUnitQ)};
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(ring.idx + kUnitQ);
     int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
     int* zero_flag = abort_flag + 1;
@@ -286,14 +303,15 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
         if (DYN)
             for (int q = 0; q < kUnitQ; ++q) {
                 tc::mbar_init(&ring.full[q], 1);
-                tc::mbar_init(&ring.empty[q], 5);
+                tc::mbar_init(&ring.empty[q], F8 ? kUnitReadersF8 : kUnitReaders);
             }
         if (F8) {
             for (int s = 0; s < STAGES; ++s) tc::mbar_init(&conv[s], 4);  // one arrival per warp of a group
-            for (int s = 0; s < S8; ++s) {
-                tc::mbar_init(&full8[s], 1);
-                tc::mbar_init(&empty8[s], 2);  // both MMA warps release a slot
+            for (int s = 0; s < SA; ++s) {
+                tc::mbar_init(&fullA[s], 1);
+                tc::mbar_init(&emptyA[s], 4);
             }
+            for (int s = 0; s < SBR; ++s) tc::mbar_init(&fullB[s], 1);
         }
         *abort_flag = 0;
         *zero_flag = 0;
@@ -332,24 +350,75 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
     volatile int* abortv = abort_flag;
     const uint64_t tmo = p.timeout_ns;
 
-    if (F8 && (warp == 0 || warp == kTmaWarp2)) {
-        // ------------------------------------------------------------ FP8 tile producers
-        // Fill the slot ring in unit / K-block order, far ahead of the MMAs: warp 0 the even
-        // K blocks, warp kTmaWarp2 the odd ones (one TMA issuer alone does not keep up).
-        const int pg = warp == 0 ? 0 : 1;
+    if (F8 && warp == 0) {
+        // ------------------------------------------------------------ FP8 weight-tile producer
+        // Fills the A ring in unit / K-block order; needs nothing from other CTAs, so a down
+        // unit's tiles stream in while its chunk's SwiGLU rows are still being written.
         const uint64_t pol = tc::policy_evict_first();
         uint32_t issued = 0, issued_parity = 0;
-        constexpr int S8d = S8 > 0 ? S8 : 1;
+        constexpr int SAd = SA > 0 ? SA : 1;
         int seq = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        int qi = 0;
+        for (int u = blockIdx.x; ok; u += gridDim.x) {
+            if (!take_unit(ring, p.unit_ctr, n_units, qi, u, abortv, tmo)) {
+                ok = false;
+                if (lane == 0) record_timeout(p.err, 7, u, -1, -1, 0, n_units, 0);
+                break;
+            }
+            if (u < 0) break;
+            const Unit w = decode_unit<MODE, NCH>(u, p, nrc, nsc);
+            const CUtensorMap* mA = &maps.a[(w.dn ? 2 : 0) + (w.shared ? 1 : 0)];
+            for (int kb = 0; kb < w.kb; ++kb, ++seq) {
+                const int slot = seq % SAd;
+                const uint32_t ph = (seq / SAd) & 1u;
+                int good = 1;
+                if (lane == 0) {
+                    good = tc::mbar_wait(&emptyA[slot], ph ^ 1u, abortv, tmo);
+                    if (good) {
+                        tc::mbar_arrive_expect_tx(&fullA[slot], kF8Tile);
+                        tc::tma_load_2d_hint(aring + slot * kF8Tile, mA, &fullA[slot], kb * 128, w.rowA0, pol);
+                        issued |= 1u << slot;
+                        issued_parity = (issued_parity & ~(1u << slot)) | (ph << slot);
+                    }
+                }
+                good = __shfl_sync(0xffffffffu, good, 0);
+                if (!good) {
+                    ok = false;
+                    if (lane == 0) record_timeout(p.err, 1, u, kb, slot, ph, n_units, w.n);
+                    break;
+                }
+            }
+        }
+        if (lane == 0) {
+            if (!ok) {
+                *abort_flag = 1;
+                record_error(p.err, kErrTimeoutProducer);
+            }
+            for (int s = 0; s < SA; ++s)
+                if (issued & (1u << s)) tc::mbar_wait(&fullA[s], (issued_parity >> s) & 1u, zero_flag, kTeardownNs);
+        }
+        __syncwarp();
+    } else if (F8 && warp == kTmaWarp2) {
+        // ------------------------------------------------------------ FP8 token-row producer
+        // Fills the B ring in the same order, slot i once TMEM A stage i is free; a down
+        // unit's SwiGLU rows once its chunk's gate/up epilogues (any CTA) counted them stored.
+        uint32_t issued = 0, issued_parity = 0;
+        constexpr int SBd = SBR > 0 ? SBR : 1;
+        int seq = 0;
+        bool ok = true;
+        int qi = 0;
+        for (int u = blockIdx.x; ok; u += gridDim.x) {
+            if (!read_unit(ring, qi, u, abortv, tmo)) {
+                ok = false;
+                break;
+            }
+            if (u < 0) break;
             const Unit w = decode_unit<MODE, NCH>(u, p, nrc, nsc);
             const int nb = (w.n + 15) >> 4;
-            const CUtensorMap* mA = &maps.a[(w.dn ? 2 : 0) + (w.shared ? 1 : 0)];
             const CUtensorMap* mB = &maps.b[w.dn ? 1 : 0];
+            int good = 1;
             if (w.dn) {
-                // the SwiGLU rows of this chunk come from gate/up units of other CTAs
-                int good = 1;
                 if (lane == 0)
                     good = wait_count(&p.done[w.c], 4 * (w.shared ? p.shared_tiles : p.routed_tiles), abortv, tmo);
                 good = __shfl_sync(0xffffffffu, good, 0);
@@ -360,30 +429,26 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
                 }
             }
             for (int kb = 0; kb < w.kb; ++kb, ++seq) {
-                if ((seq & 1) != pg) continue;
-                const int slot = seq % S8d;
-                const uint32_t ph8 = (seq / S8d) & 1u;
-                int good = 1;
+                const int slot = seq % SBd;
+                const uint32_t ph = (seq / SBd) & 1u;
                 if (lane == 0) {
-                    good = tc::mbar_wait(&empty8[slot], ph8 ^ 1u, abortv, tmo);
+                    good = tc::mbar_wait(&empty[slot], ph ^ 1u, abortv, tmo);
                     if (good) {
-                        uint8_t* dst = f8ring + slot * SL;
-                        tc::mbar_arrive_expect_tx(&full8[slot], kF8Tile + 2 * nb * kBoxBBytes);
-                        tc::tma_load_2d_hint(dst, mA, &full8[slot], kb * 128, w.rowA0, pol);
+                        uint8_t* dst = bring + slot * BL;
+                        tc::mbar_arrive_expect_tx(&fullB[slot], 2 * nb * kBoxBBytes);
                         for (int b = 0; b < nb; ++b) {
-                            tc::tma_load_2d(dst + kF8Tile + b * kBoxBBytes, mB, &full8[slot], kb * 128,
+                            tc::tma_load_2d(dst + b * kBoxBBytes, mB, &fullB[slot], kb * 128, w.slot0 + 16 * b);
+                            tc::tma_load_2d(dst + NCH * 128 + b * kBoxBBytes, mB, &fullB[slot], kb * 128 + 64,
                                             w.slot0 + 16 * b);
-                            tc::tma_load_2d(dst + kF8Tile + NCH * 128 + b * kBoxBBytes, mB, &full8[slot],
-                                            kb * 128 + 64, w.slot0 + 16 * b);
                         }
                         issued |= 1u << slot;
-                        issued_parity = (issued_parity & ~(1u << slot)) | (ph8 << slot);
+                        issued_parity = (issued_parity & ~(1u << slot)) | (ph << slot);
                     }
                 }
                 good = __shfl_sync(0xffffffffu, good, 0);
                 if (!good) {
                     ok = false;
-                    if (lane == 0) record_timeout(p.err, 1, u, kb, slot, ph8, n_units, w.n);
+                    if (lane == 0) record_timeout(p.err, 1, u, kb, slot, ph, n_units, w.n);
                     break;
                 }
             }
@@ -393,8 +458,8 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
                 *abort_flag = 1;
                 record_error(p.err, kErrTimeoutProducer);
             }
-            for (int s = 0; s < S8; ++s)
-                if (issued & (1u << s)) tc::mbar_wait(&full8[s], (issued_parity >> s) & 1u, zero_flag, kTeardownNs);
+            for (int s = 0; s < SBR; ++s)
+                if (issued & (1u << s)) tc::mbar_wait(&fullB[s], (issued_parity >> s) & 1u, zero_flag, kTeardownNs);
         }
         __syncwarp();
     } else if (warp == 0) {
@@ -488,8 +553,6 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
         const int mh = (F8 && warp == kMmaWarp2) ? 1 : 0;
         int stage = 0;
         uint32_t phase = 0;
-        int slot = 0;  // F8: the slot holding this K block's token rows
-        uint32_t ph8 = 0;
         bool ok = true;
         int it = 0;
         int qi = 0;
@@ -515,7 +578,7 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
                 if (!good) record_timeout(p.err, 2, u, -1, buf, aph, n_units, w.n);
                 tc::fence_after_sync();
                 for (int kb = 0; kb < w.kb && good; ++kb) {
-                    // F8: the converted A operand (its converters saw the slot's token rows land)
+                    // F8: the converted A operand (its converters saw the token rows land)
                     good = tc::mbar_wait(F8 ? &conv[stage] : &full[stage], phase, abortv, tmo);
                     if (!good) {
                         record_timeout(p.err, 3, u, kb, stage, phase, n_units, w.n);
@@ -524,13 +587,12 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
                     tc::fence_after_sync();
                     if (F8) {
                         const uint32_t at = tmem_base + static_cast<uint32_t>(f8_a_column(NCH) + 64 * stage);
-                        const uint32_t sb = tc::smem_addr(f8ring + slot * SL + kF8Tile + mh * NCH * 128);
+                        const uint32_t sb = tc::smem_addr(bring + stage * BL + mh * NCH * 128);
                         uint64_t bd[4];  // this warp's 64-wide half of the K block, four K = 16 steps
 #pragma unroll
                         for (int k = 0; k < 4; ++k) bd[k] = tc::sdesc_k_sw128(sb + 32 * k);
                         tc::mma4_f16_tmem_a(d_tmem, at + 32 * mh, bd, idesc, kb != 0);
                         tc::mma_commit(&empty[stage]);
-                        tc::mma_commit(&empty8[slot]);
                     } else {
                         const uint32_t sa = tc::smem_addr(smem + stage * SB);
                         const uint32_t sb = sa + kABytes;
@@ -543,10 +605,6 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
-                    }
-                    if (F8 && ++slot == S8) {
-                        slot = 0;
-                        ph8 ^= 1u;
                     }
                 }
                 if (good) tc::mma_commit(&tfull[buf]);
@@ -712,39 +770,54 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
     } else if (F8 && warp < kMmaWarp2) {
         // ------------------------------------------------------------ FP8 -> f16 converters (warps 6..13)
         // Two groups of four warps take alternate K blocks.  Within a group each warp takes
-        // the 32 weight rows of its TMEM lane quarter; thread i converts row 32q + i of the
-        // slot's FP8 tile (128 bytes, 16-byte chunk j of row r at chunk j ^ (r & 7): the
-        // TMA's 128-byte swizzle, so a warp's reads hit distinct banks) into 64 f16x2 words
-        // (values times 2^-8, exactly) and stores them as TMEM lane 32q + i, columns
+        // the 32 weight rows of its TMEM lane quarter; thread i reads row 32q + i of the
+        // FP8 tile (128 bytes, 16-byte chunk j of row r at chunk j ^ (r & 7): the TMA's
+        // 128-byte swizzle, so a warp's reads hit distinct banks) and releases the A slot,
+        // then, once the TMEM stage is free, converts the row into 64 f16x2 words (values
+        // times 2^-8, exactly) and stores them as TMEM lane 32q + i, columns
         // f8_a_column(NCH) + 64 stage ..: A row i in lane i, elements 2c, 2c+1 in column c.
         const int q = warp & 3;
         const int grp = (warp - 6) >> 2;
         const int row = 32 * q + lane;
         const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(32 * q) << 16);
-        constexpr int S8d = S8 > 0 ? S8 : 1;
+        constexpr int SAd = SA > 0 ? SA : 1;
         bool ok = true;
         int seq = 0;
-        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        int qi = 0;
+        for (int u = blockIdx.x; ok; u += gridDim.x) {
+            if (!read_unit(ring, qi, u, abortv, tmo)) {
+                ok = false;
+                break;
+            }
+            if (u < 0) break;
             const Unit w = decode_unit<MODE, NCH>(u, p, nrc, nsc);
             for (int kb = 0; kb < w.kb; ++kb, ++seq) {
                 if ((seq & 1) != grp) continue;
                 const int stage = seq % STAGES;
                 const uint32_t phase = (seq / STAGES) & 1u;
-                const int slot = seq % S8d;
-                const uint32_t ph8 = (seq / S8d) & 1u;
-                const bool got = __all_sync(0xffffffffu, tc::mbar_wait(&empty[stage], phase ^ 1u, abortv, tmo) &&
-                                                             tc::mbar_wait(&full8[slot], ph8, abortv, tmo));
-                if (!got) {
+                const int slot = seq % SAd;
+                const uint32_t pha = (seq / SAd) & 1u;
+                if (!__all_sync(0xffffffffu, tc::mbar_wait(&fullA[slot], pha, abortv, tmo))) {
                     ok = false;
-                    if (lane == 0) record_timeout(p.err, 8, u, kb, slot, ph8, n_units, w.n);
+                    if (lane == 0) record_timeout(p.err, 8, u, kb, slot, pha, n_units, w.n);
+                    break;
+                }
+                const uint4* src = reinterpret_cast<const uint4*>(aring + slot * kF8Tile + 128 * row);
+                uint4 raw[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) raw[i] = src[i ^ (row & 7)];
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&emptyA[slot]);  // the tile is in registers
+                if (!__all_sync(0xffffffffu, tc::mbar_wait(&empty[stage], phase ^ 1u, abortv, tmo))) {
+                    ok = false;
+                    if (lane == 0) record_timeout(p.err, 9, u, kb, stage, phase, n_units, w.n);
                     break;
                 }
                 tc::fence_after_sync();
-                const uint4* src = reinterpret_cast<const uint4*>(f8ring + slot * SL + 128 * row);
                 uint32_t h[64];  // the row's 128 codes as 64 f16x2 words, stored with one instruction
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    const uint4 v = src[i ^ (row & 7)];
+                    const uint4 v = raw[i];
                     const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
@@ -754,7 +827,12 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
                 }
                 tc::tmem_st64(lane_base + static_cast<uint32_t>(f8_a_column(NCH) + 64 * stage), h);
                 tc::fence_before_sync();
-                __syncwarp();
+                // the stage's token rows have landed before the MMA warps may read them
+                if (!__all_sync(0xffffffffu, lane != 0 || tc::mbar_wait(&fullB[stage], phase, abortv, tmo))) {
+                    ok = false;
+                    if (lane == 0) record_timeout(p.err, 10, u, kb, stage, phase, n_units, w.n);
+                    break;
+                }
                 if (lane == 0) tc::mbar_arrive(&conv[stage]);
             }
         }
