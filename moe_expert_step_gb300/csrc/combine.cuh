@@ -158,4 +158,91 @@ __device__ void combine_row(int t, int H, int k, const float* __restrict__ y, co
     }
 }
 
+// combine_row (MODE 1 or 2) for one token by all 512 threads of the block, H <= 2048:
+// thread gt + 256 takes the second 1024-column pass of thread gt, so every load of the
+// row is in flight at once.  Each column's arithmetic is combine_row's, and the sum of
+// squares is added in its order (thread gt's first-pass terms, then the second pass's,
+// then the same 256-thread tree), so the row is bit-identical.  s_slot / s_g / red are
+// one group's scratch, shared by both halves; pair holds 256 floats.
+template <typename T, int MODE, typename Sink = NoSink>
+__device__ void combine_row_pair(int t, int H, int k, const float* __restrict__ y, const int32_t* __restrict__ slot_of,
+                                 const int32_t* __restrict__ slot_sh, const float* __restrict__ gate_rr,
+                                 int has_shared, const float* __restrict__ h_in, float* __restrict__ h,
+                                 T* __restrict__ x, int* s_slot, float* s_g, float* red, float* pair, Sink sink,
+                                 bool slots_loaded) {
+    static_assert(MODE == 1 || MODE == 2, "residual modes only");
+    const int gt = threadIdx.x & 511;
+    const bool on = t >= 0;
+    if (MODE != 2 && !slots_loaded) {
+        if (on && gt < k) {
+            s_slot[gt] = slot_of[t * k + gt];
+            s_g[gt] = gate_rr[t * k + gt];
+        }
+        if (on && gt == 32) s_slot[32] = has_shared ? slot_sh[t] : -1;
+        __syncthreads();
+    }
+    const size_t row = static_cast<size_t>(on ? t : 0) * H;
+    const int c = (gt & 255) * 4 + 1024 * (gt >> 8);
+    const bool mine = on && c < H;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    float ss = 0.f;
+    if (mine) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (MODE != 2) {
+            const int ssl = s_slot[32];
+            const float4 vs = ssl >= 0 ? __ldg(reinterpret_cast<const float4*>(y + static_cast<size_t>(ssl) * H + c))
+                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int j0 = 0; j0 < k; j0 += 8) {
+                float4 w[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const int sl = (j0 + q < k) ? s_slot[j0 + q] : -1;
+                    w[q] = sl >= 0 ? __ldg(reinterpret_cast<const float4*>(y + static_cast<size_t>(sl) * H + c))
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    if (j0 + q < k && s_slot[j0 + q] >= 0) {
+                        const float g = s_g[j0 + q];
+                        acc.x += g * w[q].x;
+                        acc.y += g * w[q].y;
+                        acc.z += g * w[q].z;
+                        acc.w += g * w[q].w;
+                    }
+                }
+            }
+            if (ssl >= 0) {
+                acc.x += vs.x;
+                acc.y += vs.y;
+                acc.z += vs.z;
+                acc.w += vs.w;
+            }
+        }
+        const float4 base = *reinterpret_cast<const float4*>((MODE == 1 ? h : h_in) + row + c);
+        v = make_float4(base.x + acc.x, base.y + acc.y, base.z + acc.z, base.w + acc.w);
+        *reinterpret_cast<float4*>(h + row + c) = v;
+        ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+    }
+    if (gt >= 256) pair[gt - 256] = ss;
+    __syncthreads();
+    if (gt < 256) ss += pair[gt];
+    // the 256-thread tree of group_sum_256 over threads 0..255 (warps 8..15 take part in
+    // the shuffles only; their sums are not read)
+    ss = warp_sum(ss);
+    const int lane = threadIdx.x & 31, warp = gt >> 5;
+    if (lane == 0 && warp < 8) red[warp] = ss;
+    __syncthreads();
+    float tt = (gt < 8) ? red[gt] : 0.f;
+    if (warp == 0) tt = warp_sum(tt);
+    if (gt == 0) red[8] = tt;
+    __syncthreads();
+    const float tot = red[8];
+    const float inv = 1.0f / sqrtf(tot / static_cast<float>(H) + kRmsEps);
+    if (mine) {
+        const float4 n = make_float4(v.x * inv, v.y * inv, v.z * inv, v.w * inv);
+        store4<T>(x + row + c, n);
+        sink(c, n);
+    }
+}
+
 }  // namespace moestep

@@ -216,6 +216,7 @@ struct UnitRing {
     uint64_t* full;   // [kUnitQ] the producer wrote the entry (count 1)
     uint64_t* empty;  // [kUnitQ] every reader warp read it (count kUnitReaders / kUnitReadersF8)
     int* idx;         // [kUnitQ] unit index, or -1: no more units
+    int4* ent;        // FP8 [kUnitQ][2]: the unit decoded, {u, kb, rowA0, slot0}, {n, mt, c, shared | dn << 1}
 };
 
 // Producer warp: the next unit (or -1), taken from *ctr by lane 0 and published in the ring;
@@ -254,6 +255,54 @@ __device__ __forceinline__ bool read_unit(const UnitRing& r, int& qi, int& u, vo
     return __shfl_sync(0xffffffffu, good, 0) != 0;
 }
 
+// FP8 launch: the producer also decodes the unit and publishes it decoded, so the MMA
+// warps, which bound that launch, and the other roles spend no chunk-list read per unit
+// (in the bf16 launch every warp decodes the index itself, in parallel with the others).
+template <int MODE, int NCH>
+__device__ __forceinline__ bool take_unit_f8(const UnitRing& r, const GemmParams& p, int nrc, int nsc, int n_units,
+                                             int& qi, int& u, Unit& w, volatile int* abort, uint64_t tmo) {
+    const int e = qi % kUnitQ;
+    int good = 1;
+    if ((threadIdx.x & 31) == 0) {
+        good = tc::mbar_wait(&r.empty[e], ((qi / kUnitQ) & 1) ^ 1u, abort, tmo);
+        if (good) {
+            int v = atomicAdd(p.unit_ctr, 1);
+            if (v >= n_units) v = -1;
+            Unit d{};
+            if (v >= 0) d = decode_unit<MODE, NCH>(v, p, nrc, nsc);
+            r.ent[2 * e] = make_int4(v, d.kb, d.rowA0, d.slot0);
+            r.ent[2 * e + 1] = make_int4(d.n, d.mt, d.c, (d.shared ? 1 : 0) | (d.dn ? 2 : 0));
+            tc::mbar_arrive(&r.full[e]);
+        }
+    }
+    ++qi;
+    good = __shfl_sync(0xffffffffu, good, 0);
+    __syncwarp();  // lane 0's entry, read back by every lane
+    if (good) {
+        const int4 a = r.ent[2 * e], b = r.ent[2 * e + 1];
+        u = a.x;
+        w = Unit{a.y, a.z, a.z + 64, a.w, b.x, b.y, b.z, (b.w & 1) != 0, (b.w & 2) != 0};
+    }
+    return good != 0;
+}
+
+// FP8 reader warp: the next unit, decoded (u = -1: none left); false if the wait gave up.
+__device__ __forceinline__ bool read_unit_f8(const UnitRing& r, int& qi, int& u, Unit& w, volatile int* abort,
+                                             uint64_t tmo) {
+    const int e = qi % kUnitQ;
+    int good = 1;
+    if ((threadIdx.x & 31) == 0) good = tc::mbar_wait(&r.full[e], (qi / kUnitQ) & 1, abort, tmo);
+    good = __shfl_sync(0xffffffffu, good, 0);
+    ++qi;
+    if (!good) return false;
+    const int4 a = r.ent[2 * e], b = r.ent[2 * e + 1];
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) tc::mbar_arrive(&r.empty[e]);
+    u = a.x;
+    w = Unit{a.y, a.z, a.z + 64, a.w, b.x, b.y, b.z, (b.w & 1) != 0, (b.w & 2) != 0};
+    return true;
+}
+
 template <int MODE, int NCH>
 __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ TensorMaps maps, const GemmParams p) {
@@ -282,8 +331,15 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
     uint64_t* fullB = emptyA + SA;       // F8: the token rows landed (TMA bytes); freed with empty[]
     uint64_t* rend = fullB + SBR;
     constexpr bool DYN = EXP;  // units handed out at run time (UnitRing)
-    const UnitRing ring{rend, rend + kUnitQ, reinterpret_cast<int*>(rend + 2 * kUnitQ)};
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(ring.idx + kUnitQ);
+    int* ring_idx = reinterpret_cast<int*>(rend + 2 * kUnitQ);
+    // F8: the decoded entries after the indices, 16-byte aligned (within the barrier area)
+    int4* ring_ent = F8 ? reinterpret_cast<int4*>((reinterpret_cast<uintptr_t>(ring_idx + kUnitQ) + 15) & ~uintptr_t(15))
+                        : nullptr;
+    static_assert(!F8 || (3 * STAGES + 5 + 2 * SA + SBR + 2 * kUnitQ) * 8 + 4 * kUnitQ + 16 + 2 * kUnitQ * 16 + 16 <= 1024,
+                  "FP8 barrier area");
+    const UnitRing ring{rend, rend + kUnitQ, ring_idx, ring_ent};
+    uint32_t* tmem_holder =
+        F8 ? reinterpret_cast<uint32_t*>(ring_ent + 2 * kUnitQ) : reinterpret_cast<uint32_t*>(ring.idx + kUnitQ);
     int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
     int* zero_flag = abort_flag + 1;
 
@@ -361,13 +417,13 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
         bool ok = true;
         int qi = 0;
         for (int u = blockIdx.x; ok; u += gridDim.x) {
-            if (!take_unit(ring, p.unit_ctr, n_units, qi, u, abortv, tmo)) {
+            Unit w;
+            if (!take_unit_f8<MODE, NCH>(ring, p, nrc, nsc, n_units, qi, u, w, abortv, tmo)) {
                 ok = false;
                 if (lane == 0) record_timeout(p.err, 7, u, -1, -1, 0, n_units, 0);
                 break;
             }
             if (u < 0) break;
-            const Unit w = decode_unit<MODE, NCH>(u, p, nrc, nsc);
             const CUtensorMap* mA = &maps.a[(w.dn ? 2 : 0) + (w.shared ? 1 : 0)];
             for (int kb = 0; kb < w.kb; ++kb, ++seq) {
                 const int slot = seq % SAd;
@@ -409,12 +465,12 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
         bool ok = true;
         int qi = 0;
         for (int u = blockIdx.x; ok; u += gridDim.x) {
-            if (!read_unit(ring, qi, u, abortv, tmo)) {
+            Unit w;
+            if (!read_unit_f8(ring, qi, u, w, abortv, tmo)) {
                 ok = false;
                 break;
             }
             if (u < 0) break;
-            const Unit w = decode_unit<MODE, NCH>(u, p, nrc, nsc);
             const int nb = (w.n + 15) >> 4;
             const CUtensorMap* mB = &maps.b[w.dn ? 1 : 0];
             int good = 1;
@@ -544,13 +600,79 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
                 if (issued & (1u << s)) tc::mbar_wait(&full[s], (issued_parity >> s) & 1u, zero_flag, kTeardownNs);
         }
         __syncwarp();
-    } else if (warp == 1 || (F8 && warp == kMmaWarp2)) {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (F8 && (warp == 1 || warp == kMmaWarp2)) {
+        // ------------------------------------------------------------ FP8 MMA issuers
+        // Lane 0 alone runs the role, unit reads included (no warp-wide step per unit: these
+        // two warps bound the FP8 launch); the other lanes wait at the end.  Warp 1 issues
+        // the first 64-wide half of every K block into accumulator 0, warp kMmaWarp2 the
+        // second half into accumulator 1 (TMEM columns 2 NCH ..); the epilogue adds the two.
+        const int mh = warp == kMmaWarp2 ? 1 : 0;
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            int qi = 0;
+            for (int it = 0;; ++it) {
+                int u;
+                Unit w;
+                const int e = qi % kUnitQ;
+                if (!tc::mbar_wait(&ring.full[e], (qi / kUnitQ) & 1, abortv, tmo)) {
+                    ok = false;
+                    break;
+                }
+                ++qi;
+                const int4 a = ring.ent[2 * e], b = ring.ent[2 * e + 1];
+                tc::mbar_arrive(&ring.empty[e]);
+                u = a.x;
+                if (u < 0) break;
+                w = Unit{a.y, a.z, a.z + 64, a.w, b.x, b.y, b.z, (b.w & 1) != 0, (b.w & 2) != 0};
+                const int buf = it & 1;
+                const uint32_t aph = (it >> 1) & 1;
+                const int N = ((w.n + 15) >> 4) << 4;
+                const uint32_t idesc = tc::idesc_f16(128, N);
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(mh * 2 * NCH + buf * NCH);
+                bool good = tc::mbar_wait(&tempty[buf], aph ^ 1u, abortv, tmo);
+                if (!good) record_timeout(p.err, 2, u, -1, buf, aph, n_units, w.n);
+                tc::fence_after_sync();
+                for (int kb = 0; kb < w.kb && good; ++kb) {
+                    // the converted A operand (its converters saw the token rows land)
+                    good = tc::mbar_wait(&conv[stage], phase, abortv, tmo);
+                    if (!good) {
+                        record_timeout(p.err, 3, u, kb, stage, phase, n_units, w.n);
+                        break;
+                    }
+                    tc::fence_after_sync();
+                    const uint32_t at = tmem_base + static_cast<uint32_t>(f8_a_column(NCH) + 64 * stage);
+                    const uint32_t sb = tc::smem_addr(bring + stage * BL + mh * NCH * 128);
+                    uint64_t bd[4];  // this warp's 64-wide half of the K block, four K = 16 steps
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) bd[k] = tc::sdesc_k_sw128(sb + 32 * k);
+                    tc::mma4_f16_tmem_a(d_tmem, at + 32 * mh, bd, idesc, kb != 0);
+                    tc::mma_commit(&empty[stage]);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!good) {
+                    ok = false;
+                    break;
+                }
+                tc::mma_commit(&tfull[buf]);
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                record_error(p.err, kErrTimeoutMma);
+            }
+            // every MMA issued here has finished before TMEM and shared memory are released
+            tc::mma_commit(fin);
+            tc::mbar_wait(fin, 0, zero_flag, kTeardownNs);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer (bf16)
         // Lane 0 alone walks a unit's K blocks (no warp-wide step per block); the warp
-        // agrees on success once per unit.  F8: two MMA warps, warp 1 issuing the first
-        // 64-wide half of every K block into accumulator 0 and warp kMmaWarp2 the second
-        // half into accumulator 1 (TMEM columns 2 NCH ..); the epilogue adds the two.
-        const int mh = (F8 && warp == kMmaWarp2) ? 1 : 0;
+        // agrees on success once per unit.
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
@@ -570,38 +692,27 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
             const int buf = it & 1;
             const uint32_t aph = (it >> 1) & 1;
             const int N = ((w.n + 15) >> 4) << 4;
-            const uint32_t idesc = F8 ? tc::idesc_f16(128, N) : tc::idesc_bf16(128, N);
-            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(mh * 2 * NCH + buf * NCH);
+            const uint32_t idesc = tc::idesc_bf16(128, N);
+            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * NCH);
             int good = 1;
             if (lane == 0) {
                 good = tc::mbar_wait(&tempty[buf], aph ^ 1u, abortv, tmo);
                 if (!good) record_timeout(p.err, 2, u, -1, buf, aph, n_units, w.n);
                 tc::fence_after_sync();
                 for (int kb = 0; kb < w.kb && good; ++kb) {
-                    // F8: the converted A operand (its converters saw the token rows land)
-                    good = tc::mbar_wait(F8 ? &conv[stage] : &full[stage], phase, abortv, tmo);
+                    good = tc::mbar_wait(&full[stage], phase, abortv, tmo);
                     if (!good) {
                         record_timeout(p.err, 3, u, kb, stage, phase, n_units, w.n);
                         break;
                     }
                     tc::fence_after_sync();
-                    if (F8) {
-                        const uint32_t at = tmem_base + static_cast<uint32_t>(f8_a_column(NCH) + 64 * stage);
-                        const uint32_t sb = tc::smem_addr(bring + stage * BL + mh * NCH * 128);
-                        uint64_t bd[4];  // this warp's 64-wide half of the K block, four K = 16 steps
+                    const uint32_t sa = tc::smem_addr(smem + stage * SB);
+                    const uint32_t sb = sa + kABytes;
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) bd[k] = tc::sdesc_k_sw128(sb + 32 * k);
-                        tc::mma4_f16_tmem_a(d_tmem, at + 32 * mh, bd, idesc, kb != 0);
-                        tc::mma_commit(&empty[stage]);
-                    } else {
-                        const uint32_t sa = tc::smem_addr(smem + stage * SB);
-                        const uint32_t sb = sa + kABytes;
-#pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            tc::mma_bf16(d_tmem, tc::sdesc_k_sw128(sa + 32 * k), tc::sdesc_k_sw128(sb + 32 * k),
-                                         idesc, (kb | k) != 0);
-                        tc::mma_commit(&empty[stage]);
-                    }
+                    for (int k = 0; k < 4; ++k)
+                        tc::mma_bf16(d_tmem, tc::sdesc_k_sw128(sa + 32 * k), tc::sdesc_k_sw128(sb + 32 * k), idesc,
+                                     (kb | k) != 0);
+                    tc::mma_commit(&empty[stage]);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -628,8 +739,9 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
         int it = 0;
         int qi = 0;
         for (int u = blockIdx.x;; u += gridDim.x, ++it) {
+            Unit w;
             if (DYN) {
-                if (!read_unit(ring, qi, u, abortv, tmo)) {
+                if (!(F8 ? read_unit_f8(ring, qi, u, w, abortv, tmo) : read_unit(ring, qi, u, abortv, tmo))) {
                     if (lane == 0) {
                         *abort_flag = 1;
                         record_error(p.err, kErrTimeoutEpilogue);
@@ -640,7 +752,7 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
             } else if (u >= n_units) {
                 break;
             }
-            const Unit w = decode_unit<MODE, NCH>(u, p, nrc, nsc);
+            if (!F8) w = decode_unit<MODE, NCH>(u, p, nrc, nsc);
             const int buf = it & 1;
             const uint32_t aph = (it >> 1) & 1;
             int good = tc::mbar_wait(&tfull[buf], aph, abortv, tmo);
@@ -785,12 +897,12 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
         int seq = 0;
         int qi = 0;
         for (int u = blockIdx.x; ok; u += gridDim.x) {
-            if (!read_unit(ring, qi, u, abortv, tmo)) {
+            Unit w;
+            if (!read_unit_f8(ring, qi, u, w, abortv, tmo)) {
                 ok = false;
                 break;
             }
             if (u < 0) break;
-            const Unit w = decode_unit<MODE, NCH>(u, p, nrc, nsc);
             for (int kb = 0; kb < w.kb; ++kb, ++seq) {
                 if ((seq & 1) != grp) continue;
                 const int stage = seq % STAGES;

@@ -968,6 +968,22 @@ __global__ void __launch_bounds__(kRouteTcThreads, 1) route_combine_kernel(Route
     pdl_wait();
     // 1. combine of this CTA's tokens of the tile; each normalised row also goes to the
     //    x tile of every CTA of the cluster (rows past the block's last token are zero)
+    if (CL >= 8 && H <= 2048) {
+        // one token per CTA: both groups of 256 threads take its row (all loads in flight at once)
+        const int t = t0 + rank < T ? t0 + rank : -1;
+        const ClusterRowSink sink{xs, rank * LD, CL};
+        int* s0 = c_slot - 33 * grp;  // group 0's scratch (the preload filled it)
+        float* g0 = c_g - 33 * grp;
+        float* r0 = c_red - 9 * grp;
+        if (a.mode == 1)
+            combine_row_pair<bf16, 1>(t, H, k, a.y, a.slot_of, a.slot_sh, a.gate_rr_prev, a.has_shared, nullptr,
+                                      a.hres, a.x, s0, g0, r0, part, sink, pre);
+        else
+            combine_row_pair<bf16, 2>(t, H, k, nullptr, nullptr, nullptr, nullptr, 0, a.h_in, a.hres, a.x, s0, g0, r0,
+                                      part, sink, false);
+        if (t < 0)
+            for (int c = threadIdx.x * 4; c < H; c += 4 * kRouteTcThreads) sink(c, make_float4(0.f, 0.f, 0.f, 0.f));
+    } else {
     for (int j0 = 0; j0 < 8; j0 += 2 * CL) {
         const int j = j0 + rank + CL * grp;
         const int t = (j < 8 && t0 + j < T) ? t0 + j : -1;
@@ -980,6 +996,7 @@ __global__ void __launch_bounds__(kRouteTcThreads, 1) route_combine_kernel(Route
                                  nullptr, c_slot, c_g, c_red, sink);
         if (j < 8 && t < 0)
             for (int c = (threadIdx.x & 255) * 4; c < H; c += 1024) sink(c, make_float4(0.f, 0.f, 0.f, 0.f));
+    }
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
     cluster.sync();  // the tile's x rows and this CTA's router rows are in shared memory
