@@ -203,8 +203,9 @@ __device__ __forceinline__ void record_timeout(int* err, int role, int u, int kb
     }
 }
 
-// Units of the expert launches are handed out at run time: the (weight) producer warp takes
-// each next unit index from a global counter (so CTAs that stream faster take more units and
+// Units of the expert launches are handed out at run time: a CTA's first unit is its block
+// index (no counter round trip at the launch's start); the (weight) producer warp takes
+// each later unit index from a global counter (so CTAs that stream faster take more units and
 // the launch ends together) and publishes it in a ring of kUnitQ shared-memory entries that
 // every other role's warps read in the same order (bf16: the MMA warp and the four epilogue
 // warps; FP8 also the token-row producer, the second MMA warp and the eight converters).  Gate/up units have the lower
@@ -228,7 +229,8 @@ __device__ __forceinline__ bool take_unit(const UnitRing& r, int* ctr, int n_uni
         const int e = qi % kUnitQ;
         good = tc::mbar_wait(&r.empty[e], ((qi / kUnitQ) & 1) ^ 1u, abort, tmo);
         if (good) {
-            v = atomicAdd(ctr, 1);
+            // a CTA's first unit is its own index, the rest come from the counter
+            v = qi == 0 ? static_cast<int>(blockIdx.x) : static_cast<int>(gridDim.x) + atomicAdd(ctr, 1);
             if (v >= n_units) v = -1;
             r.idx[e] = v;
             tc::mbar_arrive(&r.full[e]);
@@ -266,7 +268,7 @@ __device__ __forceinline__ bool take_unit_f8(const UnitRing& r, const GemmParams
     if ((threadIdx.x & 31) == 0) {
         good = tc::mbar_wait(&r.empty[e], ((qi / kUnitQ) & 1) ^ 1u, abort, tmo);
         if (good) {
-            int v = atomicAdd(p.unit_ctr, 1);
+            int v = qi == 0 ? static_cast<int>(blockIdx.x) : static_cast<int>(gridDim.x) + atomicAdd(p.unit_ctr, 1);
             if (v >= n_units) v = -1;
             Unit d{};
             if (v >= 0) d = decode_unit<MODE, NCH>(v, p, nrc, nsc);
