@@ -351,7 +351,7 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             tc::mbar_init(&full[s], 1);
-            tc::mbar_init(&empty[s], F8 ? 2 : 1);  // F8: both MMA warps release a stage
+            tc::mbar_init(&empty[s], 1);  // the MMA warp that used the stage releases it
         }
         for (int b = 0; b < 2; ++b) {
             tc::mbar_init(&tfull[b], F8 ? 2 : 1);  // F8: both MMA warps commit
@@ -605,15 +605,15 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
     } else if (F8 && (warp == 1 || warp == kMmaWarp2)) {
         // ------------------------------------------------------------ FP8 MMA issuers
         // Lane 0 alone runs the role, unit reads included (no warp-wide step per unit: these
-        // two warps bound the FP8 launch); the other lanes wait at the end.  Warp 1 issues
-        // the first 64-wide half of every K block into accumulator 0, warp kMmaWarp2 the
-        // second half into accumulator 1 (TMEM columns 2 NCH ..); the epilogue adds the two.
+        // two warps bound the FP8 launch); the other lanes wait at the end.  Warp 1 issues the
+        // eight MMAs of a unit's even K blocks into accumulator 0, warp kMmaWarp2 those of its
+        // odd K blocks into accumulator 1 (TMEM columns 2 NCH ..), each with one wait and one
+        // commit per K block; the epilogue adds the two.
         const int mh = warp == kMmaWarp2 ? 1 : 0;
         if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0;
             bool ok = true;
             int qi = 0;
+            int seq0 = 0;  // K blocks of the earlier units (the converters' stage sequence)
             for (int it = 0;; ++it) {
                 int u;
                 Unit w;
@@ -636,7 +636,10 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
                 bool good = tc::mbar_wait(&tempty[buf], aph ^ 1u, abortv, tmo);
                 if (!good) record_timeout(p.err, 2, u, -1, buf, aph, n_units, w.n);
                 tc::fence_after_sync();
-                for (int kb = 0; kb < w.kb && good; ++kb) {
+                for (int kb = mh; kb < w.kb && good; kb += 2) {
+                    const int seq = seq0 + kb;
+                    const int stage = seq % STAGES;
+                    const uint32_t phase = (seq / STAGES) & 1u;
                     // the converted A operand (its converters saw the token rows land)
                     good = tc::mbar_wait(&conv[stage], phase, abortv, tmo);
                     if (!good) {
@@ -645,22 +648,19 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
                     }
                     tc::fence_after_sync();
                     const uint32_t at = tmem_base + static_cast<uint32_t>(f8_a_column(NCH) + 64 * stage);
-                    const uint32_t sb = tc::smem_addr(bring + stage * BL + mh * NCH * 128);
-                    uint64_t bd[4];  // this warp's 64-wide half of the K block, four K = 16 steps
+                    const uint32_t sb = tc::smem_addr(bring + stage * BL);
+                    uint64_t bd[8];  // K = 16 steps 0..7: the two 64-wide B boxes, 32 bytes per step
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) bd[k] = tc::sdesc_k_sw128(sb + 32 * k);
-                    tc::mma4_f16_tmem_a(d_tmem, at + 32 * mh, bd, idesc, kb != 0);
+                    for (int k = 0; k < 8; ++k) bd[k] = tc::sdesc_k_sw128(sb + (k >> 2) * NCH * 128 + 32 * (k & 3));
+                    tc::mma8_f16_tmem_a(d_tmem, at, bd, idesc, kb != mh);
                     tc::mma_commit(&empty[stage]);
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
                 }
                 if (!good) {
                     ok = false;
                     break;
                 }
                 tc::mma_commit(&tfull[buf]);
+                seq0 += w.kb;
             }
             if (!ok) {
                 *abort_flag = 1;
@@ -778,10 +778,14 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
                 tc::tmem_ld32(tb + c0, v);
                 const int cnt = min(32, w.n - c0);
                 if (F8) {
-                    float v2[32];
-                    tc::tmem_ld32(tb + 2 * NCH + c0, v2);  // the second MMA warp's half of K
+                    if (w.kb > 1) {  // the second MMA warp's K blocks (none in a one-block unit)
+                        float v2[32];
+                        tc::tmem_ld32(tb + 2 * NCH + c0, v2);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] = (v[j] + v2[j]) * rs;
+                        for (int j = 0; j < 32; ++j) v[j] += v2[j];
+                    }
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] *= rs;
                 }
                 if (MODE == kGateUp || (EXP && !w.dn)) {
                     // rows alternate gate / up of one intermediate index: partner lane holds the other half
