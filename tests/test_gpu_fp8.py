@@ -1,7 +1,7 @@
 """FP8 E4M3 expert weights (one fp32 scale per weight row) on the GPU against the fp64
 oracle fed the dequantised weights (code value x row scale, exact in fp64).
 
-The expert launch converts each weight tile to f16 in shared memory (exact for
+The expert launch converts each weight tile to f16 in tensor memory (exact for
 E4M3), multiplies by f16 token rows (the bf16 layer input converted; exact but
 for values below f16's normal range) with fp32 accumulation and scales each
 accumulator row; the SwiGLU output is rounded to f16 (2^-11 relative, finer
