@@ -319,7 +319,7 @@ int run_coreset(const Ctx& c, int R, const float* top_p, const int32_t* idx, con
     if (Wgu != nullptr && c.d->dtype != MOESTEP_F32 && c.sms > R) {
         a.pf_base = static_cast<const char*>(Wgu);
         a.pf_stride = 2ll * c.d->I * c.d->H * (c.d->dtype == MOESTEP_FP8 ? 1 : 2);
-        a.pf_experts = kCoresetPrefetchExperts;
+        a.pf_experts = c.d->dtype == MOESTEP_FP8 ? kCoresetPrefetchExpertsF8 : kCoresetPrefetchExperts;
         a.pf_ctas = c.sms - R;
         a.pf_next = static_cast<const char*>(Wr_next);
         a.pf_next_bytes = 2ll * c.d->E * c.d->H;
