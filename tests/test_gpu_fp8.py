@@ -193,3 +193,32 @@ def test_fp8_codes_convert_exactly(kind):
     err = max_rel(out, ref)
     print(f"{kind} codes: max rel err {err:.3e}")
     assert err <= FP8_TOL, err
+
+
+@pytest.fixture(scope="module")
+def stack8():
+    cfg = W.STACK_FP8
+    layers = [clayer(W.device_layer(cfg, l), cfg) for l in range(cfg.n_layers)]
+    return cfg, layers, W.device_lm_head(cfg), W.host_lm_head(cfg)
+
+
+def test_fp8_stack_full_step_teacher_forced(stack8):
+    """All 40 FP8 layers in one call, the FP8 benchmark's configuration: every 8th layer and
+    the last against the oracle fed the GPU's own layer input (and the dequantised weights),
+    the LM head and commit from the GPU's final hidden state.  The update bound is the bf16
+    one (the FP8 path rounds its SwiGLU rows to f16, finer)."""
+    from tests.test_gpu_step import Step, check_commit, check_layer
+    cfg, layers, Wlm_d, Wlm = stack8
+    h0 = W.host_h0(cfg, 1)
+    masked0 = W.masked_subset(cfg, 1)
+    tokens = t(np.zeros(cfg.P, np.int32))
+    masked = t(masked0.astype(np.uint8))
+    st = Step(cfg, 1, cfg.n_layers, trace_xh=True)
+    st.run(layers, Wlm_d, 0.9, t(h0), tokens, masked)
+    np.testing.assert_array_equal(np_(st.h[0]), h0)
+    ambiguous = 0
+    for l in list(range(0, cfg.n_layers - 1, 8)) + [cfg.n_layers - 1]:
+        last = np_(st.h_out).astype(np.float64) if l == cfg.n_layers - 1 else None
+        ambiguous += check_layer(cfg, l, st, 0.9, last_h=last)
+    assert ambiguous <= 2
+    check_commit(cfg, st, Wlm, np_(tokens), np_(masked), masked0)

@@ -30,7 +30,7 @@ THR = 0.95
 
 def dims_of(cfg):
     return ms.ModelDims(H=cfg.H, E=cfg.E, k=cfg.k, I=cfg.I, Is=cfg.Is, V=cfg.V, P=cfg.P,
-                        dtype=ms.BF16 if cfg.dtype == "bf16" else ms.F32)
+                        dtype={"bf16": ms.BF16, "fp8": ms.FP8}.get(cfg.dtype, ms.F32))
 
 
 def clayer(lay):
@@ -54,7 +54,7 @@ class Step:
         self.n_sel = torch.zeros((L, R), dtype=torch.int32, device="cuda")
         self.sel = torch.zeros((L, R, cfg.E), dtype=torch.int32, device="cuda")
         self.idx = torch.zeros((L, T, cfg.k), dtype=torch.int32, device="cuda")
-        xdt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
+        xdt = torch.bfloat16 if cfg.act_dtype == "bf16" else torch.float32
         self.x = torch.zeros((L, T, cfg.H), dtype=xdt, device="cuda") if trace_xh else None
         self.h = torch.zeros((L, T, cfg.H), dtype=torch.float32, device="cuda") if trace_xh else None
 
