@@ -41,8 +41,9 @@
 //               warp turns the 32 tile rows of its TMEM lane quarter into f16
 //               (exact, values times 2^-8) and stores them with tcgen05.st
 //               as the MMA's A operand in tensor memory.
-//   warps 1, 14 MMA issuers, one 64-wide half of every K block each, into
-//               their own accumulators (the issue cost is per issuing thread).
+//   warps 1, 14 MMA issuers on one lane each, the even and the odd K blocks of
+//               every unit (eight MMAs per wait and commit) into their own
+//               accumulators (the issue cost is per issuing thread).
 //   warps 2-5   epilogue as above, adding the two accumulators and applying
 //               2^8 times each weight row's scale; SwiGLU rows stored as f16.
 // The epilogue warps never wait on each other, and every wait is bounded
@@ -58,7 +59,7 @@ namespace {
 constexpr int kThreads = 192;
 constexpr int kThreadsF8 = 512;  // + eight converter warps (two groups of four), a second MMA warp and a
                                  // second TMA warp
-constexpr int kMmaWarp2 = 14;    // FP8: issues the second 64-wide half of each K block into its own accumulator
+constexpr int kMmaWarp2 = 14;    // FP8: issues each unit's odd K blocks into its own accumulator
 constexpr int kTmaWarp2 = 15;    // FP8: loads the token rows (B ring); warp 0 loads the weight tiles
 constexpr uint64_t kTeardownNs = 1000000000ull;  // fixed limit for draining in-flight copies/MMAs
 constexpr int kABytes = 16384;            // 128 rows x 64 bf16
@@ -79,8 +80,8 @@ __host__ __device__ constexpr int smem_bytes(int nch) { return num_stages(nch) *
 // shared-memory traffic beyond reading the FP8 tile once.  The B ring has one slot per
 // A stage with the K block's token rows as two 64-wide B boxes (the MMA's B operand,
 // read in place); a stage's converters arrive only once its token rows have landed, so
-// each MMA warp waits once and commits once per K block (four MMAs): the tensor pipe,
-// not the HBM stream, is what small token counts make scarce here.
+// an MMA warp waits once and commits once per K block it takes (eight MMAs): the MMA
+// issue rate, not the HBM stream, is what small token counts make scarce here.
 constexpr int kF8Tile = 16384;    // 128 rows x 128 E4M3 bytes
 // f16 A operands in TMEM after the accumulators (two MMA warps x two buffers x NCH columns):
 // as many 64-column stages as the 512 columns leave, an even number (each converter group owns
