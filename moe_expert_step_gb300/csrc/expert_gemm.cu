@@ -39,13 +39,13 @@
 //               free again with it, at the MMAs' commit.
 //   warps 6-13  converters, two groups of four on alternate K blocks: each
 //               warp turns the 32 tile rows of its TMEM lane quarter into f16
-//               (exact, values times 2^-8) and stores them with tcgen05.st
+//               (exact, one conversion instruction per pair) and stores them with tcgen05.st
 //               as the MMA's A operand in tensor memory.
 //   warps 1, 14 MMA issuers on one lane each, the even and the odd K blocks of
 //               every unit (eight MMAs per wait and commit) into their own
 //               accumulators (the issue cost is per issuing thread).
 //   warps 2-5   epilogue as above, adding the two accumulators and applying
-//               2^8 times each weight row's scale; SwiGLU rows stored as f16.
+//               each weight row's scale; SwiGLU rows stored as f16.
 // The epilogue warps never wait on each other, and every wait is bounded
 // (timeout -> error word, orderly teardown), so no wait can hang the GPU.
 #include "common.cuh"
@@ -772,8 +772,7 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
             const uint32_t tb = tmem_base + (static_cast<uint32_t>(32 * sp) << 16) + static_cast<uint32_t>(buf * NCH);
             const int L = 32 * sp + lane;  // accumulator row held by this thread
             // F8: the scale of weight row L of this tile
-            // (times 2^8: the converted operand holds the E4M3 values times 2^-8)
-            const float rs = F8 ? 256.0f * __ldg(&p.sc[(w.dn ? 2 : 0) + (w.shared ? 1 : 0)][w.rowA0 + L]) : 1.0f;
+            const float rs = F8 ? __ldg(&p.sc[(w.dn ? 2 : 0) + (w.shared ? 1 : 0)][w.rowA0 + L]) : 1.0f;
             for (int c0 = 0; c0 < w.n; c0 += 32) {
                 float v[32];
                 tc::tmem_ld32(tb + c0, v);
@@ -892,8 +891,8 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
         // the 32 weight rows of its TMEM lane quarter; thread i reads row 32q + i of the
         // FP8 tile (128 bytes, 16-byte chunk j of row r at chunk j ^ (r & 7): the TMA's
         // 128-byte swizzle, so a warp's reads hit distinct banks) and releases the A slot,
-        // then, once the TMEM stage is free, converts the row into 64 f16x2 words (values
-        // times 2^-8, exactly) and stores them as TMEM lane 32q + i, columns
+        // then, once the TMEM stage is free, converts the row into 64 f16x2 words (exactly)
+        // and stores them as TMEM lane 32q + i, columns
         // f8_a_column(NCH) + 64 stage ..: A row i in lane i, elements 2c, 2c+1 in column c.
         const int q = warp & 3;
         const int grp = (warp - 6) >> 2;
@@ -940,8 +939,8 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
                     const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        h[8 * i + 2 * j] = tc::e4m3x2_to_f16x2_div256(wv[j], 0);
-                        h[8 * i + 2 * j + 1] = tc::e4m3x2_to_f16x2_div256(wv[j], 2);
+                        h[8 * i + 2 * j] = tc::e4m3x2_to_f16x2(wv[j], 0);
+                        h[8 * i + 2 * j + 1] = tc::e4m3x2_to_f16x2(wv[j], 2);
                     }
                 }
                 tc::tmem_st64(lane_base + static_cast<uint32_t>(f8_a_column(NCH) + 64 * stage), h);

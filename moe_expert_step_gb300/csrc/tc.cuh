@@ -272,15 +272,14 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// Two FP8 E4M3 bytes (bytes `lo` and `lo`+1 of w, low one first) -> two f16 holding
-// the values times 2^-8, exactly: a byte's seven magnitude bits shifted left by 7 are
-// the f16 pattern of value * 2^-8 (exponent 15 - 7 - 8 = bias difference minus 8; an
-// E4M3 subnormal m * 2^-9 lands on the f16 subnormal m * 2^-17), and adding the
-// shifted sign bit to itself moves it from bit 14 to bit 15.  Integer ops only.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2_div256(uint32_t w, int lo) {
-    const uint32_t x = __byte_perm(w, 0u, lo == 0 ? 0x4140u : 0x4342u);  // byte lo -> bits 0..7, lo+1 -> 16..23
-    const uint32_t y = x << 7;
-    return y + (y & 0x40004000u);
+// Two FP8 E4M3 codes (bytes `lo` and `lo`+1 of w, the low one into the low half) -> f16x2
+// with the hardware conversion, one instruction: every E4M3 value (subnormals included,
+// m * 2^-9) is an f16 value, so the conversion is exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w, int lo) {
+    const uint16_t pair = static_cast<uint16_t>(w >> (8 * lo));
+    uint32_t r;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(pair));
+    return r;
 }
 
 }  // namespace tc
