@@ -362,7 +362,7 @@ def run_gpu(args, dist: Dist):
     roofline = {"kernel": "tc_gemm_kernel<experts> (routed + shared expert gate/up, SwiGLU and down in one launch)",
                 "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                 "frac": round(achieved / hbm_peak, 4) if hbm_peak else None,
-                "traffic": load_traffic(statistics.mean(unions) + 1) if cfg.dtype != "fp8" else None,
+                "traffic": load_traffic(statistics.mean(unions) + 1, cfg.dtype),
                 "peak_source": peaks.get("source"),
                 "bytes_per_launch": int(ff_bytes_launch), "avg_launch_ms": round(ff_avg_ms, 5),
                 "launches_timed": ff_n}
@@ -587,14 +587,14 @@ def layer_head_desc(cfg, R: int) -> str:
     return "separate launches: combine + RMSNorm, router, coreset, gather"
 
 
-def load_traffic(experts_per_launch: float):
+def load_traffic(experts_per_launch: float, dtype: str = "bf16"):
     """DRAM bytes per expert-FFN launch: the ncu capture's bytes per expert (profiles/traffic.json,
-    one Clover layer) scaled to the experts of one launch here; None if the kernel sources
-    changed since that capture."""
+    one Clover layer, the launch of this weight type) scaled to the experts of one launch here;
+    None if the kernel sources changed since that capture."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
-    rec = json.load(open(p)).get("tc_gemm_experts_bf16", {})
+    rec = json.load(open(p)).get("tc_gemm_experts_fp8" if dtype == "fp8" else "tc_gemm_experts_bf16", {})
     if rec.get("kernel_sources_sha") != kernel_sources_sha() or "dram_bytes_per_expert" not in rec:
         return None
     return int(float(rec["dram_bytes_per_expert"]) * experts_per_launch)
