@@ -35,8 +35,9 @@
 //               (128-byte swizzle), one per K block; a slot is free again as
 //               soon as its converters have read it into registers.
 //   warp 15     TMA producer of the B ring: each K block's token rows as two
-//               64-wide f16 B boxes; B slot i goes with TMEM A stage i and is
-//               free again with it, at the MMAs' commit.
+//               64-wide f16 B boxes, in twice as many slots as there are TMEM
+//               A stages (the rows land well before their stage comes round);
+//               a slot is free again at its MMAs' commit.
 //   warps 6-13  converters, two groups of four on alternate K blocks: each
 //               warp turns the 32 tile rows of its TMEM lane quarter into f16
 //               (exact, one conversion instruction per pair) and stores them with tcgen05.st
@@ -77,11 +78,12 @@ __host__ __device__ constexpr int smem_bytes(int nch) { return num_stages(nch) *
 // released as soon as its converters hold it in registers, so the weight stream does
 // not wait out the MMAs.  The converted f16 A operands live in tensor memory
 // (f8_a_stages stages of 64 columns from column f8_a_column), so the conversion adds no
-// shared-memory traffic beyond reading the FP8 tile once.  The B ring has one slot per
-// A stage with the K block's token rows as two 64-wide B boxes (the MMA's B operand,
-// read in place); a stage's converters arrive only once its token rows have landed, so
-// an MMA warp waits once and commits once per K block it takes (eight MMAs): the MMA
-// issue rate, not the HBM stream, is what small token counts make scarce here.
+// shared-memory traffic beyond reading the FP8 tile once.  The B ring holds the K blocks'
+// token rows as two 64-wide B boxes (the MMA's B operand, read in place), two slots per A
+// stage, so that a stage's round trip (freed, converted, multiplied, committed) does not
+// include a load of its token rows; a stage's converters arrive only once its token rows
+// have landed, so an MMA warp waits once and commits once per K block it takes (eight
+// MMAs): the MMA issue rate, not the HBM stream, is what small token counts make scarce.
 constexpr int kF8Tile = 16384;    // 128 rows x 128 E4M3 bytes
 // f16 A operands in TMEM after the accumulators (two MMA warps x two buffers x NCH columns):
 // as many 64-column stages as the 512 columns leave, an even number (each converter group owns
@@ -89,13 +91,13 @@ constexpr int kF8Tile = 16384;    // 128 rows x 128 E4M3 bytes
 __host__ __device__ constexpr int f8_a_column(int nch) { return 4 * nch; }
 __host__ __device__ constexpr int f8_a_stages(int nch) { return ((512 - 4 * nch) / 64) & ~1; }
 __host__ __device__ constexpr int f8_b_bytes(int nch) { return 2 * nch * 128; }  // one B slot
-__host__ __device__ constexpr int f8_b_slots(int nch) { return f8_a_stages(nch); }
+__host__ __device__ constexpr int f8_b_slots(int nch) { return 2 * f8_a_stages(nch); }
 // The rest of shared memory, an even number of slots (so that each A slot is always read by the
 // same converter group).
 __host__ __device__ constexpr int f8_a_slots(int nch) {
     return ((kSmemBudget - 1024 - f8_b_slots(nch) * f8_b_bytes(nch)) / kF8Tile) & ~1;
 }
-static_assert(f8_a_slots(32) == 10 && f8_a_slots(64) == 10, "FP8 weight-tile ring");
+static_assert(f8_a_slots(32) == 8 && f8_a_slots(64) == 6, "FP8 weight-tile ring");
 static_assert(f8_a_stages(32) == 6 && f8_a_stages(64) == 4, "FP8 A stages in tensor memory");
 __host__ __device__ constexpr int smem_bytes_f8(int nch) {
     return f8_a_slots(nch) * kF8Tile + f8_b_slots(nch) * f8_b_bytes(nch) + 1024 + 1024;
@@ -331,14 +333,15 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
     uint64_t* conv = fin + 1;            // F8: the stage's weight tile is converted (count 1)
     uint64_t* fullA = conv + STAGES;     // F8: the weight tile landed (TMA bytes)
     uint64_t* emptyA = fullA + SA;       // F8: its four converter warps read it (count 4)
-    uint64_t* fullB = emptyA + SA;       // F8: the token rows landed (TMA bytes); freed with empty[]
-    uint64_t* rend = fullB + SBR;
+    uint64_t* fullB = emptyA + SA;       // F8: the token rows landed (TMA bytes)
+    uint64_t* emptyB = fullB + SBR;      // F8: the MMAs that read them completed (commit)
+    uint64_t* rend = emptyB + SBR;
     constexpr bool DYN = EXP;  // units handed out at run time (UnitRing)
     int* ring_idx = reinterpret_cast<int*>(rend + 2 * kUnitQ);
     // F8: the decoded entries after the indices, 16-byte aligned (within the barrier area)
     int4* ring_ent = F8 ? reinterpret_cast<int4*>((reinterpret_cast<uintptr_t>(ring_idx + kUnitQ) + 15) & ~uintptr_t(15))
                         : nullptr;
-    static_assert(!F8 || (3 * STAGES + 5 + 2 * SA + SBR + 2 * kUnitQ) * 8 + 4 * kUnitQ + 16 + 2 * kUnitQ * 16 + 16 <= 1024,
+    static_assert(!F8 || (3 * STAGES + 5 + 2 * SA + 2 * SBR + 2 * kUnitQ) * 8 + 4 * kUnitQ + 16 + 2 * kUnitQ * 16 + 16 <= 1024,
                   "FP8 barrier area");
     const UnitRing ring{rend, rend + kUnitQ, ring_idx, ring_ent};
     uint32_t* tmem_holder =
@@ -370,7 +373,10 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
                 tc::mbar_init(&fullA[s], 1);
                 tc::mbar_init(&emptyA[s], 4);
             }
-            for (int s = 0; s < SBR; ++s) tc::mbar_init(&fullB[s], 1);
+            for (int s = 0; s < SBR; ++s) {
+                tc::mbar_init(&fullB[s], 1);
+                tc::mbar_init(&emptyB[s], 1);  // the MMA warp that read the slot releases it
+            }
         }
         *abort_flag = 0;
         *zero_flag = 0;
@@ -460,8 +466,8 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
         __syncwarp();
     } else if (F8 && warp == kTmaWarp2) {
         // ------------------------------------------------------------ FP8 token-row producer
-        // Fills the B ring in the same order, slot i once TMEM A stage i is free; a down
-        // unit's SwiGLU rows once its chunk's gate/up epilogues (any CTA) counted them stored.
+        // Fills the B ring in the same order, a slot once the MMAs that read it completed; a
+        // down unit's SwiGLU rows once its chunk's gate/up epilogues (any CTA) counted them stored.
         uint32_t issued = 0, issued_parity = 0;
         constexpr int SBd = SBR > 0 ? SBR : 1;
         int seq = 0;
@@ -491,7 +497,7 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
                 const int slot = seq % SBd;
                 const uint32_t ph = (seq / SBd) & 1u;
                 if (lane == 0) {
-                    good = tc::mbar_wait(&empty[slot], ph ^ 1u, abortv, tmo);
+                    good = tc::mbar_wait(&emptyB[slot], ph ^ 1u, abortv, tmo);
                     if (good) {
                         uint8_t* dst = bring + slot * BL;
                         tc::mbar_arrive_expect_tx(&fullB[slot], 2 * nb * kBoxBBytes);
@@ -649,12 +655,14 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
                     }
                     tc::fence_after_sync();
                     const uint32_t at = tmem_base + static_cast<uint32_t>(f8_a_column(NCH) + 64 * stage);
-                    const uint32_t sb = tc::smem_addr(bring + stage * BL);
+                    const int bslot = seq % (SBR > 0 ? SBR : 1);
+                    const uint32_t sb = tc::smem_addr(bring + bslot * BL);
                     uint64_t bd[8];  // K = 16 steps 0..7: the two 64-wide B boxes, 32 bytes per step
 #pragma unroll
                     for (int k = 0; k < 8; ++k) bd[k] = tc::sdesc_k_sw128(sb + (k >> 2) * NCH * 128 + 32 * (k & 3));
                     tc::mma8_f16_tmem_a(d_tmem, at, bd, idesc, kb != mh);
                     tc::mma_commit(&empty[stage]);
+                    tc::mma_commit(&emptyB[bslot]);
                 }
                 if (!good) {
                     ok = false;
@@ -756,6 +764,9 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
                 break;
             }
             if (!F8) w = decode_unit<MODE, NCH>(u, p, nrc, nsc);
+            const int L = 32 * sp + lane;  // accumulator row held by this thread
+            // F8: the scale of weight row L of this tile, loaded while the unit's MMAs run
+            const float rs = F8 ? __ldg(&p.sc[(w.dn ? 2 : 0) + (w.shared ? 1 : 0)][w.rowA0 + L]) : 1.0f;
             const int buf = it & 1;
             const uint32_t aph = (it >> 1) & 1;
             int good = tc::mbar_wait(&tfull[buf], aph, abortv, tmo);
@@ -770,9 +781,6 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
             }
             tc::fence_after_sync();
             const uint32_t tb = tmem_base + (static_cast<uint32_t>(32 * sp) << 16) + static_cast<uint32_t>(buf * NCH);
-            const int L = 32 * sp + lane;  // accumulator row held by this thread
-            // F8: the scale of weight row L of this tile
-            const float rs = F8 ? __ldg(&p.sc[(w.dn ? 2 : 0) + (w.shared ? 1 : 0)][w.rowA0 + L]) : 1.0f;
             for (int c0 = 0; c0 < w.n; c0 += 32) {
                 float v[32];
                 tc::tmem_ld32(tb + c0, v);
@@ -899,6 +907,7 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
         const int row = 32 * q + lane;
         const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(32 * q) << 16);
         constexpr int SAd = SA > 0 ? SA : 1;
+        constexpr int SBRd = SBR > 0 ? SBR : 1;
         bool ok = true;
         int seq = 0;
         int qi = 0;
@@ -945,10 +954,12 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
                 }
                 tc::tmem_st64(lane_base + static_cast<uint32_t>(f8_a_column(NCH) + 64 * stage), h);
                 tc::fence_before_sync();
-                // the stage's token rows have landed before the MMA warps may read them
-                if (!__all_sync(0xffffffffu, lane != 0 || tc::mbar_wait(&fullB[stage], phase, abortv, tmo))) {
+                // the K block's token rows have landed before the MMA warps may read them
+                const int bslot = seq % SBRd;
+                const uint32_t phb = (seq / SBRd) & 1u;
+                if (!__all_sync(0xffffffffu, lane != 0 || tc::mbar_wait(&fullB[bslot], phb, abortv, tmo))) {
                     ok = false;
-                    if (lane == 0) record_timeout(p.err, 10, u, kb, stage, phase, n_units, w.n);
+                    if (lane == 0) record_timeout(p.err, 10, u, kb, bslot, phb, n_units, w.n);
                     break;
                 }
                 if (lane == 0) tc::mbar_arrive(&conv[stage]);
