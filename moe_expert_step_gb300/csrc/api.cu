@@ -382,7 +382,7 @@ int run_experts(const Ctx& c, int R, const void* x, const moestep_layer* layer, 
     if (get_encode() != MOESTEP_OK) return MOESTEP_ECUDA;
     const bool sh = d->Is > 0;
     const bool f8 = d->dtype == MOESTEP_FP8;
-    TensorMaps m;
+    TensorMaps m{};
     int rc;
     if (f8) {
         if ((rc = make_map_fp8(&m.a[0], layer->Wgu, d->H, 2ull * d->E * d->I))) return rc;
@@ -397,6 +397,10 @@ int run_experts(const Ctx& c, int R, const void* x, const moestep_layer* layer, 
     }
     if ((rc = make_map(&m.b[0], at<void>(c.ws, L.xp), d->H, L.max_slots, 16))) return rc;
     if ((rc = make_map(&m.b[1], at<void>(c.ws, L.act), L.act_ld, L.max_slots, 16))) return rc;
+    for (int i = 1; f8 && i <= 2; ++i) {  // 32- and 64-row boxes: a K block's token rows in one copy
+        if ((rc = make_map(&m.b[2 * i], at<void>(c.ws, L.xp), d->H, L.max_slots, 16u << i))) return rc;
+        if ((rc = make_map(&m.b[2 * i + 1], at<void>(c.ws, L.act), L.act_ld, L.max_slots, 16u << i))) return rc;
+    }
     GemmParams g{};
     g.plan = plan;
     g.chunks = at<int4>(c.ws, L.chunks);
@@ -439,7 +443,7 @@ int run_lm_commit(const Ctx& c, int R, const void* hidden, const void* Wlm, floa
     int n_tiles;
     if (d->dtype != MOESTEP_F32) {
         if (get_encode() != MOESTEP_OK) return MOESTEP_ECUDA;
-        TensorMaps m;
+        TensorMaps m{};
         int rc;
         if ((rc = make_map(&m.a[0], Wlm, d->H, d->V, 64))) return rc;
         if ((rc = make_map(&m.b[0], hidden, d->H, T, 16))) return rc;

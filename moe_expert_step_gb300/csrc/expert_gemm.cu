@@ -34,10 +34,11 @@
 //   warp 0      TMA producer of the A ring: 128 x 128-byte FP8 weight tiles
 //               (128-byte swizzle), one per K block; a slot is free again as
 //               soon as its converters have read it into registers.
-//   warp 15     TMA producer of the B ring: each K block's token rows as two
-//               64-wide f16 B boxes, in twice as many slots as there are TMEM
-//               A stages (the rows land well before their stage comes round);
-//               a slot is free again at its MMAs' commit.
+//   warp 15     TMA producer of the B ring: each K block's token rows (f16) in
+//               one 4 KiB granule per 16 tokens, contiguous, so one MMA covers
+//               all of a unit's tokens; a ring of 12-16 granules (the rows land
+//               well before their stage comes round); a granule is free again
+//               at its MMAs' commit.
 //   warps 6-13  converters, two groups of four on alternate K blocks: each
 //               warp turns the 32 tile rows of its TMEM lane quarter into f16
 //               (exact, one conversion instruction per pair) and stores them with tcgen05.st
@@ -53,6 +54,8 @@
 #include "kernels.h"
 #include "launch.cuh"
 #include "tc.cuh"
+
+#include <type_traits>
 
 namespace moestep {
 namespace {
@@ -79,28 +82,36 @@ __host__ __device__ constexpr int smem_bytes(int nch) { return num_stages(nch) *
 // not wait out the MMAs.  The converted f16 A operands live in tensor memory
 // (f8_a_stages stages of 64 columns from column f8_a_column), so the conversion adds no
 // shared-memory traffic beyond reading the FP8 tile once.  The B ring holds the K blocks'
-// token rows as two 64-wide B boxes (the MMA's B operand, read in place), two slots per A
-// stage, so that a stage's round trip (freed, converted, multiplied, committed) does not
-// include a load of its token rows; a stage's converters arrive only once its token rows
-// have landed, so an MMA warp waits once and commits once per K block it takes (eight
-// MMAs): the MMA issue rate, not the HBM stream, is what small token counts make scarce.
+// token rows (the MMA's B operand, read in place) far enough ahead that a stage's round
+// trip (freed, converted, multiplied, committed) does not include a load of its token
+// rows; a stage's converters arrive only once its token rows have landed, so an MMA warp
+// waits once per K block it takes (eight MMAs).  The ring is sized in 16-token granules,
+// so a unit with few tokens (the usual case: a handful per expert) takes one granule per
+// K block and the shared memory left over holds more weight tiles in flight.
 constexpr int kF8Tile = 16384;    // 128 rows x 128 E4M3 bytes
 // f16 A operands in TMEM after the accumulators (two MMA warps x two buffers x NCH columns):
 // as many 64-column stages as the 512 columns leave, an even number (each converter group owns
 // every other stage)
 __host__ __device__ constexpr int f8_a_column(int nch) { return 4 * nch; }
 __host__ __device__ constexpr int f8_a_stages(int nch) { return ((512 - 4 * nch) / 64) & ~1; }
-__host__ __device__ constexpr int f8_b_bytes(int nch) { return 2 * nch * 128; }  // one B slot
-__host__ __device__ constexpr int f8_b_slots(int nch) { return 2 * f8_a_stages(nch); }
+// A granule: 16 token rows of one K block of 128, in two halves of 2 KiB (K 0..63 and
+// K 64..127, 128-byte swizzle) kept in two half-rings, so that n consecutive granules form
+// one B operand of 16 n rows per half.
+constexpr int kGranule = 4096;
+constexpr int kGranuleHalf = kGranule / 2;
+__host__ __device__ constexpr int f8_b_granules(int nch) { return nch <= 32 ? 12 : 24; }
+static_assert(f8_b_granules(32) % 4 == 0 && f8_b_granules(64) % 4 == 0, "whole entries of up to 4 granules");
 // The rest of shared memory, an even number of slots (so that each A slot is always read by the
-// same converter group).
+// same converter group).  At 64-token chunks the token-row ring takes 24 granules (eight K blocks
+// of 48-64 tokens ahead) and leaves 8 weight slots.
 __host__ __device__ constexpr int f8_a_slots(int nch) {
-    return ((kSmemBudget - 1024 - f8_b_slots(nch) * f8_b_bytes(nch)) / kF8Tile) & ~1;
+    return ((kSmemBudget - 1024 - f8_b_granules(nch) * kGranule) / kF8Tile) & ~1;
 }
-static_assert(f8_a_slots(32) == 8 && f8_a_slots(64) == 6, "FP8 weight-tile ring");
+constexpr int kF8BarrierBytes = 2048;  // the FP8 launch's barriers and unit ring
+static_assert(f8_a_slots(32) == 10 && f8_a_slots(64) == 8, "FP8 weight-tile ring");
 static_assert(f8_a_stages(32) == 6 && f8_a_stages(64) == 4, "FP8 A stages in tensor memory");
 __host__ __device__ constexpr int smem_bytes_f8(int nch) {
-    return f8_a_slots(nch) * kF8Tile + f8_b_slots(nch) * f8_b_bytes(nch) + 1024 + 1024;
+    return f8_a_slots(nch) * kF8Tile + f8_b_granules(nch) * kGranule + kF8BarrierBytes + 1024;
 }
 static_assert(smem_bytes_f8(32) <= 232448 && smem_bytes_f8(64) <= 232448, "FP8 shared memory");
 
@@ -108,6 +119,25 @@ struct Unit {
     int kb, rowA0, rowA1, slot0, n, mt, c;
     bool shared, dn;
 };
+
+// Token-row entries of the FP8 launch.  Every role that touches the granule ring walks the
+// same K blocks in the same order and places them alike: each K block of a unit with n tokens
+// takes an entry of granules_for(n) granules (a power of two; one copy per half-ring of that
+// many 16-row granules), a unit's first entry starts at the ring position rounded up to a
+// multiple of that (the ring's size is a multiple of 4, so no entry runs past its end) and the
+// unit's later entries follow one another around the ring.  An entry's copies complete on its
+// first granule's full barrier; the MMAs that read it release every granule of it.  Granules
+// that an entry skips sit out that lap; the roles that wait on the ring's barriers keep the use
+// counts mod 2 (per granule for the empty barriers, per first granule for the full ones).
+__device__ __forceinline__ int granules_for(int n) {
+    const int q = (n + 15) >> 4;
+    return q <= 1 ? 1 : q <= 2 ? 2 : 4;
+}
+template <int G>
+__device__ __forceinline__ int granule_start(int pos, int nbp) {
+    const int p = (pos + nbp - 1) & ~(nbp - 1);
+    return p >= G ? 0 : p;
+}
 
 template <int MODE, int NCH>
 __device__ __forceinline__ Unit decode_unit(int u, const GemmParams& p, int nrc, int nsc) {
@@ -140,14 +170,21 @@ __device__ __forceinline__ Unit decode_unit(int u, const GemmParams& p, int nrc,
             rpe = p.dn_rows_per_expert;
         }
     }
+    // Within each half the routed units come first, except in the FP8 launch: there the shared
+    // expert's units (all of the block's tokens, so the widest token-row entries) come first, so
+    // that they run alongside routed units rather than at the end of the launch.
+    constexpr bool kSharedFirst = MODE == kExpertsF8;
     const int routed_units = nrc * rt;
+    const int shared_units = nsc * st;
     int c, mt;
-    if (u < routed_units) {
-        c = u / rt;
-        mt = u - c * rt;
+    const bool shared = kSharedFirst ? u < shared_units : u >= routed_units;
+    if (!shared) {
+        const int v = kSharedFirst ? u - shared_units : u;
+        c = v / rt;
+        mt = v - c * rt;
         w.shared = false;
     } else {
-        const int v = u - routed_units;
+        const int v = kSharedFirst ? u : u - routed_units;
         const int cs = v / st;
         mt = v - cs * st;
         c = nrc + cs;
@@ -316,15 +353,14 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
     constexpr int STAGES = F8 ? f8_a_stages(NCH) : num_stages(NCH);  // F8: A stages in TMEM
     constexpr int SB = F8 ? 0 : stage_bytes(NCH);
     constexpr int SA = F8 ? f8_a_slots(NCH) : 0;          // F8: weight-tile slots
-    constexpr int SBR = F8 ? f8_b_slots(NCH) : 0;         // F8: token-row slots
-    constexpr int BL = f8_b_bytes(NCH);
+    constexpr int GB = F8 ? f8_b_granules(NCH) : 0;       // F8: token-row granules
     constexpr uint32_t TMEM_COLS = F8 ? 512u : ((2 * NCH < 32) ? 32u : static_cast<uint32_t>(2 * NCH));
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* aring = smem + STAGES * SB;  // F8: SA weight tiles of kF8Tile bytes
-    uint8_t* bring = aring + SA * kF8Tile;  // F8: SBR token-row slots of BL bytes
-    uint64_t* bars = reinterpret_cast<uint64_t*>(bring + SBR * BL);
+    uint8_t* bring = aring + SA * kF8Tile;  // F8: GB token-row granules (two half-rings)
+    uint64_t* bars = reinterpret_cast<uint64_t*>(bring + GB * kGranule);
     uint64_t* full = bars;
     uint64_t* empty = bars + STAGES;
     uint64_t* tfull = bars + 2 * STAGES;
@@ -333,15 +369,16 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
     uint64_t* conv = fin + 1;            // F8: the stage's weight tile is converted (count 1)
     uint64_t* fullA = conv + STAGES;     // F8: the weight tile landed (TMA bytes)
     uint64_t* emptyA = fullA + SA;       // F8: its four converter warps read it (count 4)
-    uint64_t* fullB = emptyA + SA;       // F8: the token rows landed (TMA bytes)
-    uint64_t* emptyB = fullB + SBR;      // F8: the MMAs that read them completed (commit)
-    uint64_t* rend = emptyB + SBR;
+    uint64_t* fullB = emptyA + SA;       // F8: a granule's token rows landed (TMA bytes)
+    uint64_t* emptyB = fullB + GB;       // F8: the MMAs that read them completed (commit)
+    uint64_t* rend = emptyB + GB;
     constexpr bool DYN = EXP;  // units handed out at run time (UnitRing)
     int* ring_idx = reinterpret_cast<int*>(rend + 2 * kUnitQ);
     // F8: the decoded entries after the indices, 16-byte aligned (within the barrier area)
     int4* ring_ent = F8 ? reinterpret_cast<int4*>((reinterpret_cast<uintptr_t>(ring_idx + kUnitQ) + 15) & ~uintptr_t(15))
                         : nullptr;
-    static_assert(!F8 || (3 * STAGES + 5 + 2 * SA + 2 * SBR + 2 * kUnitQ) * 8 + 4 * kUnitQ + 16 + 2 * kUnitQ * 16 + 16 <= 1024,
+    static_assert(!F8 || (3 * STAGES + 5 + 2 * SA + 2 * GB + 2 * kUnitQ) * 8 + 4 * kUnitQ + 16 + 2 * kUnitQ * 16 + 16 <=
+                             kF8BarrierBytes,
                   "FP8 barrier area");
     const UnitRing ring{rend, rend + kUnitQ, ring_idx, ring_ent};
     uint32_t* tmem_holder =
@@ -373,9 +410,9 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
                 tc::mbar_init(&fullA[s], 1);
                 tc::mbar_init(&emptyA[s], 4);
             }
-            for (int s = 0; s < SBR; ++s) {
+            for (int s = 0; s < GB; ++s) {
                 tc::mbar_init(&fullB[s], 1);
-                tc::mbar_init(&emptyB[s], 1);  // the MMA warp that read the slot releases it
+                tc::mbar_init(&emptyB[s], 1);  // the MMA warp that read the granule releases it
             }
         }
         *abort_flag = 0;
@@ -383,6 +420,8 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
         tc::fence_mbar_init();
         tc::prefetch_tmap(&maps.a[0]);
         tc::prefetch_tmap(&maps.b[0]);
+        if (F8)
+            for (int i = 2; i < 6; ++i) tc::prefetch_tmap(&maps.b[i]);
         if (MODE != kLmHead) {
             tc::prefetch_tmap(&maps.a[1]);
             if (EXP) {
@@ -466,11 +505,12 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
         __syncwarp();
     } else if (F8 && warp == kTmaWarp2) {
         // ------------------------------------------------------------ FP8 token-row producer
-        // Fills the B ring in the same order, a slot once the MMAs that read it completed; a
+        // Fills the B ring in the same order, a granule once the MMAs that read it completed; a
         // down unit's SwiGLU rows once its chunk's gate/up epilogues (any CTA) counted them stored.
+        // One copy of 16, 32 or 64 rows per half-ring and K block.
         uint32_t issued = 0, issued_parity = 0;
-        constexpr int SBd = SBR > 0 ? SBR : 1;
-        int seq = 0;
+        uint32_t epar = 0, fpar = 0;  // use counts mod 2: per granule, per first granule of an entry
+        int gpos = 0;
         bool ok = true;
         int qi = 0;
         for (int u = blockIdx.x; ok; u += gridDim.x) {
@@ -480,8 +520,9 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
                 break;
             }
             if (u < 0) break;
-            const int nb = (w.n + 15) >> 4;
-            const CUtensorMap* mB = &maps.b[w.dn ? 1 : 0];
+            const int nbp = granules_for(w.n);
+            int g0 = granule_start<GB>(gpos, nbp);
+            const CUtensorMap* mB = &maps.b[(w.dn ? 1 : 0) + (nbp & 6)];  // boxes of 16 nbp rows
             int good = 1;
             if (w.dn) {
                 if (lane == 0)
@@ -493,37 +534,57 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
                     break;
                 }
             }
-            for (int kb = 0; kb < w.kb; ++kb, ++seq) {
-                const int slot = seq % SBd;
-                const uint32_t ph = (seq / SBd) & 1u;
-                if (lane == 0) {
-                    good = tc::mbar_wait(&emptyB[slot], ph ^ 1u, abortv, tmo);
-                    if (good) {
-                        uint8_t* dst = bring + slot * BL;
-                        tc::mbar_arrive_expect_tx(&fullB[slot], 2 * nb * kBoxBBytes);
-                        for (int b = 0; b < nb; ++b) {
-                            tc::tma_load_2d(dst + b * kBoxBBytes, mB, &fullB[slot], kb * 128, w.slot0 + 16 * b);
-                            tc::tma_load_2d(dst + NCH * 128 + b * kBoxBBytes, mB, &fullB[slot], kb * 128 + 64,
-                                            w.slot0 + 16 * b);
+            // the unit's K blocks with the entry size a constant (one granule nearly always)
+            auto kblocks = [&](auto nbp_c) -> bool {
+                constexpr int NBP = decltype(nbp_c)::value;
+                for (int kb = 0; kb < w.kb; ++kb) {
+                    int gbad = -1;
+                    if (lane == 0) {
+#pragma unroll
+                        for (int j = 0; j < NBP; ++j) {
+                            const int g = g0 + j;
+                            if (good && !tc::mbar_wait(&emptyB[g], ((epar >> g) & 1u) ^ 1u, abortv, tmo)) {
+                                good = 0;
+                                gbad = g;
+                            }
                         }
-                        issued |= 1u << slot;
-                        issued_parity = (issued_parity & ~(1u << slot)) | (ph << slot);
+                        if (good) {
+                            const uint32_t ph = (fpar >> g0) & 1u;
+                            tc::mbar_arrive_expect_tx(&fullB[g0], NBP * kGranule);
+                            tc::tma_load_2d(bring + g0 * kGranuleHalf, mB, &fullB[g0], kb * 128, w.slot0);
+                            tc::tma_load_2d(bring + (GB + g0) * kGranuleHalf, mB, &fullB[g0], kb * 128 + 64,
+                                            w.slot0);
+                            issued |= 1u << g0;
+                            issued_parity = (issued_parity & ~(1u << g0)) | (ph << g0);
+                        }
+                    }
+                    epar ^= ((1u << NBP) - 1u) << g0;
+                    fpar ^= 1u << g0;
+                    g0 += NBP;
+                    if (g0 == GB) g0 = 0;
+                    good = __shfl_sync(0xffffffffu, good, 0);
+                    if (!good) {
+                        if (lane == 0) record_timeout(p.err, 1, u, kb, gbad, 0, n_units, w.n);
+                        return false;
                     }
                 }
-                good = __shfl_sync(0xffffffffu, good, 0);
-                if (!good) {
-                    ok = false;
-                    if (lane == 0) record_timeout(p.err, 1, u, kb, slot, ph, n_units, w.n);
-                    break;
-                }
+                return true;
+            };
+            const bool kok = nbp == 1   ? kblocks(std::integral_constant<int, 1>{})
+                             : nbp == 2 ? kblocks(std::integral_constant<int, 2>{})
+                                        : kblocks(std::integral_constant<int, 4>{});
+            if (!kok) {
+                ok = false;
+                break;
             }
+            gpos = g0;
         }
         if (lane == 0) {
             if (!ok) {
                 *abort_flag = 1;
                 record_error(p.err, kErrTimeoutProducer);
             }
-            for (int s = 0; s < SBR; ++s)
+            for (int s = 0; s < GB; ++s)
                 if (issued & (1u << s)) tc::mbar_wait(&fullB[s], (issued_parity >> s) & 1u, zero_flag, kTeardownNs);
         }
         __syncwarp();
@@ -621,6 +682,7 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
             bool ok = true;
             int qi = 0;
             int seq0 = 0;  // K blocks of the earlier units (the converters' stage sequence)
+            int gpos = 0;  // the token-row ring position after the earlier units
             for (int it = 0;; ++it) {
                 int u;
                 Unit w;
@@ -643,33 +705,51 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
                 bool good = tc::mbar_wait(&tempty[buf], aph ^ 1u, abortv, tmo);
                 if (!good) record_timeout(p.err, 2, u, -1, buf, aph, n_units, w.n);
                 tc::fence_after_sync();
-                for (int kb = mh; kb < w.kb && good; kb += 2) {
-                    const int seq = seq0 + kb;
-                    const int stage = seq % STAGES;
-                    const uint32_t phase = (seq / STAGES) & 1u;
-                    // the converted A operand (its converters saw the token rows land)
-                    good = tc::mbar_wait(&conv[stage], phase, abortv, tmo);
-                    if (!good) {
-                        record_timeout(p.err, 3, u, kb, stage, phase, n_units, w.n);
-                        break;
-                    }
-                    tc::fence_after_sync();
-                    const uint32_t at = tmem_base + static_cast<uint32_t>(f8_a_column(NCH) + 64 * stage);
-                    const int bslot = seq % (SBR > 0 ? SBR : 1);
-                    const uint32_t sb = tc::smem_addr(bring + bslot * BL);
-                    uint64_t bd[8];  // K = 16 steps 0..7: the two 64-wide B boxes, 32 bytes per step
+                const int nbp = granules_for(w.n);  // token-row granules per K block
+                const int p0 = granule_start<GB>(gpos, nbp);
+                // this warp's K blocks with the entry size a constant (one granule nearly always)
+                auto kblocks = [&](auto nbp_c) {
+                    constexpr int NBP = decltype(nbp_c)::value;
+                    int g0 = p0 + mh * NBP;  // this warp's first K block's entry
+                    if (g0 >= GB) g0 -= GB;
+                    for (int kb = mh; kb < w.kb && good; kb += 2) {
+                        const int seq = seq0 + kb;
+                        const int stage = seq % STAGES;
+                        const uint32_t phase = (seq / STAGES) & 1u;
+                        // the converted A operand (its converters saw the token rows land)
+                        good = tc::mbar_wait(&conv[stage], phase, abortv, tmo);
+                        if (!good) {
+                            record_timeout(p.err, 3, u, kb, stage, phase, n_units, w.n);
+                            break;
+                        }
+                        tc::fence_after_sync();
+                        const uint32_t at = tmem_base + static_cast<uint32_t>(f8_a_column(NCH) + 64 * stage);
+                        const uint32_t sb = tc::smem_addr(bring + g0 * kGranuleHalf);
+                        uint64_t bd[8];  // K = 16 steps 0..7: half-ring k >> 2, 32 bytes per step
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) bd[k] = tc::sdesc_k_sw128(sb + (k >> 2) * NCH * 128 + 32 * (k & 3));
-                    tc::mma8_f16_tmem_a(d_tmem, at, bd, idesc, kb != mh);
-                    tc::mma_commit(&empty[stage]);
-                    tc::mma_commit(&emptyB[bslot]);
-                }
+                        for (int k = 0; k < 8; ++k)
+                            bd[k] = tc::sdesc_k_sw128(sb + (k >> 2) * GB * kGranuleHalf + 32 * (k & 3));
+                        tc::mma8_f16_tmem_a(d_tmem, at, bd, idesc, kb != mh);
+                        tc::mma_commit(&empty[stage]);
+#pragma unroll
+                        for (int j = 0; j < NBP; ++j) tc::mma_commit(&emptyB[g0 + j]);
+                        g0 += 2 * NBP;
+                        if (g0 >= GB) g0 -= GB;
+                    }
+                };
+                if (nbp == 1)
+                    kblocks(std::integral_constant<int, 1>{});
+                else if (nbp == 2)
+                    kblocks(std::integral_constant<int, 2>{});
+                else
+                    kblocks(std::integral_constant<int, 4>{});
                 if (!good) {
                     ok = false;
                     break;
                 }
                 tc::mma_commit(&tfull[buf]);
                 seq0 += w.kb;
+                gpos = (p0 + w.kb * nbp) % (GB > 0 ? GB : 4);
             }
             if (!ok) {
                 *abort_flag = 1;
@@ -907,10 +987,11 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
         const int row = 32 * q + lane;
         const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(32 * q) << 16);
         constexpr int SAd = SA > 0 ? SA : 1;
-        constexpr int SBRd = SBR > 0 ? SBR : 1;
         bool ok = true;
         int seq = 0;
         int qi = 0;
+        uint32_t fpar = 0;  // use count mod 2 of each granule as an entry's first
+        int gpos = 0;
         for (int u = blockIdx.x; ok; u += gridDim.x) {
             Unit w;
             if (!read_unit_f8(ring, qi, u, w, abortv, tmo)) {
@@ -918,7 +999,15 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
                 break;
             }
             if (u < 0) break;
+            const int nbp = granules_for(w.n);
+            int gn = granule_start<GB>(gpos, nbp);
             for (int kb = 0; kb < w.kb; ++kb, ++seq) {
+                // every K block's entry, the other group's too, to keep the parities
+                const int g0 = gn;
+                const uint32_t phb = (fpar >> g0) & 1u;
+                fpar ^= 1u << g0;
+                gn += nbp;
+                if (gn == GB) gn = 0;
                 if ((seq & 1) != grp) continue;
                 const int stage = seq % STAGES;
                 const uint32_t phase = (seq / STAGES) & 1u;
@@ -955,15 +1044,14 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
                 tc::tmem_st64(lane_base + static_cast<uint32_t>(f8_a_column(NCH) + 64 * stage), h);
                 tc::fence_before_sync();
                 // the K block's token rows have landed before the MMA warps may read them
-                const int bslot = seq % SBRd;
-                const uint32_t phb = (seq / SBRd) & 1u;
-                if (!__all_sync(0xffffffffu, lane != 0 || tc::mbar_wait(&fullB[bslot], phb, abortv, tmo))) {
+                if (!__all_sync(0xffffffffu, lane != 0 || tc::mbar_wait(&fullB[g0], phb, abortv, tmo))) {
                     ok = false;
-                    if (lane == 0) record_timeout(p.err, 10, u, kb, bslot, phb, n_units, w.n);
+                    if (lane == 0) record_timeout(p.err, 10, u, kb, g0, 0, n_units, w.n);
                     break;
                 }
                 if (lane == 0) tc::mbar_arrive(&conv[stage]);
             }
+            gpos = gn;
         }
         if (!ok && lane == 0) {
             *abort_flag = 1;

@@ -23,7 +23,9 @@ enum GemmMode { kGateUp = 0, kDown = 1, kLmHead = 2, kExperts = 3, kExpertsF8 = 
 // SwiGLU output stored as f16.
 struct TensorMaps {
     CUtensorMap a[4];
-    CUtensorMap b[2];
+    // token rows: [0] gathered rows, [1] SwiGLU rows, in 16-row boxes; the FP8 expert launch
+    // also [2], [3] in 32-row and [4], [5] in 64-row boxes
+    CUtensorMap b[6];
 };
 
 struct GemmParams {

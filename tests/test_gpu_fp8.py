@@ -114,12 +114,15 @@ def test_fp8_batched():
     check_ffn(W.LAYER_FP8, 16, 0.9, tag="x_batched")
 
 
-def test_fp8_layer_step():
-    """One FP8 layer + LM head through block_decode_step (bf16 router, norm and LM head)."""
+@pytest.mark.parametrize("corr", [0.0, 0.9])
+def test_fp8_layer_step(corr):
+    """One FP8 layer + LM head through block_decode_step (bf16 router, norm and LM head).
+    corr = 0.9: the block's tokens share a hidden component, so routed experts get up to 32
+    tokens (token-row entries of one and two 16-token granules mixed in the launch's ring)."""
     cfg = W.LAYER_FP8
     lay = W.device_layer(cfg, 0)
     Wlm_d = W.device_lm_head(cfg)
-    h0 = W.host_h0(cfg, 1)
+    h0 = W.host_h0(cfg, 1, correlation=corr)
     masked0 = W.masked_subset(cfg, 1)
     d = dims_of(cfg)
     ws = ms.workspace(d, 1)
@@ -148,7 +151,7 @@ def test_fp8_layer_step():
                                      router_kind(cfg.H, cfg.E, cfg.dtype), np_(idx)[0])
     assert amb == 0
     err = max_rel(np_(h_out) - h0, h - h0)
-    print(f"fp8 layer step: MoE update max rel err {err:.3e}")
+    print(f"fp8 layer step (corr {corr}): MoE update max rel err {err:.3e}")
     assert err <= FP8_TOL
     assert max_rel(np_(hidden), hid) <= BF16_TOL
     assert np.abs(np_(conf) - oc).max() < 1e-2
