@@ -72,7 +72,7 @@ constexpr int kSmemBudget = 232448 - 1024 - 512;
 
 __host__ __device__ constexpr int stage_bytes(int nch) { return kABytes + nch * 128; }
 __host__ __device__ constexpr int num_stages(int nch) {
-    return (kSmemBudget / stage_bytes(nch)) > 10 ? 10 : (kSmemBudget / stage_bytes(nch));
+    return (kSmemBudget / stage_bytes(nch)) > 11 ? 11 : (kSmemBudget / stage_bytes(nch));
 }
 __host__ __device__ constexpr int smem_bytes(int nch) { return num_stages(nch) * stage_bytes(nch) + 512 + 1024; }
 
