@@ -211,6 +211,24 @@ def aligned(a, perm) -> np.ndarray:
     return np.take_along_axis(np.asarray(a), perm, axis=1)
 
 
+def assert_ranked_equal(got, cs: oracle.CoresetResult, r: int, tol: float = 1e-5, where=None):
+    """The kept experts of request r in ranking order against the oracle's: the same set, and
+    the same order except within runs of experts whose aggregated masses lie within
+    tol * total of each other (their order is an fp32 decision on computed masses)."""
+    want = list(cs.sel[r])
+    got = [int(e) for e in got]
+    assert sorted(got) == sorted(want), (where, "kept set")
+    agg = cs.agg[r]
+    total = sum(agg.values()) or 1
+    i = 0
+    while i < len(want):        # one run of near-equal aggregates at a time
+        j = i + 1
+        while j < len(want) and abs(agg[want[j - 1]] - agg[want[j]]) <= tol * total:
+            j += 1
+        assert sorted(got[i:j]) == sorted(want[i:j]), (where, i, got[i:j], want[i:j])
+        i = j
+
+
 def coreset_margin(cs: oracle.CoresetResult) -> float:
     """Smallest relative distance between a request's target and the cumulative sums
     around its cut (how much the masses may move before the kept set changes)."""

@@ -206,11 +206,12 @@ def stack8():
 
 
 def test_fp8_stack_full_step_teacher_forced(stack8):
-    """All 40 FP8 layers in one call, the FP8 benchmark's configuration: every 8th layer and
-    the last against the oracle fed the GPU's own layer input (and the dequantised weights),
-    the LM head and commit from the GPU's final hidden state.  The update bound is the bf16
-    one (the FP8 path rounds its SwiGLU rows to f16, finer)."""
-    from tests.test_gpu_step import Step, check_commit, check_layer
+    """All 40 FP8 layers in one call, the FP8 benchmark's configuration, against the oracle
+    fed the GPU's own layer input: every layer's routing and coreset; the MoE update (with
+    the dequantised weights) of every 8th layer and the last; the LM head and commit from
+    the GPU's final hidden state.  The update bound is the bf16 one (the FP8 path rounds its
+    SwiGLU rows to f16, finer)."""
+    from tests.test_gpu_step import Step, check_commit, check_layer, check_routing
     cfg, layers, Wlm_d, Wlm = stack8
     h0 = W.host_h0(cfg, 1)
     masked0 = W.masked_subset(cfg, 1)
@@ -220,8 +221,9 @@ def test_fp8_stack_full_step_teacher_forced(stack8):
     st.run(layers, Wlm_d, 0.9, t(h0), tokens, masked)
     np.testing.assert_array_equal(np_(st.h[0]), h0)
     ambiguous = 0
-    for l in list(range(0, cfg.n_layers - 1, 8)) + [cfg.n_layers - 1]:
+    full = set(range(0, cfg.n_layers - 1, 8)) | {cfg.n_layers - 1}
+    for l in range(cfg.n_layers):
         last = np_(st.h_out).astype(np.float64) if l == cfg.n_layers - 1 else None
-        ambiguous += check_layer(cfg, l, st, 0.9, last_h=last)
+        ambiguous += check_layer(cfg, l, st, 0.9, last_h=last) if l in full else check_routing(cfg, l, st, 0.9)[3]
     assert ambiguous <= 2
     check_commit(cfg, st, Wlm, np_(tokens), np_(masked), masked0)

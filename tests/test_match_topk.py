@@ -11,7 +11,8 @@ import pytest
 import oracle
 import synth
 from synth import workloads as W
-from tests.helpers import (SWAP_LOG, _tc_order, aligned, dot_error_bound, match_topk, router_kind, topk_margin_ok)
+from tests.helpers import (SWAP_LOG, _tc_order, aligned, assert_ranked_equal, dot_error_bound, match_topk, router_kind,
+                           topk_margin_ok)
 
 
 def test_exact_order_is_identity():
@@ -105,3 +106,20 @@ def test_router_kind_mirrors_the_dispatch_rule():
     assert router_kind(256, 16, "f32") == "ffma"
     assert router_kind(256, 64, "bf16") == "ffma"      # H % 512 != 0
     assert router_kind(512, 48, "bf16") == "ffma"      # E % 32 != 0
+
+
+def _cs(sel, agg):
+    return oracle.CoresetResult(np.array([len(sel)]), [sel], None, None, [sel], [agg], [None])
+
+
+def test_ranked_equal_allows_swaps_only_within_near_ties():
+    agg = {3: 1000, 5: 600, 7: 599, 9: 100}          # 5 and 7 within 1e-3 of the total (2299)
+    cs = _cs([3, 5, 7, 9], agg)
+    assert_ranked_equal([3, 5, 7, 9], cs, 0, tol=1e-3)
+    assert_ranked_equal([3, 7, 5, 9], cs, 0, tol=1e-3)
+    with pytest.raises(AssertionError):                 # the same swap with a tighter window
+        assert_ranked_equal([3, 7, 5, 9], cs, 0, tol=1e-4)
+    with pytest.raises(AssertionError):                 # a decided order swapped
+        assert_ranked_equal([5, 3, 7, 9], cs, 0, tol=1e-3)
+    with pytest.raises(AssertionError):                 # a different kept set
+        assert_ranked_equal([3, 5, 7, 11], cs, 0, tol=1e-3)
