@@ -35,10 +35,11 @@
 //               (128-byte swizzle), one per K block; a slot is free again as
 //               soon as its converters have read it into registers.
 //   warp 15     TMA producer of the B ring: each K block's token rows (f16) in
-//               one 4 KiB granule per 16 tokens, contiguous, so one MMA covers
-//               all of a unit's tokens; a ring of 12-16 granules (the rows land
-//               well before their stage comes round); a granule is free again
-//               at its MMAs' commit.
+//               an entry of 1, 2 or 4 consecutive 4 KiB granules of 16 tokens
+//               (one copy per K half), so one MMA covers all of a unit's tokens;
+//               a ring of 12 granules (24 at 64-token chunks), so the rows land
+//               well before their stage comes round; an entry is free again at
+//               its MMAs' commit.
 //   warps 6-13  converters, two groups of four on alternate K blocks: each
 //               warp turns the 32 tile rows of its TMEM lane quarter into f16
 //               (exact, one conversion instruction per pair) and stores them with tcgen05.st
