@@ -571,9 +571,10 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
                 }
                 return true;
             };
-            const bool kok = nbp == 1   ? kblocks(std::integral_constant<int, 1>{})
-                             : nbp == 2 ? kblocks(std::integral_constant<int, 2>{})
-                                        : kblocks(std::integral_constant<int, 4>{});
+            // (entries of 4 granules only at 64-token chunks)
+            const bool kok = nbp == 1                 ? kblocks(std::integral_constant<int, 1>{})
+                             : (NCH <= 32 || nbp == 2) ? kblocks(std::integral_constant<int, 2>{})
+                                                       : kblocks(std::integral_constant<int, NCH <= 32 ? 2 : 4>{});
             if (!kok) {
                 ok = false;
                 break;
@@ -740,10 +741,10 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
                 };
                 if (nbp == 1)
                     kblocks(std::integral_constant<int, 1>{});
-                else if (nbp == 2)
+                else if (NCH <= 32 || nbp == 2)  // (entries of 4 granules only at 64-token chunks)
                     kblocks(std::integral_constant<int, 2>{});
                 else
-                    kblocks(std::integral_constant<int, 4>{});
+                    kblocks(std::integral_constant<int, NCH <= 32 ? 2 : 4>{});
                 if (!good) {
                     ok = false;
                     break;
