@@ -298,37 +298,6 @@ __device__ __forceinline__ bool read_unit(const UnitRing& r, int& qi, int& u, vo
     return __shfl_sync(0xffffffffu, good, 0) != 0;
 }
 
-// FP8 launch: the producer also decodes the unit and publishes it decoded, so the MMA
-// warps, which bound that launch, and the other roles spend no chunk-list read per unit
-// (in the bf16 launch every warp decodes the index itself, in parallel with the others).
-template <int MODE, int NCH>
-__device__ __forceinline__ bool take_unit_f8(const UnitRing& r, const GemmParams& p, int nrc, int nsc, int n_units,
-                                             int& qi, int& u, Unit& w, volatile int* abort, uint64_t tmo) {
-    const int e = qi % kUnitQ;
-    int good = 1;
-    if ((threadIdx.x & 31) == 0) {
-        good = tc::mbar_wait(&r.empty[e], ((qi / kUnitQ) & 1) ^ 1u, abort, tmo);
-        if (good) {
-            int v = qi == 0 ? static_cast<int>(blockIdx.x) : static_cast<int>(gridDim.x) + atomicAdd(p.unit_ctr, 1);
-            if (v >= n_units) v = -1;
-            Unit d{};
-            if (v >= 0) d = decode_unit<MODE, NCH>(v, p, nrc, nsc);
-            r.ent[2 * e] = make_int4(v, d.kb, d.rowA0, d.slot0);
-            r.ent[2 * e + 1] = make_int4(d.n, d.mt, d.c, (d.shared ? 1 : 0) | (d.dn ? 2 : 0));
-            tc::mbar_arrive(&r.full[e]);
-        }
-    }
-    ++qi;
-    good = __shfl_sync(0xffffffffu, good, 0);
-    __syncwarp();  // lane 0's entry, read back by every lane
-    if (good) {
-        const int4 a = r.ent[2 * e], b = r.ent[2 * e + 1];
-        u = a.x;
-        w = Unit{a.y, a.z, a.z + 64, a.w, b.x, b.y, b.z, (b.w & 1) != 0, (b.w & 2) != 0};
-    }
-    return good != 0;
-}
-
 // FP8 reader warp: the next unit, decoded (u = -1: none left); false if the wait gave up.
 __device__ __forceinline__ bool read_unit_f8(const UnitRing& r, int& qi, int& u, Unit& w, volatile int* abort,
                                              uint64_t tmo) {
@@ -458,44 +427,46 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
     if (F8 && warp == 0) {
         // ------------------------------------------------------------ FP8 weight-tile producer
         // Fills the A ring in unit / K-block order; needs nothing from other CTAs, so a down
-        // unit's tiles stream in while its chunk's SwiGLU rows are still being written.
-        const uint64_t pol = tc::policy_evict_first();
-        uint32_t issued = 0, issued_parity = 0;
-        constexpr int SAd = SA > 0 ? SA : 1;
-        int seq = 0;
-        bool ok = true;
-        int qi = 0;
-        for (int u = blockIdx.x; ok; u += gridDim.x) {
-            Unit w;
-            if (!take_unit_f8<MODE, NCH>(ring, p, nrc, nsc, n_units, qi, u, w, abortv, tmo)) {
-                ok = false;
-                if (lane == 0) record_timeout(p.err, 7, u, -1, -1, 0, n_units, 0);
-                break;
-            }
-            if (u < 0) break;
-            const CUtensorMap* mA = &maps.a[(w.dn ? 2 : 0) + (w.shared ? 1 : 0)];
-            for (int kb = 0; kb < w.kb; ++kb, ++seq) {
-                const int slot = seq % SAd;
-                const uint32_t ph = (seq / SAd) & 1u;
-                int good = 1;
-                if (lane == 0) {
-                    good = tc::mbar_wait(&emptyA[slot], ph ^ 1u, abortv, tmo);
-                    if (good) {
-                        tc::mbar_arrive_expect_tx(&fullA[slot], kF8Tile);
-                        tc::tma_load_2d_hint(aring + slot * kF8Tile, mA, &fullA[slot], kb * 128, w.rowA0, pol);
-                        issued |= 1u << slot;
-                        issued_parity = (issued_parity & ~(1u << slot)) | (ph << slot);
-                    }
-                }
-                good = __shfl_sync(0xffffffffu, good, 0);
-                if (!good) {
+        // unit's tiles stream in while its chunk's SwiGLU rows are still being written.  Lane 0
+        // alone runs the role: it takes each unit (a CTA's first unit is its block index, the
+        // rest come from the global counter), decodes it and publishes it decoded in the unit
+        // ring for the other roles.
+        if (lane == 0) {
+            const uint64_t pol = tc::policy_evict_first();
+            uint32_t issued = 0, issued_parity = 0;
+            constexpr int SAd = SA > 0 ? SA : 1;
+            int seq = 0;
+            bool ok = true;
+            for (int qi = 0; ok; ++qi) {
+                const int e = qi % kUnitQ;
+                if (!tc::mbar_wait(&ring.empty[e], ((qi / kUnitQ) & 1) ^ 1u, abortv, tmo)) {
                     ok = false;
-                    if (lane == 0) record_timeout(p.err, 1, u, kb, slot, ph, n_units, w.n);
+                    record_timeout(p.err, 7, -1, -1, -1, 0, n_units, 0);
                     break;
                 }
+                int u = qi == 0 ? static_cast<int>(blockIdx.x) : static_cast<int>(gridDim.x) + atomicAdd(p.unit_ctr, 1);
+                if (u >= n_units) u = -1;
+                Unit w{};
+                if (u >= 0) w = decode_unit<MODE, NCH>(u, p, nrc, nsc);
+                ring.ent[2 * e] = make_int4(u, w.kb, w.rowA0, w.slot0);
+                ring.ent[2 * e + 1] = make_int4(w.n, w.mt, w.c, (w.shared ? 1 : 0) | (w.dn ? 2 : 0));
+                tc::mbar_arrive(&ring.full[e]);
+                if (u < 0) break;
+                const CUtensorMap* mA = &maps.a[(w.dn ? 2 : 0) + (w.shared ? 1 : 0)];
+                for (int kb = 0; kb < w.kb; ++kb, ++seq) {
+                    const int slot = seq % SAd;
+                    const uint32_t ph = (seq / SAd) & 1u;
+                    if (!tc::mbar_wait(&emptyA[slot], ph ^ 1u, abortv, tmo)) {
+                        ok = false;
+                        record_timeout(p.err, 1, u, kb, slot, ph, n_units, w.n);
+                        break;
+                    }
+                    tc::mbar_arrive_expect_tx(&fullA[slot], kF8Tile);
+                    tc::tma_load_2d_hint(aring + slot * kF8Tile, mA, &fullA[slot], kb * 128, w.rowA0, pol);
+                    issued |= 1u << slot;
+                    issued_parity = (issued_parity & ~(1u << slot)) | (ph << slot);
+                }
             }
-        }
-        if (lane == 0) {
             if (!ok) {
                 *abort_flag = 1;
                 record_error(p.err, kErrTimeoutProducer);
@@ -508,80 +479,68 @@ __global__ void __launch_bounds__(MODE == kExpertsF8 ? kThreadsF8 : kThreads, 1)
         // ------------------------------------------------------------ FP8 token-row producer
         // Fills the B ring in the same order, a granule once the MMAs that read it completed; a
         // down unit's SwiGLU rows once its chunk's gate/up epilogues (any CTA) counted them stored.
-        // One copy of 16, 32 or 64 rows per half-ring and K block.
-        uint32_t issued = 0, issued_parity = 0;
-        uint32_t epar = 0, fpar = 0;  // use counts mod 2: per granule, per first granule of an entry
-        int gpos = 0;
-        bool ok = true;
-        int qi = 0;
-        for (int u = blockIdx.x; ok; u += gridDim.x) {
-            Unit w;
-            if (!read_unit_f8(ring, qi, u, w, abortv, tmo)) {
-                ok = false;
-                break;
-            }
-            if (u < 0) break;
-            const int nbp = granules_for(w.n);
-            int g0 = granule_start<GB>(gpos, nbp);
-            const CUtensorMap* mB = &maps.b[(w.dn ? 1 : 0) + (nbp & 6)];  // boxes of 16 nbp rows
-            int good = 1;
-            if (w.dn) {
-                if (lane == 0)
-                    good = wait_count(&p.done[w.c], 4 * (w.shared ? p.shared_tiles : p.routed_tiles), abortv, tmo);
-                good = __shfl_sync(0xffffffffu, good, 0);
-                if (!good) {
+        // One copy of 16, 32 or 64 rows per half-ring and K block.  Lane 0 alone runs the role,
+        // unit reads included (no warp-wide step per K block: its loop paces the token rows).
+        if (lane == 0) {
+            uint32_t issued = 0, issued_parity = 0;
+            uint32_t epar = 0, fpar = 0;  // use counts mod 2: per granule, per first granule of an entry
+            int gpos = 0;
+            bool ok = true;
+            for (int qi = 0;;) {
+                const int e = qi % kUnitQ;
+                if (!tc::mbar_wait(&ring.full[e], (qi / kUnitQ) & 1, abortv, tmo)) {
                     ok = false;
-                    if (lane == 0) record_timeout(p.err, 6, u, -1, -1, 0, n_units, w.n);
                     break;
                 }
-            }
-            // the unit's K blocks with the entry size a constant (one granule nearly always)
-            auto kblocks = [&](auto nbp_c) -> bool {
-                constexpr int NBP = decltype(nbp_c)::value;
-                for (int kb = 0; kb < w.kb; ++kb) {
-                    int gbad = -1;
-                    if (lane == 0) {
+                ++qi;
+                const int4 ea = ring.ent[2 * e], eb = ring.ent[2 * e + 1];
+                tc::mbar_arrive(&ring.empty[e]);
+                const int u = ea.x;
+                if (u < 0) break;
+                const Unit w{ea.y, ea.z, ea.z + 64, ea.w, eb.x, eb.y, eb.z, (eb.w & 1) != 0, (eb.w & 2) != 0};
+                const int nbp = granules_for(w.n);
+                int g0 = granule_start<GB>(gpos, nbp);
+                const CUtensorMap* mB = &maps.b[(w.dn ? 1 : 0) + (nbp & 6)];  // boxes of 16 nbp rows
+                if (w.dn && !wait_count(&p.done[w.c], 4 * (w.shared ? p.shared_tiles : p.routed_tiles), abortv, tmo)) {
+                    ok = false;
+                    record_timeout(p.err, 6, u, -1, -1, 0, n_units, w.n);
+                    break;
+                }
+                // the unit's K blocks with the entry size a constant (one granule nearly always)
+                auto kblocks = [&](auto nbp_c) -> bool {
+                    constexpr int NBP = decltype(nbp_c)::value;
+                    for (int kb = 0; kb < w.kb; ++kb) {
 #pragma unroll
                         for (int j = 0; j < NBP; ++j) {
                             const int g = g0 + j;
-                            if (good && !tc::mbar_wait(&emptyB[g], ((epar >> g) & 1u) ^ 1u, abortv, tmo)) {
-                                good = 0;
-                                gbad = g;
+                            if (!tc::mbar_wait(&emptyB[g], ((epar >> g) & 1u) ^ 1u, abortv, tmo)) {
+                                record_timeout(p.err, 1, u, kb, g, 0, n_units, w.n);
+                                return false;
                             }
                         }
-                        if (good) {
-                            const uint32_t ph = (fpar >> g0) & 1u;
-                            tc::mbar_arrive_expect_tx(&fullB[g0], NBP * kGranule);
-                            tc::tma_load_2d(bring + g0 * kGranuleHalf, mB, &fullB[g0], kb * 128, w.slot0);
-                            tc::tma_load_2d(bring + (GB + g0) * kGranuleHalf, mB, &fullB[g0], kb * 128 + 64,
-                                            w.slot0);
-                            issued |= 1u << g0;
-                            issued_parity = (issued_parity & ~(1u << g0)) | (ph << g0);
-                        }
+                        const uint32_t ph = (fpar >> g0) & 1u;
+                        tc::mbar_arrive_expect_tx(&fullB[g0], NBP * kGranule);
+                        tc::tma_load_2d(bring + g0 * kGranuleHalf, mB, &fullB[g0], kb * 128, w.slot0);
+                        tc::tma_load_2d(bring + (GB + g0) * kGranuleHalf, mB, &fullB[g0], kb * 128 + 64, w.slot0);
+                        issued |= 1u << g0;
+                        issued_parity = (issued_parity & ~(1u << g0)) | (ph << g0);
+                        epar ^= ((1u << NBP) - 1u) << g0;
+                        fpar ^= 1u << g0;
+                        g0 += NBP;
+                        if (g0 == GB) g0 = 0;
                     }
-                    epar ^= ((1u << NBP) - 1u) << g0;
-                    fpar ^= 1u << g0;
-                    g0 += NBP;
-                    if (g0 == GB) g0 = 0;
-                    good = __shfl_sync(0xffffffffu, good, 0);
-                    if (!good) {
-                        if (lane == 0) record_timeout(p.err, 1, u, kb, gbad, 0, n_units, w.n);
-                        return false;
-                    }
+                    return true;
+                };
+                // (entries of 4 granules only at 64-token chunks)
+                const bool kok = nbp == 1                 ? kblocks(std::integral_constant<int, 1>{})
+                                 : (NCH <= 32 || nbp == 2) ? kblocks(std::integral_constant<int, 2>{})
+                                                           : kblocks(std::integral_constant<int, NCH <= 32 ? 2 : 4>{});
+                if (!kok) {
+                    ok = false;
+                    break;
                 }
-                return true;
-            };
-            // (entries of 4 granules only at 64-token chunks)
-            const bool kok = nbp == 1                 ? kblocks(std::integral_constant<int, 1>{})
-                             : (NCH <= 32 || nbp == 2) ? kblocks(std::integral_constant<int, 2>{})
-                                                       : kblocks(std::integral_constant<int, NCH <= 32 ? 2 : 4>{});
-            if (!kok) {
-                ok = false;
-                break;
+                gpos = g0;
             }
-            gpos = g0;
-        }
-        if (lane == 0) {
             if (!ok) {
                 *abort_flag = 1;
                 record_error(p.err, kErrTimeoutProducer);
